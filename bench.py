@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the tiled tensor-core GEMM (one JSON line on stdout).
+
+Default workload: bf16 GEMM 8192 x 8192 x 8192, A row-major, B column-major,
+alpha = 1, beta = 0, fp32 accumulation, bf16 out; A, B i.i.d. uniform[-1, 1]
+(SplitMix64 stream, seed 1).  One step = one ttc_gemm call (the whole hot
+path: tile scheduling, TMA staging, tcgen05 mainloop, fused epilogue).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ttc|reference]
+
+--impl reference times the CPU oracle (the plain triple loop) on the host
+cores, on a bounded sample of the same workload, in the same metric.
+For N > 1 (torchrun) each rank runs an independent replica (the GEMM has no
+exchange step); the value is the work of all ranks over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_spec(name):
+    import synth
+    if name in synth.WORKLOADS:
+        return dict(synth.WORKLOADS[name])
+    raise SystemExit(f"unknown workload {name}; choose from {sorted(synth.WORKLOADS)}")
+
+
+def algorithmic_bytes(spec):
+    """Bytes the GEMM must move at least once: A, B, D, plus C when beta != 0 and the bias."""
+    M, N, K = spec["M"], spec["N"], spec["K"]
+    ein = 1 if spec["dtype"] == "i8" else 2
+    eout = 4 if spec["dtype"] == "i8" else 2
+    b = (M * K + K * N) * ein + M * N * eout
+    if spec.get("beta", 0.0) != 0.0:
+        b += M * N * eout
+    if spec.get("dist_bias"):
+        b += N * 4
+    return b
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample_rate(p, spec, budget_s, threads=0):
+    """Times the oracle on a bounded sample of output elements; returns (flop/s, desc, cores)."""
+    import numpy as np
+
+    import oracle
+    alpha, beta, act = spec["alpha"], spec["beta"], spec["act"]
+    # calibrate on a small sample, then size the timed sample to ~budget_s
+    n0 = 64
+    ii = np.zeros(n0, dtype=np.int64)
+    jj = np.arange(n0, dtype=np.int64) % p.N
+    t0 = time.perf_counter()
+    _, _, used = oracle.gemm_elements(p, ii, jj, alpha=alpha, beta=beta, act=act, nthreads=threads)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(max(n0, min(p.M * p.N, n0 * budget_s / dt)))
+    rows = max(1, n // p.N)
+    n = rows * p.N if n >= p.N else n
+    ii = (np.arange(n, dtype=np.int64) // p.N) % p.M
+    jj = np.arange(n, dtype=np.int64) % p.N
+    t0 = time.perf_counter()
+    _, _, used = oracle.gemm_elements(p, ii, jj, alpha=alpha, beta=beta, act=act, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n * p.K
+    desc = f"{n} output elements ({n / p.N:.2f} rows x {p.N} cols, full K={p.K}) in {dt:.2f} s"
+    return flops / dt, desc, used, dt
+
+
+def run_reference(args, spec, name):
+    """The CPU oracle, as it stands, on a bounded sample of the workload (rank 0 only)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import synth
+    p, alpha, beta, act = synth.make(spec)
+    import oracle
+    oracle.build()
+    per_step = max(1.0, 60.0 / max(1, args.steps + args.warmup))
+    per_step = min(per_step, 10.0)
+    for _ in range(args.warmup):
+        oracle_sample_rate(p, spec, min(per_step, 2.0))
+    rates, descs, used = [], [], 0
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        r, desc, used, _ = oracle_sample_rate(p, spec, per_step)
+        rates.append(r)
+        descs.append(desc)
+    wall = time.perf_counter() - t_all
+    value = statistics.median(rates) / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[spec["dtype"]],
+        "data": "synthetic", "config": config_of(spec, name, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": used, "kind": "oracle",
+                         "sample": descs[-1] if descs else ""},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "GEMM TFLOPS (bf16 8192^3) and % of GB300 dense tensor peak, 1 GPU"
+DTYPE_NAME = {"bf16": "bf16", "f16": "f16", "i8": "int8"}
+
+
+def config_of(spec, name, world):
+    return {"workload": name, "M": spec["M"], "N": spec["N"], "K": spec["K"], "dtype": spec["dtype"],
+            "layoutA": spec["layoutA"], "layoutB": spec["layoutB"], "alpha": spec["alpha"],
+            "beta": spec["beta"], "act": spec["act"], "bias": bool(spec.get("dist_bias")),
+            "seed": spec["seed"], "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (no flush)" if algorithmic_bytes(spec) > 2 * 129e6
+            else "L2 flushed between steps"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="bf16_8192")
+    ap.add_argument("--impl", default="ttc", choices=["ttc", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    spec = workload_spec(args.workload)
+    name = args.workload
+    if args.impl == "reference":
+        return run_reference(args, spec, name)
+
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup()
+    import synth
+    import tiled_tensor_core_02_gb300 as ttc
+    from tiled_tensor_core_02_gb300 import _build
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    ttc.load()
+
+    p, alpha, beta, act = synth.make(spec)
+    M, N, K = p.M, p.N, p.K
+    flops = 2.0 * M * N * K
+    esz_out = 4 if p.dtype == "i8" else 2
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    A, B = dev(p.A), dev(p.B)
+    C = dev(p.C) if p.C is not None else None
+    bias = dev(p.bias) if p.bias is not None else None
+    D = torch.empty(M * N, dtype=torch.int32 if p.dtype == "i8" else torch.int16, device="cuda")
+    need_flush = algorithmic_bytes(spec) <= 2 * 129e6
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda") if need_flush else None
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    lay = {"row": ttc.ROW_MAJOR, "col": ttc.COL_MAJOR}
+
+    def step(Ap=A, Bp=B, Cp=C, Dp=D):
+        st = ttc.ttc_gemm(M, N, K, Ap.data_ptr(), p.lda, lay[p.layoutA], Bp.data_ptr(), p.ldb,
+                          lay[p.layoutB], Cp.data_ptr() if (Cp is not None and beta != 0.0) else None,
+                          p.ldc, Dp.data_ptr(), N, alpha, beta,
+                          bias.data_ptr() if bias is not None else None, ttc.ACT[act],
+                          ttc.DTYPE[p.dtype], s)
+        if st != 0:
+            raise ttc.TTCError(st)
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ttc.ttc_get_device_error(s) != 0:
+        raise SystemExit("device error during warm-up")
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = ttc.ttc_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    launches = ttc.ttc_launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    if ttc.ttc_get_device_error(s) != 0:
+        raise SystemExit("device error during the timed region")
+    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = t_start.elapsed_time(t_end)
+    if flush is not None:
+        total_ms = sum(kern_ms)  # the L2 flush between steps is not part of a step
+    total_ms = max_over_ranks(total_ms, world)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    avg_kernel_s = statistics.mean(kern_ms) * 1e-3
+
+    peaks, peak_src = load_peaks()
+    if p.dtype == "i8":
+        # int8 runs on the bf16 tensor pipe (exact for int8 values); same peak
+        peak = peaks["bf16_tflops"]
+    elif p.dtype == "f16":
+        peak = peaks["bf16_tflops"]  # fp16 and bf16 have the same dense tensor rate
+    else:
+        peak = peaks["bf16_tflops"]
+    achieved = flops / avg_kernel_s / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": load_traffic(name),
+                "peak_source": f"{peak_src} bf16 burst (MEASURED_PEAKS.json bf16_tflops)"
+                if peak_src == "measured" else "fallback 1.9 PFLOP/s bf16 burst",
+                "alg_bytes": algorithmic_bytes(spec),
+                "achieved_gbs": algorithmic_bytes(spec) / avg_kernel_s / 1e9,
+                "kernel_ms_median": statistics.median(kern_ms), "kernel_ms_min": min(kern_ms)}
+
+    # ---------------------------------------------------------------- end to end
+    hA = torch.empty(A.numel(), dtype=A.dtype, pin_memory=True).copy_(A)
+    hB = torch.empty(B.numel(), dtype=B.dtype, pin_memory=True).copy_(B)
+    hC = torch.empty(C.numel(), dtype=C.dtype, pin_memory=True).copy_(C) if C is not None else None
+    hD = torch.empty(D.numel(), dtype=D.dtype, pin_memory=True)
+    dA, dB = torch.empty_like(A), torch.empty_like(B)
+    dC = torch.empty_like(C) if C is not None else None
+    h2d = hA.numel() * hA.element_size() + hB.numel() * hB.element_size() + \
+        (hC.numel() * hC.element_size() if (hC is not None and beta != 0.0) else 0)
+    d2h = hD.numel() * hD.element_size()
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        if dC is not None and beta != 0.0:
+            dC.copy_(hC, non_blocking=True)
+        step(dA, dB, dC, D)
+        hD.copy_(D, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = flops * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, used, _ = oracle_sample_rate(p, spec, args.cpu_budget)
+        cpu = {"value": rate / 1e12, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": desc}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.dtype], "data": "synthetic",
+            "config": config_of(spec, name, world),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clocks,
+            "frac_of_peak": value / peak,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def load_traffic(name):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(name)
+    except (OSError, ValueError):
+        return None
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,130 @@
+/*
+ * ttc — tiled tensor-core GEMM for GB300 (sm_103a), C ABI.
+ *
+ * Computes  D = act(alpha * A * B + beta * C + bias)  on one GPU.
+ *
+ * Sources the operation follows (CUTLASS / CuTe tutorial pages):
+ *   - "CUTLASS tutorial: from hand-written GEMM to CuTe / Tensor Core kernels"
+ *     (hpc.payai.win/cutlass), section 1: the GEMM C[M,N] = A[M,K] x B[K,N]
+ *     mapped onto CTA tiles, and its Epilogue box (alpha/beta, then
+ *     bias/activation, then store);
+ *   - same page, section 2: device::Gemm is the host entry point and behaves
+ *     like cuBLAS (alpha scales A*B, beta scales the existing C);
+ *   - PitchLinearStripminedThreadMap source walkthrough (lpnh.cn/news/2469163),
+ *     sections 4.1 and 6.3: an element's address is its row times the pitch
+ *     plus its column, with the pitch taken from the tensor's layout.
+ *
+ * Storage.  A is M x K, B is K x N (logical).  TTC_ROW_MAJOR places element
+ * (i, j) at i * ld + j; TTC_COL_MAJOR places it at i + j * ld.  C and D are
+ * M x N, row-major, with leading dimensions ldc and ldd.  For TTC_F16 and
+ * TTC_BF16, C and D have the input type and the product is accumulated in
+ * fp32.  For TTC_I8, A and B are int8 and C and D are int32; the result is
+ * exact.  bias is fp32[N] (added per output column) or NULL.
+ *
+ * Ownership.  Every pointer is caller-owned device memory.  The library keeps
+ * no reference to any of it after the call returns and allocates no device
+ * memory on this path.
+ *
+ * Asynchrony.  ttc_gemm only enqueues work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and returns.  Calls on different host threads
+ * are safe.
+ *
+ * Errors.  Every entry point returns a status; none aborts or throws.
+ *   TTC_ERR_INVALID_ARG: negative sizes; a leading dimension below the
+ *     contiguous extent (A row-major lda < K, column-major lda < M; B
+ *     row-major ldb < N, column-major ldb < K; ldc < N when C is read;
+ *     ldd < N); NULL A or B when M*N*K > 0; NULL D when M*N > 0; NULL C with
+ *     beta != 0; D overlapping C other than exactly in place (D == C and
+ *     ldd == ldc); an unknown enum value.
+ *   TTC_ERR_UNSUPPORTED: TTC_I8 with bias, act != NONE, alpha != 1 or beta
+ *     not in {0, 1}; a size or leading dimension beyond 2^31 - 1 elements.
+ *   TTC_ERR_CUDA: a CUDA runtime or driver call failed (launch, device query).
+ *   TTC_ERR_TIMEOUT: returned by ttc_get_device_error when a kernel's bounded
+ *     wait ran out; the kernel then ended early and D is undefined.
+ * M == 0 or N == 0 is a no-op returning TTC_OK.  K == 0 gives
+ * D = act(beta * C + bias).  beta == 0 never reads C (NaNs in C do not
+ * propagate).
+ */
+#ifndef TTC_H_
+#define TTC_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TTC_OK = 0,
+  TTC_ERR_INVALID_ARG = 1,
+  TTC_ERR_UNSUPPORTED = 2,
+  TTC_ERR_CUDA = 3,
+  TTC_ERR_TIMEOUT = 4
+} ttc_status;
+
+typedef enum { TTC_ROW_MAJOR = 0, TTC_COL_MAJOR = 1 } ttc_layout;
+
+typedef enum { TTC_ACT_NONE = 0, TTC_ACT_RELU = 1, TTC_ACT_GELU_TANH = 2 } ttc_act;
+
+typedef enum { TTC_F16 = 0, TTC_BF16 = 1, TTC_I8 = 2 } ttc_dtype;
+
+/*
+ * D = act(alpha * A * B + beta * C + bias).  See the file comment for the
+ * meaning, layout, ownership and error behaviour of every argument.
+ * act: NONE, RELU = max(v, 0), GELU_TANH = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).
+ * stream: a cudaStream_t passed as void*.
+ */
+ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda, ttc_layout layoutA,
+                    const void* B, int64_t ldb, ttc_layout layoutB,
+                    const void* C, int64_t ldc,
+                    void* D, int64_t ldd,
+                    float alpha, float beta, const float* bias,
+                    ttc_act act, ttc_dtype dtype, void* stream);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device error word that
+ * the library's kernels set when a bounded wait runs out (TTC_ERR_TIMEOUT), or
+ * TTC_OK.  A CUDA error seen while synchronizing is returned as TTC_ERR_CUDA.
+ * The word is per device, shared by all streams.
+ */
+ttc_status ttc_get_device_error(void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* ttc_status_string(ttc_status status);
+
+/*
+ * Debug and test knobs (not needed for normal use).  Process-wide; read at
+ * every ttc_gemm call.
+ *   TTC_KNOB_TIMEOUT_NS: budget of every in-kernel barrier wait (default
+ *     2e9 ns); values <= 0 restore the default.
+ *   TTC_KNOB_INJECT_STALL: when 1, the next kernels make their tensor-core
+ *     issuer wait on a barrier that nothing arrives at, so every wait runs
+ *     out; used to test that a stalled pipeline ends with TTC_ERR_TIMEOUT
+ *     instead of hanging.
+ *   TTC_KNOB_FORCE_GENERIC_LOAD: when 1, operands are staged with plain
+ *     loads even when TMA could describe them.
+ *   TTC_KNOB_FORCE_GENERIC_STORE: when 1, results are written with plain
+ *     predicated stores even when TMA could describe D.
+ *   TTC_KNOB_TILE_N: force the CTA tile width (256, 128, 64, 32 or 16); 0
+ *     lets the planner choose.
+ * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
+ */
+typedef enum {
+  TTC_KNOB_TIMEOUT_NS = 0,
+  TTC_KNOB_INJECT_STALL = 1,
+  TTC_KNOB_FORCE_GENERIC_LOAD = 2,
+  TTC_KNOB_FORCE_GENERIC_STORE = 3,
+  TTC_KNOB_TILE_N = 4
+} ttc_knob;
+
+ttc_status ttc_set_knob(ttc_knob knob, int64_t value);
+
+/* Number of kernel launches ttc_gemm has enqueued in this process. */
+int64_t ttc_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TTC_H_ */

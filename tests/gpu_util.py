@@ -1,0 +1,46 @@
+"""Helpers shared by the GPU tests: upload a synth.Problem, run the C ABI, read back."""
+import numpy as np
+import torch
+
+import tiled_tensor_core_02_gb300 as ttc
+
+LAY = {"row": ttc.ROW_MAJOR, "col": ttc.COL_MAJOR}
+
+
+def to_dev(buf):
+    if buf is None:
+        return None
+    a = np.ascontiguousarray(buf)
+    if a.dtype == np.uint16:
+        a = a.view(np.int16)
+    if a.size == 0:
+        a = np.zeros(1, dtype=a.dtype)
+    return torch.from_numpy(a).cuda()
+
+
+def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_dev=None,
+        expect=0, stream=None):
+    """Runs ttc_gemm on problem p; returns the M x N output (storage type) as numpy."""
+    out_np = np.int32 if p.dtype == "i8" else np.int16
+    ldd = p.N if ldd is None else ldd
+    A = to_dev(p.A)
+    B = to_dev(p.B)
+    C = C_dev if C_dev is not None else (to_dev(p.C) if p.C is not None else None)
+    bias = to_dev(p.bias) if (use_bias and p.bias is not None) else None
+    if D is None:
+        D = torch.full((max(p.M * ldd, 1),), -1, dtype=torch.int32 if out_np == np.int32 else torch.int16,
+                       device="cuda")
+    s = torch.cuda.current_stream().cuda_stream if stream is None else stream
+    st = ttc.ttc_gemm(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA], B.data_ptr(), p.ldb,
+                      LAY[p.layoutB], C.data_ptr() if (C is not None and beta != 0.0) else None,
+                      p.ldc, D.data_ptr(), ldd, alpha, beta,
+                      bias.data_ptr() if bias is not None else None, ttc.ACT[act], ttc.DTYPE[p.dtype], s)
+    assert st == expect, ttc.STATUS.get(st, st)
+    if st != 0:
+        return None
+    err = ttc.ttc_get_device_error(s)
+    assert err == 0, ttc.STATUS.get(err, err)
+    d = D.cpu().numpy()
+    if out_np == np.int16:
+        d = d.view(np.uint16)
+    return d[: p.M * ldd].reshape(p.M, ldd)[:, : p.N] if p.M else d[:0].reshape(0, p.N)

@@ -1,0 +1,92 @@
+"""CPU-side checks of the C ABI: the library builds and loads, exports every
+symbol include/ttc.h declares, and rejects bad arguments before touching a GPU."""
+import os
+import re
+
+import pytest
+
+import tiled_tensor_core_02_gb300 as ttc
+from tiled_tensor_core_02_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return ttc.load()
+
+
+def declared_symbols():
+    names = set()
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(ttc_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert names, "no declarations found"
+    assert names == set(ttc.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in ttc.STATUS.items():
+        assert ttc.ttc_status_string(code) == name
+
+
+def test_knobs_validate(lib):
+    assert ttc.ttc_set_knob("tile_n", 128) == 0
+    assert ttc.ttc_set_knob("tile_n", 100) == 1
+    assert ttc.ttc_set_knob("tile_n", 0) == 0
+    assert ttc.ttc_set_knob("inject_stall", 2) == 1
+    assert ttc.ttc_set_knob(99, 0) == 1
+
+
+BF16 = ttc.DTYPE["bf16"]
+I8 = ttc.DTYPE["i8"]
+R, C = ttc.ROW_MAJOR, ttc.COL_MAJOR
+P = 1 << 20  # a fake, never-dereferenced address: these calls must fail before any GPU work
+
+
+def call(M=64, N=64, K=64, A=P, lda=None, la=R, B=P, ldb=None, lb=C, Cp=None, ldc=None, D=P * 2,
+         ldd=None, alpha=1.0, beta=0.0, bias=None, act=0, dtype=BF16):
+    lda = (K if la == R else M) if lda is None else lda
+    ldb = (N if lb == R else K) if ldb is None else ldb
+    ldc = N if ldc is None else ldc
+    ldd = N if ldd is None else ldd
+    return ttc.ttc_gemm(M, N, K, A, lda, la, B, ldb, lb, Cp, ldc, D, ldd, alpha, beta, bias, act,
+                        dtype, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(M=-1), dict(N=-2), dict(K=-3),
+    dict(la=5), dict(lb=7), dict(act=9), dict(dtype=9),
+    dict(lda=63), dict(la=C, lda=63), dict(ldb=63), dict(lb=R, ldb=63), dict(ldd=63),
+    dict(A=None), dict(B=None), dict(D=None),
+    dict(beta=1.0, Cp=None), dict(beta=1.0, Cp=P * 4, ldc=63),
+    dict(beta=1.0, Cp=P * 2 + 2, D=P * 2),       # partial overlap of C and D
+    dict(beta=1.0, Cp=P * 2, ldc=96, D=P * 2),    # same base, different pitch
+])
+def test_invalid_arguments(lib, kw):
+    assert call(**kw) == 1
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype=I8, bias=P), dict(dtype=I8, act=1), dict(dtype=I8, alpha=2.0),
+    dict(dtype=I8, beta=0.5, Cp=P * 4),
+    dict(M=1 << 31),
+])
+def test_unsupported_combinations(lib, kw):
+    assert call(**kw) == 2
+
+
+def test_empty_problems_are_noops(lib):
+    assert call(M=0) == 0
+    assert call(N=0) == 0
+    assert call(M=0, A=None, B=None, D=None) == 0

@@ -1,0 +1,201 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Floating outputs must lie within the oracle's per-element tolerance (see
+oracle/__init__.py); int8 -> int32 must be bit-exact.  Sizes the oracle can
+finish in seconds are compared element by element; the full-size workloads
+are compared on sampled rows, columns and elements (and with a Freivalds
+check where the epilogue is linear).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tiled_tensor_core_02_gb300 as ttc
+from gpu_util import run, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from tiled_tensor_core_02_gb300 import _build
+    _build.build()
+    ttc.load()
+    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n"):
+        ttc.ttc_set_knob(k, 0)
+    yield
+
+
+def check_full(p, d, alpha, beta, act="none", use_bias=True):
+    r, sabs = oracle.gemm_full(p, alpha=alpha, beta=beta, act=act, use_bias=use_bias)
+    if p.dtype == "i8":
+        assert np.array_equal(d.astype(np.int64), r.astype(np.int64))
+        return 0.0
+    ok, worst, w = oracle.check_float(oracle.decode(d.ravel(), p.dtype), r.ravel(), sabs.ravel(), p.dtype)
+    assert ok, f"worst error ratio {worst:.3f} at {divmod(w, p.N)}: got {oracle.decode(d.ravel()[w:w+1], p.dtype)} want {r.ravel()[w]}"
+    return worst
+
+
+def check_sampled(p, d, alpha, beta, act="none", seed=0):
+    ii, jj = oracle.sample_indices(p.M, p.N, seed)
+    r, sabs, _ = oracle.gemm_elements(p, ii, jj, alpha=alpha, beta=beta, act=act)
+    got = d[ii, jj]
+    if p.dtype == "i8":
+        assert np.array_equal(got.astype(np.int64), r.astype(np.int64))
+        return
+    ok, worst, w = oracle.check_float(oracle.decode(got, p.dtype), r, sabs, p.dtype)
+    assert ok, f"worst ratio {worst:.3f} at ({ii[w]},{jj[w]})"
+
+
+def freivalds(p, d, alpha, beta, seed):
+    """D x == alpha A (B x) + beta C x within the summed per-element tolerance."""
+    x = oracle.freivalds_vector(p.N, seed)
+    bx = oracle.matvec(p.K, p.N, p.B, p.ldb, p.layoutB, p.dtype, x)
+    want = alpha * oracle.matvec(p.M, p.K, p.A, p.lda, p.layoutA, p.dtype, bx)
+    if beta != 0.0:
+        want += beta * (oracle.decode(p.C, p.dtype).reshape(p.M, p.ldc)[:, :p.N] @ x)
+    dv = oracle.decode(d, p.dtype) if p.dtype != "i8" else d.astype(np.float64)
+    got = dv @ x
+    if p.dtype == "i8":
+        assert np.array_equal(got, want)
+        return
+    # per-row bound: the sum of per-element tolerances, with S_abs bounded by K*max|a|*max|b|
+    amax = np.abs(oracle.decode(p.A, p.dtype)).max()
+    bmax = np.abs(oracle.decode(p.B, p.dtype)).max()
+    tol = p.N * (1e-2 * p.K * amax * bmax * 2.0**-7 + 1e-3) + np.abs(dv).sum(axis=1) * 2.0**-8
+    assert np.all(np.abs(got - want) <= tol)
+
+
+# ------------------------------------------------------------------ small, full checks
+
+def test_fp16_256_cube():
+    p, a, b, act = synth.make(synth.WORKLOADS["fp16_256"])
+    d = run(p, a, b, act)
+    check_full(p, d, a, b, act)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_majorness_ragged_tiles(dtype, la, lb):
+    # several tiles plus ragged tails in M, N and K; leading dims keep TMA legal
+    M, N, K = 300, 520, 200
+    p = synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=10, distC="uniform",
+                      dist_bias="normal:0.5",
+                      lda=(208 if la == "row" else 304), ldb=(520 if lb == "row" else 200))
+    d = run(p, 1.25, -0.75, "none")
+    check_full(p, d, 1.25, -0.75)
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_tanh"])
+def test_epilogue_bias_activation(act):
+    p = synth.Problem(256, 384, 192, dtype="bf16", seed=11, distA="normal:1.0",
+                      distB="normal:0.1", dist_bias="normal:0.5")
+    d = run(p, 1.0, 0.0, act)
+    check_full(p, d, 1.0, 0.0, act)
+
+
+@pytest.mark.parametrize("tile_n", [256, 128, 64, 32])
+def test_every_tile_width(tile_n):
+    ttc.ttc_set_knob("tile_n", tile_n)
+    try:
+        p = synth.Problem(200, 136, 136, dtype="bf16", seed=12, distC="uniform")
+        d = run(p, 0.5, 2.0)
+        check_full(p, d, 0.5, 2.0)
+    finally:
+        ttc.ttc_set_knob("tile_n", 0)
+
+
+def test_generic_store_path():
+    ttc.ttc_set_knob("force_generic_store", 1)
+    try:
+        p = synth.Problem(130, 70, 64, dtype="bf16", seed=13, distC="uniform")
+        d = run(p, 1.0, 1.0, ldd=77)
+        check_full(p, d, 1.0, 1.0)
+    finally:
+        ttc.ttc_set_knob("force_generic_store", 0)
+
+
+def test_k_zero_is_epilogue_only():
+    p = synth.Problem(64, 48, 0, dtype="bf16", seed=14, distC="uniform", dist_bias="uniform",
+                      lda=1, ldb=1)
+    d = run(p, 3.0, 0.5, "relu")
+    check_full(p, d, 3.0, 0.5, "relu")
+
+
+def test_beta_zero_ignores_nan_c():
+    p = synth.Problem(128, 64, 64, dtype="bf16", seed=15, distC="uniform")
+    p.C[:] = 0x7FC0
+    d = run(p, 1.0, 0.0)
+    check_full(p, d, 1.0, 0.0)
+
+
+def test_in_place_c_equals_d():
+    p = synth.Problem(192, 256, 128, dtype="bf16", seed=16, distC="uniform")
+    Cd = to_dev(p.C)
+    d = run(p, 1.0, 1.0, C_dev=Cd, D=Cd)
+    check_full(p, d, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (7, 8, 16), (1, 1, 1), (129, 33, 65), (16, 512, 1024)])
+def test_small_and_degenerate(M, N, K):
+    p = synth.Problem(M, N, K, dtype="bf16", seed=17, distC="uniform",
+                      lda=((K + 7) // 8) * 8, ldb=((K + 7) // 8) * 8)
+    d = run(p, 1.0, 1.0, ldd=((N + 7) // 8) * 8)
+    check_full(p, d, 1.0, 1.0)
+
+
+def test_two_streams_and_repeat():
+    p = synth.Problem(256, 256, 256, dtype="bf16", seed=18)
+    s2 = torch.cuda.Stream()
+    d1 = run(p, 1.0, 0.0)
+    d2 = run(p, 1.0, 0.0, stream=s2.cuda_stream)
+    assert np.array_equal(d1, d2)
+    check_full(p, d1, 1.0, 0.0)
+
+
+# ------------------------------------------------------------------ the suite's workloads
+
+def test_bf16_4096_alpha_beta_full():
+    p, a, b, act = synth.make(synth.WORKLOADS["bf16_4096"])
+    d = run(p, a, b, act)
+    check_full(p, d, a, b, act)
+
+
+def test_bf16_mlp_gelu_sampled():
+    p, a, b, act = synth.make(synth.WORKLOADS["bf16_mlp_8192x14336x4096"])
+    d = run(p, a, b, act)
+    check_sampled(p, d, a, b, act, seed=2)
+
+
+def test_bf16_8192_sampled_and_freivalds():
+    p, a, b, act = synth.make(synth.WORKLOADS["bf16_8192"])
+    d = run(p, a, b, act)
+    check_sampled(p, d, a, b, act, seed=1)
+    freivalds(p, d, a, b, seed=1)
+
+
+# ------------------------------------------------------------------ failure detection
+
+def test_stalled_pipeline_times_out_and_context_survives():
+    """A tensor-core issuer that waits on a barrier nothing arrives at must end
+    the kernel with TTC_ERR_TIMEOUT within the wait budget, and the context
+    must stay usable."""
+    p = synth.Problem(256, 512, 512, dtype="bf16", seed=19)
+    ttc.ttc_set_knob("timeout_ns", 200_000_000)
+    ttc.ttc_set_knob("inject_stall", 1)
+    try:
+        A, B = to_dev(p.A), to_dev(p.B)
+        D = torch.zeros(p.M * p.N, dtype=torch.int16, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        st = ttc.ttc_gemm(p.M, p.N, p.K, A.data_ptr(), p.lda, 0, B.data_ptr(), p.ldb, 1, None, p.N,
+                          D.data_ptr(), p.N, 1.0, 0.0, None, 0, ttc.DTYPE["bf16"], s)
+        assert st == 0
+        assert ttc.ttc_get_device_error(s) == 4
+    finally:
+        ttc.ttc_set_knob("inject_stall", 0)
+        ttc.ttc_set_knob("timeout_ns", 0)
+    assert ttc.ttc_get_device_error(None) == 0
+    d = run(p, 1.0, 0.0)
+    check_full(p, d, 1.0, 0.0)

@@ -1,0 +1,299 @@
+// Host side of the ttc C ABI: argument validation, layout canonicalisation,
+// TMA descriptor encoding, planning (tile width, grid, rasterization) and the
+// kernel launch.  See include/ttc.h for the contract of each entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "gemm_kernel.cuh"
+#include "ttc.h"
+#include "ttc_layout.hpp"
+
+namespace ttc {
+
+__device__ uint32_t g_device_error;  // first failure code of any kernel on this device
+
+namespace {
+
+std::atomic<int64_t> g_timeout_ns{2000000000ll};
+std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_force_generic_load{0};
+std::atomic<int> g_force_generic_store{0};
+std::atomic<int> g_force_tile_n{0};
+std::atomic<int64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sm_count = 0;
+  uint32_t* err = nullptr;
+  bool attrs_set[16] = {};
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+ttc_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TTC_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return TTC_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return TTC_ERR_CUDA;
+    d.err = static_cast<uint32_t*>(p);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return TTC_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  *out = &d;
+  return TTC_OK;
+}
+
+// 2-D tensor map over a row-major-in-memory view: `inner` contiguous
+// elements, `outer` rows `pitch_elems` apart.
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
+               CUtensorMapSwizzle sw) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_elems * (uint64_t)esize};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tma_ok(const void* p, int64_t ld, int esize) {
+  return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * esize) % 16 == 0) && ld * esize < (1ll << 40);
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+template <int BN, bool BF16>
+ttc_status launch_f16(const GemmParams& prm, DeviceInfo* dev, int grid, cudaStream_t stream) {
+  using Cfg = TileCfg<BN>;
+  auto kern = gemm_f16_kernel<BN, BF16>;
+  constexpr int slot = (BN == 256 ? 0 : BN == 128 ? 1 : BN == 64 ? 2 : 3) + (BF16 ? 4 : 0);
+  if (!dev->attrs_set[slot]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
+      return TTC_ERR_CUDA;
+    dev->attrs_set[slot] = true;
+  }
+  kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return TTC_OK;
+}
+
+template <bool BF16>
+ttc_status launch_bn(int bn, const GemmParams& prm, DeviceInfo* dev, int grid, cudaStream_t s) {
+  switch (bn) {
+    case 256: return launch_f16<256, BF16>(prm, dev, grid, s);
+    case 128: return launch_f16<128, BF16>(prm, dev, grid, s);
+    case 64: return launch_f16<64, BF16>(prm, dev, grid, s);
+    case 32: return launch_f16<32, BF16>(prm, dev, grid, s);
+    default: return TTC_ERR_UNSUPPORTED;
+  }
+}
+
+bool ranges_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
+}
+
+}  // namespace
+}  // namespace ttc
+
+using namespace ttc;
+
+extern "C" {
+
+const char* ttc_status_string(ttc_status s) {
+  switch (s) {
+    case TTC_OK: return "TTC_OK";
+    case TTC_ERR_INVALID_ARG: return "TTC_ERR_INVALID_ARG";
+    case TTC_ERR_UNSUPPORTED: return "TTC_ERR_UNSUPPORTED";
+    case TTC_ERR_CUDA: return "TTC_ERR_CUDA";
+    case TTC_ERR_TIMEOUT: return "TTC_ERR_TIMEOUT";
+  }
+  return "TTC_UNKNOWN_STATUS";
+}
+
+ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
+  switch (knob) {
+    case TTC_KNOB_TIMEOUT_NS: g_timeout_ns.store(value > 0 ? value : 2000000000ll); return TTC_OK;
+    case TTC_KNOB_INJECT_STALL:
+      if (value != 0 && value != 1) return TTC_ERR_INVALID_ARG;
+      g_inject_stall.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_FORCE_GENERIC_LOAD:
+      if (value != 0 && value != 1) return TTC_ERR_INVALID_ARG;
+      g_force_generic_load.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_FORCE_GENERIC_STORE:
+      if (value != 0 && value != 1) return TTC_ERR_INVALID_ARG;
+      g_force_generic_store.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_TILE_N:
+      if (value != 0 && value != 256 && value != 128 && value != 64 && value != 32 && value != 16)
+        return TTC_ERR_INVALID_ARG;
+      g_force_tile_n.store((int)value);
+      return TTC_OK;
+  }
+  return TTC_ERR_INVALID_ARG;
+}
+
+int64_t ttc_launch_count(void) { return g_launches.load(); }
+
+ttc_status ttc_get_device_error(void* stream) {
+  DeviceInfo* dev = nullptr;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+  ttc_status st = device_info(&dev);
+  if (st != TTC_OK) return st;
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, dev->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return TTC_ERR_CUDA;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpy(dev->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) return TTC_ERR_CUDA;
+    return TTC_ERR_TIMEOUT;
+  }
+  return TTC_OK;
+}
+
+ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA, const void* B,
+                    int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D, int64_t ldd, float alpha,
+                    float beta, const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
+  // ------------------------------------------------------------ validation
+  if (M < 0 || N < 0 || K < 0) return TTC_ERR_INVALID_ARG;
+  if ((layoutA != TTC_ROW_MAJOR && layoutA != TTC_COL_MAJOR) ||
+      (layoutB != TTC_ROW_MAJOR && layoutB != TTC_COL_MAJOR))
+    return TTC_ERR_INVALID_ARG;
+  if (act != TTC_ACT_NONE && act != TTC_ACT_RELU && act != TTC_ACT_GELU_TANH) return TTC_ERR_INVALID_ARG;
+  if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return TTC_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return TTC_OK;
+  const int64_t a_min = layoutA == TTC_ROW_MAJOR ? K : M;
+  const int64_t b_min = layoutB == TTC_ROW_MAJOR ? N : K;
+  if (lda < (a_min > 1 ? a_min : 1) || ldb < (b_min > 1 ? b_min : 1) || ldd < N) return TTC_ERR_INVALID_ARG;
+  if (beta != 0.0f && (C == nullptr || ldc < N)) return TTC_ERR_INVALID_ARG;
+  if (D == nullptr) return TTC_ERR_INVALID_ARG;
+  if (K > 0 && (A == nullptr || B == nullptr)) return TTC_ERR_INVALID_ARG;
+  const int out_esize = dtype == TTC_I8 ? 4 : 2;
+  if (beta != 0.0f) {
+    const int64_t c_bytes = ((M - 1) * ldc + N) * out_esize;
+    const int64_t d_bytes = ((M - 1) * ldd + N) * out_esize;
+    const bool in_place = (C == D) && (ldc == ldd);
+    if (!in_place && ranges_overlap(C, c_bytes, D, d_bytes)) return TTC_ERR_INVALID_ARG;
+  }
+  if (dtype == TTC_I8) {
+    if (bias != nullptr || act != TTC_ACT_NONE || alpha != 1.0f || (beta != 0.0f && beta != 1.0f))
+      return TTC_ERR_UNSUPPORTED;
+    return TTC_ERR_UNSUPPORTED;  // int8 path not built yet
+  }
+  const int64_t lim = 0x7FFFFFFFll;
+  if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim || ldd > lim) return TTC_ERR_UNSUPPORTED;
+
+  DeviceInfo* dev = nullptr;
+  ttc_status st = device_info(&dev);
+  if (st != TTC_OK) return st;
+
+  // ------------------------------------------------------------ canonicalisation
+  // A size-1 mode leaves its stride free: a 1 x K column-major A with lda = 1
+  // is the same memory as a row-major one, and so on.
+  if (M == 1 && layoutA == TTC_COL_MAJOR && lda == 1) {
+    layoutA = TTC_ROW_MAJOR;
+    lda = round_up(K > 0 ? K : 1, 8);
+  } else if (K == 1 && layoutA == TTC_ROW_MAJOR && lda == 1) {
+    layoutA = TTC_COL_MAJOR;
+    lda = round_up(M, 8);
+  }
+  if (N == 1 && layoutB == TTC_ROW_MAJOR && ldb == 1) {
+    layoutB = TTC_COL_MAJOR;
+    ldb = round_up(K > 0 ? K : 1, 8);
+  } else if (K == 1 && layoutB == TTC_COL_MAJOR && ldb == 1) {
+    layoutB = TTC_ROW_MAJOR;
+    ldb = round_up(N, 8);
+  }
+  if (M == 1 && !tma_ok(D, ldd, 2) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 8);
+
+  const bool a_mn = layoutA == TTC_COL_MAJOR;
+  const bool b_mn = layoutB == TTC_ROW_MAJOR;
+
+  // ------------------------------------------------------------ plan
+  int bn = g_force_tile_n.load();
+  if (bn == 0) bn = N > 128 ? 256 : N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
+  if (b_mn && bn < 64) return TTC_ERR_UNSUPPORTED;
+  if (bn == 16) return TTC_ERR_UNSUPPORTED;
+
+  const bool load_tma = K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2));
+  if (!load_tma || g_force_generic_load.load()) return TTC_ERR_UNSUPPORTED;  // generic producer not built yet
+  const bool store_tma = tma_ok(D, ldd, 2) && !g_force_generic_store.load();
+
+  static_assert(sizeof(GemmParams) <= 4096, "kernel parameter space");
+  GemmParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (K > 0) {
+    bool ok;
+    if (!a_mn)
+      ok = encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      ok = encode_2d(&prm.tmA, dt, 2, A, M, K, lda, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return TTC_ERR_CUDA;
+    if (!b_mn)
+      ok = encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+    else
+      ok = encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!ok) return TTC_ERR_CUDA;
+  }
+  if (store_tma && !encode_2d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return TTC_ERR_CUDA;
+
+  prm.M = (int)M;
+  prm.N = (int)N;
+  prm.K = (int)K;
+  prm.num_m_blocks = (int)((M + kBM - 1) / kBM);
+  prm.num_n_blocks = (int)((N + bn - 1) / bn);
+  prm.num_k_blocks = (int)((K + kBK - 1) / kBK);
+  prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
+  prm.group_m = prm.num_m_blocks < 16 ? prm.num_m_blocks : 16;
+  prm.a_mn = a_mn;
+  prm.b_mn = b_mn;
+  prm.alpha = alpha;
+  prm.beta = beta;
+  prm.C = beta != 0.0f ? C : nullptr;
+  prm.ldc = ldc;
+  prm.D = D;
+  prm.ldd = ldd;
+  prm.bias = bias;
+  prm.act = (int)act;
+  prm.d_tma = store_tma ? 1 : 0;
+  prm.err = dev->err;
+  prm.timeout_ns = (uint64_t)g_timeout_ns.load();
+  prm.inject_stall = g_inject_stall.load();
+
+  const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return dtype == TTC_BF16 ? launch_bn<true>(bn, prm, dev, grid, s) : launch_bn<false>(bn, prm, dev, grid, s);
+}
+
+}  // extern "C"
