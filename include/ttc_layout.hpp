@@ -152,6 +152,11 @@ inline IntTuple parse_int_tuple(const std::string& s, size_t& pos) {
       while (pos < s.size() && s[pos] == ' ') ++pos;
       if (pos < s.size() && s[pos] == ',') {
         ++pos;
+        while (pos < s.size() && s[pos] == ' ') ++pos;
+        if (pos < s.size() && s[pos] == ')') {  // "(1,)": a one-element tuple
+          ++pos;
+          break;
+        }
         continue;
       }
       if (pos < s.size() && s[pos] == ')') {
