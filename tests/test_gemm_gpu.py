@@ -199,3 +199,82 @@ def test_stalled_pipeline_times_out_and_context_survives():
     assert ttc.ttc_get_device_error(None) == 0
     d = run(p, 1.0, 0.0)
     check_full(p, d, 1.0, 0.0)
+
+
+# ------------------------------------------------------------------ operands TMA cannot describe
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_generic_producer_forced(dtype, la, lb):
+    ttc.ttc_set_knob("force_generic_load", 1)
+    try:
+        p = synth.Problem(300, 520, 200, dtype=dtype, layoutA=la, layoutB=lb, seed=20, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 1.0, 1.0, "relu")
+        check_full(p, d, 1.0, 1.0, "relu")
+    finally:
+        ttc.ttc_set_knob("force_generic_load", 0)
+
+
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_odd_leading_dimensions(la, lb):
+    # odd pitches: no TMA for any operand, no vector loads, predicated stores
+    M, N, K = 257, 131, 97
+    p = synth.Problem(M, N, K, dtype="bf16", layoutA=la, layoutB=lb, seed=21, distC="uniform",
+                      lda=(K if la == "row" else M) + 1, ldb=(N if lb == "row" else K) + 3, ldc=N + 5)
+    d = run(p, 1.0, 1.0, ldd=N + 7)
+    check_full(p, d, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("shape", synth.RAGGED_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_ragged_sweep(shape, la, lb):
+    """The ragged / skinny sweep with tight leading dimensions, checked in full."""
+    p, a, b, act = synth.make(synth.ragged_workload(*shape, la, lb))
+    d = run(p, a, b, act)
+    check_full(p, d, a, b, act)
+
+
+# ------------------------------------------------------------------ int8 -> int32, exact
+
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_int8_small_all_layouts(la, lb):
+    p = synth.Problem(200, 150, 300, dtype="i8", layoutA=la, layoutB=lb, seed=22, distA="int8",
+                      distB="int8")
+    d = run(p, 1.0, 0.0)
+    check_full(p, d, 1.0, 0.0)
+
+
+def test_int8_beta_one_adds_c():
+    p = synth.Problem(130, 70, 64, dtype="i8", seed=23, distA="int8", distB="int8")
+    rng = np.random.default_rng(0)
+    c = rng.integers(-2**20, 2**20, size=(p.M, p.N)).astype(np.int32)
+    p.C_log = c
+    p.C, p.ldc = synth.to_layout(c, "row")
+    d = run(p, 1.0, 1.0)
+    check_full(p, d, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("K", [1024, 1025, 8192])
+def test_int8_extreme_values_stay_exact(K):
+    """-128 * -128 everywhere: each 1024-deep partial sum reaches 2^24, the
+    largest integer an fp32 accumulator holds exactly; the int32 result is
+    K * 2^14."""
+    M, N = 128, 64
+    p = synth.Problem.from_logical(np.full((M, K), -128, np.int8), np.full((K, N), -128, np.int8), dtype="i8")
+    d = run(p, 1.0, 0.0)
+    assert np.all(d == K * 16384)
+    # mixed signs that cancel only in exact arithmetic
+    a = np.full((M, K), 127, np.int8)
+    a[:, 1::2] = -128
+    b = np.full((K, N), 127, np.int8)
+    q = synth.Problem.from_logical(a, b, dtype="i8")
+    d = run(q, 1.0, 0.0)
+    check_full(q, d, 1.0, 0.0)
+
+
+def test_int8_8192_sampled_and_freivalds():
+    p, a, b, act = synth.make(synth.WORKLOADS["i8_8192"])
+    d = run(p, a, b, act)
+    check_sampled(p, d, a, b, act, seed=3)
+    freivalds(p, d, a, b, seed=3)

@@ -11,7 +11,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "gemm_kernel.cuh"
+#include "gemm_launch.cuh"
 #include "ttc.h"
 #include "ttc_layout.hpp"
 
@@ -34,7 +34,6 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   uint32_t* err = nullptr;
-  bool attrs_set[16] = {};
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
@@ -89,30 +88,27 @@ bool tma_ok(const void* p, int64_t ld, int esize) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
-template <int BN, bool BF16>
-ttc_status launch_f16(const GemmParams& prm, DeviceInfo* dev, int grid, cudaStream_t stream) {
-  using Cfg = TileCfg<BN>;
-  auto kern = gemm_f16_kernel<BN, BF16>;
-  constexpr int slot = (BN == 256 ? 0 : BN == 128 ? 1 : BN == 64 ? 2 : 3) + (BF16 ? 4 : 0);
-  if (!dev->attrs_set[slot]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes) != cudaSuccess)
-      return TTC_ERR_CUDA;
-    dev->attrs_set[slot] = true;
+template <int MODE>
+cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
+  switch (bn) {
+    case 256:
+      if constexpr (MODE != kModeI8) return launch_gemm<256, MODE>(prm, grid, s);
+      return cudaErrorInvalidValue;
+    case 128: return launch_gemm<128, MODE>(prm, grid, s);
+    case 64: return launch_gemm<64, MODE>(prm, grid, s);
+    case 32: return launch_gemm<32, MODE>(prm, grid, s);
+    default: return cudaErrorInvalidValue;
   }
-  kern<<<grid, kThreads, Cfg::kSmemBytes, stream>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return TTC_ERR_CUDA;
-  g_launches.fetch_add(1);
-  return TTC_OK;
 }
 
-template <bool BF16>
-ttc_status launch_bn(int bn, const GemmParams& prm, DeviceInfo* dev, int grid, cudaStream_t s) {
-  switch (bn) {
-    case 256: return launch_f16<256, BF16>(prm, dev, grid, s);
-    case 128: return launch_f16<128, BF16>(prm, dev, grid, s);
-    case 64: return launch_f16<64, BF16>(prm, dev, grid, s);
-    case 32: return launch_f16<32, BF16>(prm, dev, grid, s);
-    default: return TTC_ERR_UNSUPPORTED;
+cudaError_t launch(int mode, int bn, const GemmParams& prm, int grid, cudaStream_t s) {
+  switch (mode) {
+    case kModeTmaF16: return launch_mode<kModeTmaF16>(bn, prm, grid, s);
+    case kModeTmaBF16: return launch_mode<kModeTmaBF16>(bn, prm, grid, s);
+    case kModeGenF16: return launch_mode<kModeGenF16>(bn, prm, grid, s);
+    case kModeGenBF16: return launch_mode<kModeGenBF16>(bn, prm, grid, s);
+    case kModeI8: return launch_mode<kModeI8>(bn, prm, grid, s);
+    default: return cudaErrorInvalidValue;
   }
 }
 
@@ -204,13 +200,17 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     const bool in_place = (C == D) && (ldc == ldd);
     if (!in_place && ranges_overlap(C, c_bytes, D, d_bytes)) return TTC_ERR_INVALID_ARG;
   }
-  if (dtype == TTC_I8) {
-    if (bias != nullptr || act != TTC_ACT_NONE || alpha != 1.0f || (beta != 0.0f && beta != 1.0f))
-      return TTC_ERR_UNSUPPORTED;
-    return TTC_ERR_UNSUPPORTED;  // int8 path not built yet
-  }
+  if (dtype == TTC_I8 &&
+      (bias != nullptr || act != TTC_ACT_NONE || alpha != 1.0f || (beta != 0.0f && beta != 1.0f)))
+    return TTC_ERR_UNSUPPORTED;
   const int64_t lim = 0x7FFFFFFFll;
   if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim || ldd > lim) return TTC_ERR_UNSUPPORTED;
+  const int in_esize = dtype == TTC_I8 ? 1 : 2;
+  // every pointer must be aligned to its element type
+  if ((K > 0 && (reinterpret_cast<uintptr_t>(A) % in_esize || reinterpret_cast<uintptr_t>(B) % in_esize)) ||
+      reinterpret_cast<uintptr_t>(D) % out_esize || (beta != 0.0f && reinterpret_cast<uintptr_t>(C) % out_esize) ||
+      reinterpret_cast<uintptr_t>(bias) % 4)
+    return TTC_ERR_INVALID_ARG;
 
   DeviceInfo* dev = nullptr;
   ttc_status st = device_info(&dev);
@@ -221,38 +221,49 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   // is the same memory as a row-major one, and so on.
   if (M == 1 && layoutA == TTC_COL_MAJOR && lda == 1) {
     layoutA = TTC_ROW_MAJOR;
-    lda = round_up(K > 0 ? K : 1, 8);
+    lda = round_up(K > 0 ? K : 1, 16);
   } else if (K == 1 && layoutA == TTC_ROW_MAJOR && lda == 1) {
     layoutA = TTC_COL_MAJOR;
-    lda = round_up(M, 8);
+    lda = round_up(M, 16);
   }
   if (N == 1 && layoutB == TTC_ROW_MAJOR && ldb == 1) {
     layoutB = TTC_COL_MAJOR;
-    ldb = round_up(K > 0 ? K : 1, 8);
+    ldb = round_up(K > 0 ? K : 1, 16);
   } else if (K == 1 && layoutB == TTC_COL_MAJOR && ldb == 1) {
     layoutB = TTC_ROW_MAJOR;
-    ldb = round_up(N, 8);
+    ldb = round_up(N, 16);
   }
-  if (M == 1 && !tma_ok(D, ldd, 2) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 8);
+  if (M == 1 && !tma_ok(D, ldd, out_esize) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 16);
 
   const bool a_mn = layoutA == TTC_COL_MAJOR;
   const bool b_mn = layoutB == TTC_ROW_MAJOR;
 
   // ------------------------------------------------------------ plan
-  int bn = g_force_tile_n.load();
-  if (bn == 0) bn = N > 128 ? 256 : N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
-  if (b_mn && bn < 64) return TTC_ERR_UNSUPPORTED;
-  if (bn == 16) return TTC_ERR_UNSUPPORTED;
+  const bool load_tma = dtype != TTC_I8 && !g_force_generic_load.load() &&
+                        (K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2)));
+  int mode;
+  if (dtype == TTC_I8)
+    mode = kModeI8;
+  else if (load_tma)
+    mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
+  else
+    mode = dtype == TTC_BF16 ? kModeGenBF16 : kModeGenF16;
+  const bool store_tma = tma_ok(D, ldd, out_esize) && !g_force_generic_store.load();
 
-  const bool load_tma = K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2));
-  if (!load_tma || g_force_generic_load.load()) return TTC_ERR_UNSUPPORTED;  // generic producer not built yet
-  const bool store_tma = tma_ok(D, ldd, 2) && !g_force_generic_store.load();
+  int bn = g_force_tile_n.load();
+  if (bn == 0) {
+    if (dtype == TTC_I8)
+      bn = N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
+    else
+      bn = N > 128 ? 256 : N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
+  }
+  if (bn == 16 || (b_mn && bn < 64) || (dtype == TTC_I8 && bn > 128)) return TTC_ERR_UNSUPPORTED;
 
   static_assert(sizeof(GemmParams) <= 4096, "kernel parameter space");
   GemmParams prm;
   std::memset(&prm, 0, sizeof prm);
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (K > 0) {
+  if (K > 0 && (mode == kModeTmaF16 || mode == kModeTmaBF16)) {
     bool ok;
     if (!a_mn)
       ok = encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
@@ -265,9 +276,23 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
       ok = encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return TTC_ERR_CUDA;
   }
-  if (store_tma && !encode_2d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
-    return TTC_ERR_CUDA;
+  if (store_tma) {
+    const bool ok = dtype == TTC_I8
+                        ? encode_2d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_128B)
+                        : encode_2d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (!ok) return TTC_ERR_CUDA;
+  }
 
+  // generic producers: 8-element groups load as one vector when every group
+  // start is aligned (16 bytes for 16-bit types, 8 bytes for int8)
+  const int vec_bytes = 8 * in_esize;
+  prm.A = A;
+  prm.B = B;
+  prm.lda = lda;
+  prm.ldb = ldb;
+  prm.a_vec = reinterpret_cast<uintptr_t>(A) % vec_bytes == 0 && (lda * in_esize) % vec_bytes == 0;
+  prm.b_vec = reinterpret_cast<uintptr_t>(B) % vec_bytes == 0 && (ldb * in_esize) % vec_bytes == 0;
   prm.M = (int)M;
   prm.N = (int)N;
   prm.K = (int)K;
@@ -292,8 +317,9 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   prm.inject_stall = g_inject_stall.load();
 
   const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return dtype == TTC_BF16 ? launch_bn<true>(bn, prm, dev, grid, s) : launch_bn<false>(bn, prm, dev, grid, s);
+  if (launch(mode, bn, prm, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return TTC_OK;
 }
 
 }  // extern "C"

@@ -1,45 +1,81 @@
 // Persistent, warp-specialized tiled GEMM for sm_103a:
-//   D = act(alpha * A * B + beta * C + bias), fp16/bf16 operands, fp32 accumulation.
+//   D = act(alpha * A * B + beta * C + bias)
+// fp16/bf16 operands with fp32 accumulation, or int8 operands with an exact
+// int32 result.
 //
-// Structure (the CUTLASS tutorial's "Collective Mainloop + Collective Epilogue"
-// split on hpc.payai.win/cutlass, section 3, rebuilt for tcgen05/TMEM/TMA):
-//   warp 0      producer: one thread issues TMA loads of the A and B tiles of
-//               each k-block into a STAGES-deep ring of 128-byte-swizzled
-//               shared-memory slots (full/empty mbarrier pair per slot);
-//   warp 1      tensor-core issuer: allocates TMEM, one thread issues
-//               tcgen05.mma (M=128, N=BN, K=16) into one of two TMEM
-//               accumulators and commits completion back to the ring;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the
-//               32 TMEM lanes = tile rows its warp index selects), then
-//               alpha / beta*C / bias / activation in fp32, round to the
-//               output type, stage in swizzled shared memory and TMA-store.
-// The two TMEM accumulators let the epilogue of tile i overlap the mainloop
-// of tile i+1.  Tiles are walked persistently (tile = blockIdx.x + j*gridDim.x)
-// in grouped order: group_m consecutive M-blocks share each N-block, so a
-// wave of CTAs reuses the same A and B panels from L2.
+// Structure (the tutorial's "Collective Mainloop + Collective Epilogue" split,
+// hpc.payai.win/cutlass section 3, rebuilt for tcgen05/TMEM/TMA):
+//   producer    fills a STAGES-deep ring of 128-byte-swizzled shared-memory
+//               slots with the A and B tiles of each 64-wide k-block
+//               (full/empty mbarrier pair per slot).  TMA modes: one thread
+//               issues 2-D TMA boxes.  Generic modes (operands TMA cannot
+//               describe, and int8): four warps load with plain predicated
+//               loads along the strip-mined thread map of the
+//               PitchLinearStripminedThreadMap walkthrough (lpnh.cn, sections
+//               2-4) and write the same swizzled layout TMA would;
+//   MMA issuer  allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
+//               K=16) into one of two TMEM accumulators and commits completion
+//               back to the ring;
+//   epilogue    4 warps; each owns the 32 TMEM lanes (= tile rows) its warp
+//               index selects: tcgen05.ld, alpha / beta*C / bias / activation
+//               in fp32, round, stage in swizzled shared memory, TMA store
+//               (or predicated stores when TMA cannot describe D).
+// The two accumulators let the epilogue of one unit overlap the mainloop of
+// the next.  A unit is a whole tile for fp16/bf16; for int8 it is a chunk of
+// at most 1024 k, whose exact fp32 partial sum the epilogue adds into int32
+// registers (every partial is an integer below 2^24 in magnitude, so fp32
+// holds it exactly).  Tiles are walked persistently in grouped order: group_m
+// consecutive M-blocks share each N-block, so concurrent CTAs reuse A and B
+// panels from L2.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
+#include "ttc_layout.hpp"
 
 namespace ttc {
 
-constexpr int kBM = 128;          // UMMA M (rows of the CTA tile = TMEM lanes)
-constexpr int kBK = 64;           // k-block: 64 16-bit elements = one 128-byte swizzle row
-constexpr int kUmmaK = 16;        // K of one tcgen05.mma for 16-bit inputs
+constexpr int kBM = 128;     // UMMA M (rows of the CTA tile = TMEM lanes)
+constexpr int kBK = 64;      // k-block: 64 16-bit elements = one 128-byte swizzle row
+constexpr int kUmmaK = 16;   // K of one tcgen05.mma for 16-bit inputs
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-constexpr int kEpiCols = 32;      // columns per epilogue chunk
-constexpr int kEpiBufBytes = 32 * kEpiCols * 2;  // 32 rows x 64 bytes
-constexpr int kABytes = kBM * kBK * 2;           // 16 KiB
+constexpr int kEpiCols = 32;  // columns per epilogue chunk
+constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
+constexpr int kI8ChunkKBlocks = 16;     // int8: drain the accumulator every 1024 k
 
 enum ActKind : int { kActNone = 0, kActRelu = 1, kActGelu = 2 };
+
+// Kernel modes: how operands reach shared memory and what the element types are.
+enum Mode : int {
+  kModeTmaF16 = 0,   // TMA loads, fp16 in/out
+  kModeTmaBF16 = 1,  // TMA loads, bf16 in/out
+  kModeGenF16 = 2,   // plain loads, fp16
+  kModeGenBF16 = 3,  // plain loads, bf16
+  kModeI8 = 4,       // plain loads of int8, converted to fp16; int32 out
+};
+
+template <int MODE>
+struct ModeTraits {
+  static constexpr bool kTmaLoad = MODE == kModeTmaF16 || MODE == kModeTmaBF16;
+  static constexpr bool kBF16 = MODE == kModeTmaBF16 || MODE == kModeGenBF16;  // tensor-core input type
+  static constexpr bool kI8 = MODE == kModeI8;
+  static constexpr int kProdWarps = kTmaLoad ? 1 : 4;
+  static constexpr int kMmaWarp = kProdWarps;
+  static constexpr int kEpiWarp0 = kProdWarps + 1;
+  static constexpr int kThreads = 32 * (kProdWarps + 1 + kEpiWarps);
+  static constexpr int kOutBytes = kI8 ? 4 : 2;
+  static constexpr int kEpiBufBytes = 32 * kEpiCols * kOutBytes;  // 32 rows x (64 or 128) bytes
+};
 
 struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
   CUtensorMap tmD;
+  const void* A;  // generic modes: operand base pointers and leading dimensions
+  const void* B;
+  int64_t lda, ldb;
+  int a_vec, b_vec;  // generic modes: 1 when 8-element groups may be read as one vector
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
   int a_mn, b_mn;  // operand stored MN-major (A column-major / B row-major)
@@ -56,18 +92,19 @@ struct GemmParams {
   int inject_stall;
 };
 
-template <int BN>
+template <int BN, int MODE>
 struct TileCfg {
+  using T = ModeTraits<MODE>;
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * T::kEpiBufBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per block
   static constexpr int kStageBudget = kSmemLimit - 1024 - kBarBytes - kEpiBytes;
   static constexpr int kStages = kStageBudget / kStageBytes > 8 ? 8 : kStageBudget / kStageBytes;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kEpiBytes + kBarBytes;
-  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M=128");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole epilogue chunks");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
   static_assert((2 * BN & (2 * BN - 1)) == 0, "TMEM allocation is a power of two");
@@ -94,8 +131,7 @@ __device__ __forceinline__ float apply_act(int act, float x) {
 }
 
 template <bool BF16>
-__device__ __forceinline__ float load_elem16(const void* base, int64_t idx) {
-  const uint16_t h = reinterpret_cast<const uint16_t*>(base)[idx];
+__device__ __forceinline__ float half_bits_to_float(uint16_t h) {
   if constexpr (BF16) {
     return __bfloat162float(__ushort_as_bfloat16(h));
   } else {
@@ -123,10 +159,82 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, uint6
   }
 }
 
-template <int BN, bool BF16>
-__global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_constant__ GemmParams p) {
-  using Cfg = TileCfg<BN>;
+// ------------------------------------------------------------------ generic operand loads
+// One operand tile in memory order: ROWS rows ("outer": M/N rows of a K-major
+// operand, k rows of an MN-major one) of COLS contiguous elements.  The 128
+// producer threads walk it with the strip-mined map (8 contiguous elements per
+// access), load with predicates (zero outside the extents) and store each
+// 8-element group as one 16-byte chunk of the 128-byte-swizzled layout the
+// tensor core reads: element (r, c) sits at
+//   Swizzle<3,4,3>((c / 64) * ROWS * 128 + r * 128 + (c % 64) * 2),
+// i.e. 64-column slabs of ROWS 128-byte rows, the layout TMA writes for the
+// same tile.
+template <int ROWS, int COLS, bool kI8>
+__device__ __forceinline__ void generic_load_tile(uint8_t* sdst, const void* gsrc, int64_t ld, int outer0,
+                                                  int inner0, int outer_ext, int inner_ext, bool vec_ok, int tid) {
+  constexpr layout::StripMined map{ROWS, COLS, 128, 8};
+  static_assert(map.valid(), "strip-mined map must tile the operand tile");
+  constexpr int kIters = map.iterations();
+  constexpr layout::SwizzleBytes128 swz{};
+  const int c = map.col(tid);
+  const int gi = inner0 + c;
+  const bool inner_full = gi + 7 < inner_ext;
+  constexpr int kBatch = kIters < 4 ? kIters : 4;
+#pragma unroll
+  for (int i0 = 0; i0 < kIters; i0 += kBatch) {
+    uint4 w[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int r = map.row(tid, i0 + b);
+      const int go = outer0 + r;
+      const bool row_ok = go < outer_ext;
+      if constexpr (kI8) {
+        const int8_t* src = reinterpret_cast<const int8_t*>(gsrc) + (int64_t)go * ld + gi;
+        int8_t e[8];
+        if (row_ok && inner_full && vec_ok) {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(src));
+          *reinterpret_cast<uint2*>(e) = u;
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = (row_ok && gi + j < inner_ext) ? __ldg(src + j) : (int8_t)0;
+        }
+        uint32_t h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          // int8 values are exact in fp16
+          __half2 v = __halves2half2(__int2half_rn(e[2 * j]), __int2half_rn(e[2 * j + 1]));
+          h[j] = *reinterpret_cast<uint32_t*>(&v);
+        }
+        w[b] = make_uint4(h[0], h[1], h[2], h[3]);
+      } else {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(gsrc) + (int64_t)go * ld + gi;
+        if (row_ok && inner_full && vec_ok) {
+          w[b] = __ldg(reinterpret_cast<const uint4*>(src));
+        } else {
+          uint16_t e[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) e[j] = (row_ok && gi + j < inner_ext) ? __ldg(src + j) : (uint16_t)0;
+          w[b] = make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16),
+                            e[4] | ((uint32_t)e[5] << 16), e[6] | ((uint32_t)e[7] << 16));
+        }
+      }
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int r = map.row(tid, i0 + b);
+      const uint32_t off = swz((uint32_t)((c / 64) * ROWS * 128 + r * 128 + (c % 64) * 2));
+      *reinterpret_cast<uint4*>(sdst + off) = w[b];
+    }
+  }
+}
+
+template <int BN, int MODE>
+__global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Cfg = TileCfg<BN, MODE>;
+  using Tr = ModeTraits<MODE>;
   constexpr int S = Cfg::kStages;
+  constexpr bool kBF16 = Tr::kBF16;
+  constexpr bool kI8 = Tr::kI8;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
@@ -144,10 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtx wc{p.err, p.timeout_ns};
+  // units per tile: int8 drains its accumulator every kI8ChunkKBlocks k-blocks
+  const int chunk_kb = kI8 ? kI8ChunkKBlocks : (p.num_k_blocks > 0 ? p.num_k_blocks : 1);
+  const int units_per_tile = p.num_k_blocks > 0 ? (p.num_k_blocks + chunk_kb - 1) / chunk_kb : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
+      mbar_init(&full[s], Tr::kTmaLoad ? 1 : Tr::kProdWarps);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -157,11 +268,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
     mbar_init(stall_bar, 1);
     mbar_init(drain_bar, 1);
     fence_barrier_init();
-    prefetch_tmap(&p.tmA);
-    prefetch_tmap(&p.tmB);
+    if constexpr (Tr::kTmaLoad) {
+      prefetch_tmap(&p.tmA);
+      prefetch_tmap(&p.tmB);
+    }
     if (p.d_tma) prefetch_tmap(&p.tmD);
   }
-  if (warp == 1) {
+  if (warp == Tr::kMmaWarp) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
     tmem_relinquish();
   }
@@ -170,100 +283,144 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  if (warp == 0) {
+  if (warp < Tr::kProdWarps) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
+    if constexpr (Tr::kTmaLoad) {
+      if (lane == 0) {
+        const uint64_t pol = policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t issued_mask = 0, issued_parity = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+          int mb, nb;
+          tile_coords(t, p, mb, nb);
+          const int m0 = mb * kBM, n0 = nb * BN;
+          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+            uint8_t* a = sA + stage * kABytes;
+            uint8_t* b = sB + stage * Cfg::kBBytes;
+            const int k0 = kb * kBK;
+            if (!p.a_mn) {
+              tma_load_2d(a, &p.tmA, k0, m0, &full[stage], pol);
+            } else {
+              tma_load_2d(a, &p.tmA, m0, k0, &full[stage], pol);
+              tma_load_2d(a + kABytes / 2, &p.tmA, m0 + 64, k0, &full[stage], pol);
+            }
+            if (!p.b_mn) {
+              tma_load_2d(b, &p.tmB, k0, n0, &full[stage], pol);
+            } else {
+#pragma unroll
+              for (int h = 0; h < BN / 64; ++h)
+                tma_load_2d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, &full[stage], pol);
+            }
+            issued_mask |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) {
+          // Let every load this thread started land before the CTA exits.
+          for (int s = 0; s < S; ++s)
+            if (issued_mask & (1u << s)) drain_wait(&full[s], (issued_parity >> s) & 1u, 100000000ull);
+        }
+      }
+    } else {
+      const int tid = threadIdx.x;  // 0..127
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t issued_mask = 0, issued_parity = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
+        bool ok = true;
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
           uint8_t* a = sA + stage * kABytes;
           uint8_t* b = sB + stage * Cfg::kBBytes;
           const int k0 = kb * kBK;
-          if (!p.a_mn) {
-            tma_load_2d(a, &p.tmA, k0, m0, &full[stage], pol);
-          } else {
-            tma_load_2d(a, &p.tmA, m0, k0, &full[stage], pol);
-            tma_load_2d(a + kABytes / 2, &p.tmA, m0 + 64, k0, &full[stage], pol);
-          }
+          if (!p.a_mn)
+            generic_load_tile<kBM, kBK, kI8>(a, p.A, p.lda, m0, k0, p.M, p.K, p.a_vec, tid);
+          else
+            generic_load_tile<kBK, kBM, kI8>(a, p.A, p.lda, k0, m0, p.K, p.M, p.a_vec, tid);
           if (!p.b_mn) {
-            tma_load_2d(b, &p.tmB, k0, n0, &full[stage], pol);
+            generic_load_tile<BN, kBK, kI8>(b, p.B, p.ldb, n0, k0, p.N, p.K, p.b_vec, tid);
           } else {
-#pragma unroll
-            for (int h = 0; h < BN / 64; ++h) tma_load_2d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, &full[stage], pol);
+            if constexpr (BN >= 64) generic_load_tile<kBK, BN, kI8>(b, p.B, p.ldb, k0, n0, p.K, p.N, p.b_vec, tid);
           }
-          issued_mask |= 1u << stage;
-          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-      }
-      if (!ok) {
-        // Let every load this thread started land before the CTA exits.
-        for (int s = 0; s < S; ++s)
-          if (issued_mask & (1u << s)) drain_wait(&full[s], (issued_parity >> s) & 1u, 100000000ull);
-      }
-    }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      const uint32_t idesc = idesc_f16(BF16, p.a_mn != 0, p.b_mn != 0, kBM, BN);
-      bool ok = true;
-      bool any_mma = false;
-      if (p.inject_stall) ok = mbar_wait(stall_bar, 0, wc);  // nothing arrives here
-      int stage = 0;
-      uint32_t phase = 0;
-      int it = 0;
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
-      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x, ++it) {
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, wc)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-          const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
-#pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024);
-            const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024);
-            mma_f16(d_tmem, ad, bd, idesc, (kb | k) != 0);
-          }
-          any_mma = true;
-          mma_commit(&empty[stage]);
+          // generic-proxy writes must be visible to the tensor core (async proxy)
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        if (p.num_k_blocks == 0)
-          mbar_arrive(&tmem_full[acc]);
-        else
-          mma_commit(&tmem_full[acc]);
+      }
+    }
+  } else if (warp == Tr::kMmaWarp) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_f16(kBF16, p.a_mn != 0, p.b_mn != 0, kBM, BN);
+      bool ok = true;
+      bool any_mma = false;
+      if (p.inject_stall) ok = mbar_wait(stall_bar, 0, wc);  // nothing arrives here
+      int stage = 0;
+      uint32_t phase = 0;
+      int unit = 0;
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int u = 0; ok && u < units_per_tile; ++u, ++unit) {
+          const int acc = unit & 1;
+          const uint32_t acc_phase = (unit >> 1) & 1;
+          if (!mbar_wait(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * BN;
+          const int kb0 = u * chunk_kb;
+          const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
+          for (int kb = kb0; kb < kb1; ++kb) {
+            if (!mbar_wait(&full[stage], phase, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_addr = smem_u32(sA + stage * kABytes);
+            const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+#pragma unroll
+            for (int k = 0; k < kBK / kUmmaK; ++k) {
+              const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024);
+              const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024);
+              mma_f16(d_tmem, ad, bd, idesc, (kb != kb0) || (k != 0));
+            }
+            any_mma = true;
+            mma_commit(&empty[stage]);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+          if (!ok) break;
+          if (kb1 <= kb0)
+            mbar_arrive(&tmem_full[acc]);
+          else
+            mma_commit(&tmem_full[acc]);
+        }
       }
       if (any_mma) {
         // Every MMA must have finished with TMEM before it is freed.
@@ -273,98 +430,163 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
     }
   } else {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - 2;      // epilogue warp 0..3 (owns a staging area)
-    const int q = warp & 3;       // TMEM lane quarter this warp may access
+    const int ew = warp - Tr::kEpiWarp0;  // epilogue warp 0..3 (owns a staging area)
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int row_in_tile = q * 32 + lane;
-    uint8_t* stage_buf = sEpi + ew * 2 * kEpiBufBytes;
+    uint8_t* stage_buf = sEpi + ew * 2 * Tr::kEpiBufBytes;
     int buf = 0;
-    int it = 0;
+    int unit = 0;
     const bool has_k = p.num_k_blocks > 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      if (!mbar_wait(&tmem_full[acc], acc_phase, wc)) break;
-      tc_fence_after();
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
       int mb, nb;
       tile_coords(t, p, mb, nb);
       const int m0 = mb * kBM, n0 = nb * BN;
       const int grow = m0 + row_in_tile;
       const bool row_ok = grow < p.M;
-#pragma unroll 1
-      for (int c = 0; c < BN / kEpiCols; ++c) {
-        uint32_t r[32];
-        if (has_k) {
-          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN + c * kEpiCols, r);
-          tmem_ld_wait();
-        } else {
+
+      // int8: exact int32 sums of the per-chunk partials, held in registers
+      int32_t isum[kI8 ? BN / kEpiCols : 1][32];
+      if constexpr (kI8) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = 0u;
-        }
-        if (c == BN / kEpiCols - 1) {
-          // accumulator fully read: hand it back to the MMA issuer
+        for (int c = 0; c < BN / kEpiCols; ++c)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) isum[c][j] = 0;
+        for (int u = 0; u < units_per_tile; ++u, ++unit) {
+          const int acc = unit & 1;
+          if (!mbar_wait(&tmem_full[acc], (unit >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (has_k) {
+#pragma unroll
+            for (int c = 0; c < BN / kEpiCols; ++c) {
+              uint32_t r[32];
+              tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * kEpiCols, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) isum[c][j] += __float2int_rn(__uint_as_float(r[j]));
+            }
+          }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&tmem_empty[acc]);
         }
+        if (!ok) break;
+      } else {
+        if (!mbar_wait(&tmem_full[unit & 1], (unit >> 1) & 1, wc)) break;
+        tc_fence_after();
+      }
+      const int acc = unit & 1;  // fp16/bf16: the unit being drained below
+
+      // int8 indexes the register sums by chunk, so it unrolls; fp16/bf16 keeps one chunk's code
+      constexpr int kEpiUnroll = kI8 ? BN / kEpiCols : 1;
+#pragma unroll kEpiUnroll
+      for (int c = 0; c < BN / kEpiCols; ++c) {
         const int gcol0 = n0 + c * kEpiCols;
-        float v[32];
+        uint32_t packed[Tr::kOutBytes == 4 ? 32 : 16];
+        if constexpr (kI8) {
+          // D = sum (+ C when beta == 1); alpha == 1 (checked on the host)
+          int32_t v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
-        if (p.beta != 0.0f && row_ok) {
-          const int64_t rbase = (int64_t)grow * p.ldc;
-          const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
-                           (gcol0 + 32 <= p.N);
-          if (vec) {
-            const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.C) + rbase + gcol0);
+          for (int j = 0; j < 32; ++j) v[j] = isum[c][j];
+          if (p.beta != 0.0f && row_ok) {
+            const int32_t* crow = reinterpret_cast<const int32_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
+            const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
+                             (gcol0 + 32 <= p.N);
+            if (vec) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint4 w = __ldg(src + u);
-              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-              for (int h = 0; h < 4; ++h) {
-                float lo, hi;
-                if constexpr (BF16) {
-                  lo = __bfloat162float(__ushort_as_bfloat16((uint16_t)(ws[h] & 0xFFFFu)));
-                  hi = __bfloat162float(__ushort_as_bfloat16((uint16_t)(ws[h] >> 16)));
-                } else {
-                  lo = __half2float(__ushort_as_half((uint16_t)(ws[h] & 0xFFFFu)));
-                  hi = __half2float(__ushort_as_half((uint16_t)(ws[h] >> 16)));
-                }
-                v[u * 8 + 2 * h] = fmaf(p.beta, lo, v[u * 8 + 2 * h]);
-                v[u * 8 + 2 * h + 1] = fmaf(p.beta, hi, v[u * 8 + 2 * h + 1]);
+              for (int u4 = 0; u4 < 8; ++u4) {
+                const int4 w = __ldg(reinterpret_cast<const int4*>(crow) + u4);
+                v[4 * u4] += w.x;
+                v[4 * u4 + 1] += w.y;
+                v[4 * u4 + 2] += w.z;
+                v[4 * u4 + 3] += w.w;
               }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (gcol0 + j < p.N) v[j] += __ldg(crow + j);
             }
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) packed[j] = (uint32_t)v[j];
+        } else {
+          uint32_t r[32];
+          if (has_k) {
+            tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * kEpiCols, r);
+            tmem_ld_wait();
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gcol0 + j < p.N) v[j] = fmaf(p.beta, load_elem16<BF16>(p.C, rbase + gcol0 + j), v[j]);
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
           }
-        }
-        if (p.bias != nullptr) {
+          if (c == BN / kEpiCols - 1) {
+            // accumulator fully read: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmem_empty[acc]);
+          }
+          float v[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
-        }
-        if (p.act != kActNone) {
+          for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+          if (p.beta != 0.0f && row_ok) {
+            const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
+            const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
+                             (gcol0 + 32 <= p.N);
+            if (vec) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = apply_act(p.act, v[j]);
-        }
-        uint32_t packed[16];
+              for (int u4 = 0; u4 < 4; ++u4) {
+                const uint4 w = __ldg(reinterpret_cast<const uint4*>(crow) + u4);
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int j = 0; j < 16; ++j) packed[j] = pack2<BF16>(v[2 * j], v[2 * j + 1]);
+                for (int h = 0; h < 4; ++h) {
+                  v[u4 * 8 + 2 * h] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] & 0xFFFFu)),
+                                           v[u4 * 8 + 2 * h]);
+                  v[u4 * 8 + 2 * h + 1] =
+                      fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] >> 16)), v[u4 * 8 + 2 * h + 1]);
+                }
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(crow + j)), v[j]);
+            }
+          }
+          if (p.bias != nullptr) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
+          }
+          if (p.act != kActNone) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = apply_act(p.act, v[j]);
+          }
+#pragma unroll
+          for (int j = 0; j < 16; ++j) packed[j] = pack2<kBF16>(v[2 * j], v[2 * j + 1]);
+        }
 
         if (p.d_tma) {
           // staging buffer `buf` was last used two chunks ago; its store must
           // have finished reading shared memory
           if (lane == 0) bulk_wait_read<1>();
           __syncwarp();
-          uint8_t* sb = stage_buf + buf * kEpiBufBytes;
-          // 64-byte rows, 64-byte swizzle: 16-byte chunk index ^= (row >> 1) & 3
-          const uint32_t xr = (uint32_t)(lane >> 1) & 3u;
+          uint8_t* sb = stage_buf + buf * Tr::kEpiBufBytes;
+          if constexpr (Tr::kOutBytes == 2) {
+            // 64-byte rows, 64-byte swizzle
+            constexpr layout::SwizzleBytes64 swz{};
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint4 w = make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-            *reinterpret_cast<uint4*>(sb + lane * 64 + ((ch ^ xr) << 4)) = w;
+            for (int ch = 0; ch < 4; ++ch)
+              *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 64 + ch * 16))) =
+                  make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+          } else {
+            // 128-byte rows, 128-byte swizzle
+            constexpr layout::SwizzleBytes128 swz{};
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 128 + ch * 16))) =
+                  make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -374,22 +596,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_f16_kernel(const __grid_cons
           }
           buf ^= 1;
         } else if (row_ok) {
-          uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
+          if constexpr (Tr::kOutBytes == 4) {
+            int32_t* dst = reinterpret_cast<int32_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (gcol0 + j < p.N) {
-              const uint32_t h = (packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu;
-              dst[j] = (uint16_t)h;
-            }
+            for (int j = 0; j < 32; ++j)
+              if (gcol0 + j < p.N) dst[j] = (int32_t)packed[j];
+          } else {
+            uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gcol0 + j < p.N) dst[j] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
           }
         }
       }
+      if constexpr (!kI8) ++unit;
     }
     if (p.d_tma && lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
-  if (warp == 1) {
+  if (warp == Tr::kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, Cfg::kTmemCols);

@@ -1,0 +1,40 @@
+// Launch wrapper for one (tile width, mode) instantiation of gemm_kernel.
+// Each instantiation lives in its own translation unit (inst_*.cu) so the
+// variants compile in parallel.
+#pragma once
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "gemm_kernel.cuh"
+
+namespace ttc {
+
+template <int BN, int MODE>
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+
+template <int BN, int MODE>
+int gemm_smem_bytes() {
+  return TileCfg<BN, MODE>::kSmemBytes;
+}
+
+#define TTC_DEFINE_LAUNCH(BN, MODE)                                                                  \
+  template <>                                                                                        \
+  cudaError_t launch_gemm<BN, MODE>(const GemmParams& p, int grid, cudaStream_t stream) {           \
+    static std::atomic<bool> attr_done[64];                                                          \
+    int dev = 0;                                                                                     \
+    cudaError_t e = cudaGetDevice(&dev);                                                             \
+    if (e != cudaSuccess) return e;                                                                  \
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;                                         \
+    constexpr int smem = TileCfg<BN, MODE>::kSmemBytes;                                              \
+    if (!attr_done[dev].load()) {                                                                    \
+      e = cudaFuncSetAttribute(gemm_kernel<BN, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,    \
+                               smem);                                                                \
+      if (e != cudaSuccess) return e;                                                                \
+      attr_done[dev].store(true);                                                                    \
+    }                                                                                                \
+    gemm_kernel<BN, MODE><<<grid, ModeTraits<MODE>::kThreads, smem, stream>>>(p);                    \
+    return cudaGetLastError();                                                                       \
+  }
+
+}  // namespace ttc
