@@ -42,9 +42,10 @@ def load_peaks():
 
 def workload_spec(name):
     import synth
-    if name in synth.WORKLOADS:
-        return dict(synth.WORKLOADS[name])
-    raise SystemExit(f"unknown workload {name}; choose from {sorted(synth.WORKLOADS)}")
+    try:
+        return synth.workload(name)
+    except (KeyError, ValueError):
+        raise SystemExit(f"unknown workload {name}; choose from {synth.all_workload_names()}")
 
 
 def algorithmic_bytes(spec):
@@ -341,13 +342,21 @@ def main():
     sustained = total_ms >= 1000.0
     peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
     peak = peaks[peak_key]
-    achieved = flops / avg_kernel_s / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": load_traffic(name),
-                "peak_source": f"{peak_src} {peak_key}",
-                "alg_bytes": algorithmic_bytes(spec),
-                "achieved_gbs": algorithmic_bytes(spec) / avg_kernel_s / 1e9,
-                "kernel_ms_median": statistics.median(kern_ms), "kernel_ms_min": min(kern_ms)}
+    alg_bytes = algorithmic_bytes(spec)
+    ridge = peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if flops / alg_bytes >= ridge:
+        achieved = flops / avg_kernel_s / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "peak_source": f"{peak_src} {peak_key}"}
+    else:
+        achieved = alg_bytes / avg_kernel_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs"}
+    roofline.update({"traffic": load_traffic(name), "alg_bytes": alg_bytes,
+                     "alg_flops": flops, "intensity_flop_per_byte": flops / alg_bytes,
+                     "tflops": flops / avg_kernel_s / 1e12, "achieved_gbs": alg_bytes / avg_kernel_s / 1e9,
+                     "kernel_ms_mean": statistics.mean(kern_ms),
+                     "kernel_ms_median": statistics.median(kern_ms), "kernel_ms_min": min(kern_ms)})
 
     # ---------------------------------------------------------------- end to end
     # Every step uploads its inputs from pinned host memory, runs the GEMM and

@@ -276,6 +276,27 @@ def ragged_workload(M, N, K, la, lb):
                 distB="uniform", distC="uniform", alpha=1.0, beta=1.0, act="none")
 
 
+def workload(name):
+    """Workload dict by name: a WORKLOADS key, or ragged_<M>x<N>x<K>_<a><b> with
+    a, b in {r, c} (row/column-major A and B) for the ragged sweep."""
+    if name in WORKLOADS:
+        return dict(WORKLOADS[name])
+    if name.startswith("ragged_"):
+        dims, lay = name[len("ragged_"):].split("_")
+        M, N, K = (int(v) for v in dims.split("x"))
+        full = {"r": "row", "c": "col"}
+        return ragged_workload(M, N, K, full[lay[0]], full[lay[1]])
+    raise KeyError(name)
+
+
+def all_workload_names():
+    names = list(WORKLOADS)
+    for (M, N, K) in RAGGED_SHAPES:
+        for la, lb in MAJORNESS:
+            names.append(f"ragged_{M}x{N}x{K}_{la[0]}{lb[0]}")
+    return names
+
+
 def make(spec, **override):
     """Build the synth.Problem for a workload dict; returns (problem, alpha, beta, act)."""
     s = dict(spec)

@@ -92,7 +92,7 @@ template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
     case 256:
-      if constexpr (MODE != kModeI8) return launch_gemm<256, MODE>(prm, grid, s);
+      if constexpr (MODE != kModeI8 && MODE != kModeI8Tma) return launch_gemm<256, MODE>(prm, grid, s);
       return cudaErrorInvalidValue;
     case 128: return launch_gemm<128, MODE>(prm, grid, s);
     case 64: return launch_gemm<64, MODE>(prm, grid, s);
@@ -108,6 +108,7 @@ cudaError_t launch(int mode, int bn, const GemmParams& prm, int grid, cudaStream
     case kModeGenF16: return launch_mode<kModeGenF16>(bn, prm, grid, s);
     case kModeGenBF16: return launch_mode<kModeGenBF16>(bn, prm, grid, s);
     case kModeI8: return launch_mode<kModeI8>(bn, prm, grid, s);
+    case kModeI8Tma: return launch_mode<kModeI8Tma>(bn, prm, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -241,9 +242,11 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   // ------------------------------------------------------------ plan
   const bool load_tma = dtype != TTC_I8 && !g_force_generic_load.load() &&
                         (K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2)));
+  const bool load_tma_i8 = dtype == TTC_I8 && !g_force_generic_load.load() &&
+                           (K == 0 || (tma_ok(A, lda, 1) && tma_ok(B, ldb, 1)));
   int mode;
   if (dtype == TTC_I8)
-    mode = kModeI8;
+    mode = load_tma_i8 ? kModeI8Tma : kModeI8;
   else if (load_tma)
     mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
   else
@@ -263,6 +266,15 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   GemmParams prm;
   std::memset(&prm, 0, sizeof prm);
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (K > 0 && mode == kModeI8Tma) {
+    // raw int8 tiles, unswizzled: K-major boxes of 64 k x rows, MN-major boxes of rows x 64 k
+    const CUtensorMapDataType d8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    bool ok = !a_mn ? encode_2d(&prm.tmA, d8, 1, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)
+                    : encode_2d(&prm.tmA, d8, 1, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && (!b_mn ? encode_2d(&prm.tmB, d8, 1, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_NONE)
+                      : encode_2d(&prm.tmB, d8, 1, B, N, K, ldb, bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE));
+    if (!ok) return TTC_ERR_CUDA;
+  }
   if (K > 0 && (mode == kModeTmaF16 || mode == kModeTmaBF16)) {
     bool ok;
     if (!a_mn)

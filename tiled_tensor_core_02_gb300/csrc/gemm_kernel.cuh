@@ -53,14 +53,17 @@ enum Mode : int {
   kModeGenF16 = 2,   // plain loads, fp16
   kModeGenBF16 = 3,  // plain loads, bf16
   kModeI8 = 4,       // plain loads of int8, converted to fp16; int32 out
+  kModeI8Tma = 5,    // TMA loads of int8 into a staging ring, converter warps widen to fp16; int32 out
 };
 
 template <int MODE>
 struct ModeTraits {
   static constexpr bool kTmaLoad = MODE == kModeTmaF16 || MODE == kModeTmaBF16;
   static constexpr bool kBF16 = MODE == kModeTmaBF16 || MODE == kModeGenBF16;  // tensor-core input type
-  static constexpr bool kI8 = MODE == kModeI8;
-  static constexpr int kProdWarps = kTmaLoad ? 1 : 4;
+  static constexpr bool kStaged = MODE == kModeI8Tma;  // TMA int8 staging + converter warps
+  static constexpr bool kI8 = MODE == kModeI8 || MODE == kModeI8Tma;
+  // producer warps: 1 TMA thread; 4 plain-load warps; or 1 TMA warp + 4 converter warps
+  static constexpr int kProdWarps = kTmaLoad ? 1 : (kStaged ? 5 : 4);
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kProdWarps + 1;
   static constexpr int kThreads = 32 * (kProdWarps + 1 + kEpiWarps);
@@ -98,12 +101,17 @@ struct TileCfg {
   static constexpr int kBBytes = BN * kBK * 2;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * T::kEpiBufBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per block
   static constexpr int kStageBudget = kSmemLimit - 1024 - kBarBytes - kEpiBytes;
-  static constexpr int kStages = kStageBudget / kStageBytes > 8 ? 8 : kStageBudget / kStageBytes;
+  // int8 staging ring (staged mode): the raw int8 A and B tiles of one k-block
+  static constexpr int kStage8Bytes = T::kStaged ? (kBM + BN) * kBK : 0;
+  static constexpr int kStagesRaw = kStageBudget / (kStageBytes + kStage8Bytes);
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kStages8 = T::kStaged ? kStages : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ + kStages * kStageBytes + kEpiBytes + kBarBytes;
+  static constexpr int kSmemBytes =
+      1024 /*align slack*/ + kStages * kStageBytes + kStages8 * kStage8Bytes + kEpiBytes + kBarBytes;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole epilogue chunks");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -228,6 +236,42 @@ __device__ __forceinline__ void generic_load_tile(uint8_t* sdst, const void* gsr
   }
 }
 
+// ------------------------------------------------------------------ int8 -> fp16 conversion
+// Widens one raw int8 tile (ROWS rows of COLS bytes, as TMA wrote it, no
+// swizzle) into the fp16 128-byte-swizzled layout the tensor core reads (the
+// same placement as generic_load_tile).  Exact: with u = x + 128 (a byte),
+// the fp16 bit pattern 0x6400 | u is 1024 + u, and subtracting 1152 leaves x.
+template <int ROWS, int COLS>
+__device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16, int tid) {
+  constexpr int kChunksPerRow = COLS / 16;
+  constexpr int kChunks = ROWS * kChunksPerRow;
+  static_assert(kChunks % 128 == 0, "128 converter threads");
+  constexpr layout::SwizzleBytes128 swz{};
+  const __half2 bias2 = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+#pragma unroll
+  for (int i = 0; i < kChunks / 128; ++i) {
+    const int q = tid + 128 * i;
+    const int r = q / kChunksPerRow;
+    const int c = (q % kChunksPerRow) * 16;
+    const uint4 w = *reinterpret_cast<const uint4*>(s8 + r * COLS + c);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t u = ws[j] ^ 0x80808080u;
+      uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+      uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+      __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias2);
+      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias2);
+      h[2 * j] = *reinterpret_cast<uint32_t*>(&l2);
+      h[2 * j + 1] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    const uint32_t base = (uint32_t)((c / 64) * ROWS * 128 + r * 128 + (c % 64) * 2);
+    *reinterpret_cast<uint4*>(s16 + swz(base)) = make_uint4(h[0], h[1], h[2], h[3]);
+    *reinterpret_cast<uint4*>(s16 + swz(base + 16)) = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = TileCfg<BN, MODE>;
@@ -239,7 +283,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = sA + S * kABytes;
-  uint8_t* sEpi = sB + S * Cfg::kBBytes;
+  uint8_t* s8 = sB + S * Cfg::kBBytes;  // int8 staging ring (staged mode only)
+  constexpr int S8 = Cfg::kStages8;
+  uint8_t* sEpi = s8 + S8 * Cfg::kStage8Bytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cfg::kEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -247,7 +293,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   uint64_t* tmem_empty = bars + 2 * S + 2;
   uint64_t* stall_bar = bars + 2 * S + 4;
   uint64_t* drain_bar = bars + 2 * S + 5;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  uint64_t* full8 = bars + 2 * S + 6;
+  uint64_t* empty8 = full8 + S8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + S8);
+  static_assert((2 * S + 6 + 2 * S8) * 8 + 4 <= Cfg::kBarBytes, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -258,8 +307,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], Tr::kTmaLoad ? 1 : Tr::kProdWarps);
+      // generic: one arrive per plain-load warp; staged: one per converter warp
+      mbar_init(&full[s], Tr::kTmaLoad ? 1 : 4);
       mbar_init(&empty[s], 1);
+    }
+    for (int s = 0; s < S8; ++s) {
+      mbar_init(&full8[s], 1);
+      mbar_init(&empty8[s], 4);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
@@ -268,7 +322,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     mbar_init(stall_bar, 1);
     mbar_init(drain_bar, 1);
     fence_barrier_init();
-    if constexpr (Tr::kTmaLoad) {
+    if constexpr (Tr::kTmaLoad || Tr::kStaged) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
     }
@@ -330,6 +384,90 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           // Let every load this thread started land before the CTA exits.
           for (int s = 0; s < S; ++s)
             if (issued_mask & (1u << s)) drain_wait(&full[s], (issued_parity >> s) & 1u, 100000000ull);
+        }
+      }
+    } else if constexpr (Tr::kStaged) {
+      if (warp == 0) {
+        // TMA thread: raw int8 tiles into the staging ring
+        if (lane == 0) {
+          const uint64_t pol = policy_evict_last();
+          int st8 = 0;
+          uint32_t ph8 = 0;
+          uint32_t issued_mask = 0, issued_parity = 0;
+          bool ok = true;
+          for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, p, mb, nb);
+            const int m0 = mb * kBM, n0 = nb * BN;
+            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+              if (!mbar_wait(&empty8[st8], ph8 ^ 1u, wc)) {
+                ok = false;
+                break;
+              }
+              mbar_arrive_expect_tx(&full8[st8], Cfg::kStage8Bytes);
+              uint8_t* a = s8 + st8 * Cfg::kStage8Bytes;
+              uint8_t* b = a + kBM * kBK;
+              const int k0 = kb * kBK;
+              if (!p.a_mn)
+                tma_load_2d(a, &p.tmA, k0, m0, &full8[st8], pol);
+              else
+                tma_load_2d(a, &p.tmA, m0, k0, &full8[st8], pol);
+              if (!p.b_mn)
+                tma_load_2d(b, &p.tmB, k0, n0, &full8[st8], pol);
+              else
+                tma_load_2d(b, &p.tmB, n0, k0, &full8[st8], pol);
+              issued_mask |= 1u << st8;
+              issued_parity = (issued_parity & ~(1u << st8)) | (ph8 << st8);
+              if (++st8 == S8) {
+                st8 = 0;
+                ph8 ^= 1u;
+              }
+            }
+          }
+          if (!ok) {
+            for (int s2 = 0; s2 < S8; ++s2)
+              if (issued_mask & (1u << s2)) drain_wait(&full8[s2], (issued_parity >> s2) & 1u, 100000000ull);
+          }
+        }
+      } else {
+        // converter warps: int8 staging slot -> fp16 MMA slot
+        const int ctid = threadIdx.x - 32;  // 0..127
+        int st8 = 0, stage = 0;
+        uint32_t ph8 = 0, phase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            if (!mbar_wait(&full8[st8], ph8, wc) || !mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+              ok = false;
+              break;
+            }
+            const uint8_t* a8 = s8 + st8 * Cfg::kStage8Bytes;
+            const uint8_t* b8 = a8 + kBM * kBK;
+            uint8_t* a = sA + stage * kABytes;
+            uint8_t* b = sB + stage * Cfg::kBBytes;
+            if (!p.a_mn)
+              convert_i8_tile<kBM, kBK>(a8, a, ctid);
+            else
+              convert_i8_tile<kBK, kBM>(a8, a, ctid);
+            if (!p.b_mn)
+              convert_i8_tile<BN, kBK>(b8, b, ctid);
+            else
+              convert_i8_tile<kBK, BN>(b8, b, ctid);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              mbar_arrive(&full[stage]);
+              mbar_arrive(&empty8[st8]);
+            }
+            if (++st8 == S8) {
+              st8 = 0;
+              ph8 ^= 1u;
+            }
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
         }
       }
     } else {
