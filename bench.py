@@ -247,6 +247,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pair", type=int, default=0, choices=[0, 1, 2],
+                    help="kernel choice: 0 planner, 1 CTA-pair kernel where it applies, 2 single-CTA kernel")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload)
@@ -265,6 +267,7 @@ def main():
         _build.build()
     barrier(world)
     ttc.load()
+    ttc.ttc_set_knob("pair", args.pair)
 
     p, alpha, beta, act = synth.make(spec)
     M, N, K = p.M, p.N, p.K

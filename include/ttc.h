@@ -108,6 +108,9 @@ const char* ttc_status_string(ttc_status status);
  *     predicated stores even when TMA could describe D.
  *   TTC_KNOB_TILE_N: force the CTA tile width (256, 128, 64, 32 or 16); 0
  *     lets the planner choose.
+ *   TTC_KNOB_PAIR: 0 lets the planner choose between the single-CTA kernel and
+ *     the CTA-pair (2-SM, 256 x 256 tile) kernel; 1 uses the pair kernel
+ *     whenever it applies (fp16/bf16 operands TMA can describe); 2 never.
  * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
  */
 typedef enum {
@@ -115,7 +118,8 @@ typedef enum {
   TTC_KNOB_INJECT_STALL = 1,
   TTC_KNOB_FORCE_GENERIC_LOAD = 2,
   TTC_KNOB_FORCE_GENERIC_STORE = 3,
-  TTC_KNOB_TILE_N = 4
+  TTC_KNOB_TILE_N = 4,
+  TTC_KNOB_PAIR = 5
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -23,7 +23,7 @@ def _built():
     from tiled_tensor_core_02_gb300 import _build
     _build.build()
     ttc.load()
-    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n"):
+    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -178,11 +178,13 @@ def test_bf16_8192_sampled_and_freivalds():
 
 # ------------------------------------------------------------------ failure detection
 
-def test_stalled_pipeline_times_out_and_context_survives():
+@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+def test_stalled_pipeline_times_out_and_context_survives(pair):
     """A tensor-core issuer that waits on a barrier nothing arrives at must end
     the kernel with TTC_ERR_TIMEOUT within the wait budget, and the context
     must stay usable."""
     p = synth.Problem(256, 512, 512, dtype="bf16", seed=19)
+    ttc.ttc_set_knob("pair", pair)
     ttc.ttc_set_knob("timeout_ns", 200_000_000)
     ttc.ttc_set_knob("inject_stall", 1)
     try:
@@ -197,8 +199,11 @@ def test_stalled_pipeline_times_out_and_context_survives():
         ttc.ttc_set_knob("inject_stall", 0)
         ttc.ttc_set_knob("timeout_ns", 0)
     assert ttc.ttc_get_device_error(None) == 0
-    d = run(p, 1.0, 0.0)
-    check_full(p, d, 1.0, 0.0)
+    try:
+        d = run(p, 1.0, 0.0)
+        check_full(p, d, 1.0, 0.0)
+    finally:
+        ttc.ttc_set_knob("pair", 0)
 
 
 # ------------------------------------------------------------------ operands TMA cannot describe
@@ -278,3 +283,30 @@ def test_int8_8192_sampled_and_freivalds():
     d = run(p, a, b, act)
     check_sampled(p, d, a, b, act, seed=3)
     freivalds(p, d, a, b, seed=3)
+
+
+# ------------------------------------------------------------------ single-CTA vs CTA-pair kernels
+
+@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_pair_and_single_kernels(pair, la, lb):
+    ttc.ttc_set_knob("pair", pair)
+    try:
+        p = synth.Problem(520, 600, 264, dtype="bf16", layoutA=la, layoutB=lb, seed=24, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 0.75, 1.5, "gelu_tanh")
+        check_full(p, d, 0.75, 1.5, "gelu_tanh")
+    finally:
+        ttc.ttc_set_knob("pair", 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 70, 64), (1, 300, 128), (257, 9, 100), (600, 40, 0)])
+def test_pair_kernel_on_small_and_ragged(M, N, K):
+    ttc.ttc_set_knob("pair", 1)
+    try:
+        p = synth.Problem(M, N, K, dtype="f16", seed=25, distC="uniform", lda=max(8, (K + 7) // 8 * 8),
+                          ldb=max(8, (K + 7) // 8 * 8))
+        d = run(p, 1.0, 1.0, ldd=(N + 7) // 8 * 8)
+        check_full(p, d, 1.0, 1.0)
+    finally:
+        ttc.ttc_set_knob("pair", 0)

@@ -11,6 +11,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
 #include "ttc.h"
 #include "ttc_layout.hpp"
@@ -26,6 +27,7 @@ std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_generic_load{0};
 std::atomic<int> g_force_generic_store{0};
 std::atomic<int> g_force_tile_n{0};
+std::atomic<int> g_pair_mode{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -33,6 +35,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
+  int pair_clusters[2] = {-1, -1};  // resident CTA pairs (fp16, bf16); -1: not queried yet
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -155,6 +158,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value != 0 && value != 256 && value != 128 && value != 64 && value != 32 && value != 16)
         return TTC_ERR_INVALID_ARG;
       g_force_tile_n.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_PAIR:
+      if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
+      g_pair_mode.store((int)value);
       return TTC_OK;
   }
   return TTC_ERR_INVALID_ARG;
@@ -327,6 +334,35 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   prm.err = dev->err;
   prm.timeout_ns = (uint64_t)g_timeout_ns.load();
   prm.inject_stall = g_inject_stall.load();
+
+  // CTA-pair kernel: fp16/bf16 operands staged by TMA, a 256 x 256 tile per
+  // pair of SMs; chosen for problems at least one pair tile in each direction
+  const int pair_mode = g_pair_mode.load();
+  const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && g_force_tile_n.load() == 0;
+  if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= kPairBN))) {
+    const bool bf16 = dtype == TTC_BF16;
+    int& clusters = dev->pair_clusters[bf16 ? 1 : 0];
+    if (clusters < 0) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (clusters < 0) clusters = pair_max_clusters(bf16);
+    }
+    if (clusters > 0) {
+      if (K > 0) {
+        // B boxes cover this CTA's 128 columns of the pair tile
+        const bool ok = !b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+                              : encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return TTC_ERR_CUDA;
+      }
+      prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
+      prm.num_n_blocks = (int)((N + kPairBN - 1) / kPairBN);
+      prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
+      prm.group_m = prm.num_m_blocks < 8 ? prm.num_m_blocks : 8;
+      const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
+      if (launch_pair(bf16, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+      g_launches.fetch_add(1);
+      return TTC_OK;
+    }
+  }
 
   const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
   if (launch(mode, bn, prm, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;

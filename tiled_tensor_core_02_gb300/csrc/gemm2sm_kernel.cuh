@@ -1,0 +1,261 @@
+// CTA-pair (2-SM) variant of the fp16/bf16 TMA GEMM: one cluster of two CTAs
+// computes a 256 x 256 output tile with tcgen05.mma.cta_group::2 (M = 256,
+// N = 256, K = 16).
+//
+// Each CTA stages only its own half of the operands: rows [128 r, 128 r + 128)
+// of the A tile and columns [128 r, 128 r + 128) of the B tile (r = the CTA's
+// rank in the pair), at the same shared-memory offsets in both CTAs.  One
+// thread of the even CTA issues the pair MMA, which reads A and B halves from
+// both CTAs and writes rows [128 r, 128 r + 128) of the accumulator into CTA
+// r's TMEM.  Per SM this halves the B operand traffic of the single-CTA
+// 128 x 256 tile while keeping the same per-SM work.
+//
+// Synchronisation (barrier -> who arrives -> who waits):
+//   full[s]      even CTA only; its producer arms it with both CTAs' bytes, both
+//                CTAs' TMA loads complete on it (.cta_group::2); MMA waits.
+//   empty[s]     both CTAs; the MMA's commit is multicast to both; producers wait.
+//   tmem_full[a] both CTAs; multicast commit after a tile's last k-block;
+//                epilogue warps wait.
+//   tmem_empty[a] even CTA only; all 8 epilogue warps of the pair arrive (the
+//                odd CTA's remotely); the MMA waits before reusing accumulator a.
+// The layout of a CTA's half tiles, the epilogue and the error handling are
+// those of gemm_kernel (one CTA); every wait is bounded.
+#pragma once
+#include "gemm_kernel.cuh"
+
+namespace ttc {
+
+constexpr int kPairBM = 256;
+constexpr int kPairBN = 256;
+constexpr int kPairThreads = 192;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..5 epilogue
+
+struct PairCfg {
+  static constexpr int kAHalfBytes = 128 * kBK * 2;  // 16 KiB
+  static constexpr int kBHalfBytes = 128 * kBK * 2;  // 16 KiB
+  static constexpr int kStageBytes = kAHalfBytes + kBHalfBytes;
+  static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
+  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kBarBytes = 256;
+  static constexpr int kSmemLimit = 227 * 1024;
+  static constexpr int kStagesRaw = (kSmemLimit - 1024 - kBarBytes - kEpiBytes) / kStageBytes;
+  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kTmemCols = 2 * kPairBN;  // two accumulators
+  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
+};
+
+template <bool kBF16>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int S = PairCfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + S * PairCfg::kAHalfBytes;
+  uint8_t* sEpi = sB + S * PairCfg::kBHalfBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + PairCfg::kEpiBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* tmem_full = bars + 2 * S;
+  uint64_t* tmem_empty = bars + 2 * S + 2;
+  uint64_t* stall_bar = bars + 2 * S + 4;
+  uint64_t* drain_bar = bars + 2 * S + 5;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 6);
+  static_assert((2 * S + 6) * 8 + 4 <= PairCfg::kBarBytes, "barrier area");
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1;
+  const int num_pairs = gridDim.x >> 1;
+  const WaitCtx wc{p.err, p.timeout_ns};
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tmem_full[a], 1);
+      mbar_init(&tmem_empty[a], 2 * kEpiWarps);
+    }
+    mbar_init(stall_bar, 1);
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+    prefetch_tmap(&p.tmA);
+    prefetch_tmap(&p.tmB);
+    if (p.d_tma) prefetch_tmap(&p.tmD);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, PairCfg::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barrier initialisation and the TMEM address visible to both CTAs
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t armed_mask = 0, armed_parity = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+        int mb, nb;
+        tile_coords(t, p, mb, nb);
+        const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
+        const int n0 = nb * kPairBN + (int)rank * 128;  // this CTA's B columns
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
+          if (leader) {
+            mbar_arrive_expect_tx(&full[stage], 2 * PairCfg::kStageBytes);
+            armed_mask |= 1u << stage;
+            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+          }
+          uint8_t* a = sA + stage * PairCfg::kAHalfBytes;
+          uint8_t* b = sB + stage * PairCfg::kBHalfBytes;
+          const int k0 = kb * kBK;
+          if (!p.a_mn) {
+            tma_load_2d_pair(a, &p.tmA, k0, m0, full_leader, pol);
+          } else {
+            tma_load_2d_pair(a, &p.tmA, m0, k0, full_leader, pol);
+            tma_load_2d_pair(a + 8192, &p.tmA, m0 + 64, k0, full_leader, pol);
+          }
+          if (!p.b_mn) {
+            tma_load_2d_pair(b, &p.tmB, k0, n0, full_leader, pol);
+          } else {
+            tma_load_2d_pair(b, &p.tmB, n0, k0, full_leader, pol);
+            tma_load_2d_pair(b + 8192, &p.tmB, n0 + 64, k0, full_leader, pol);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && leader) {
+        // every stage this CTA armed completes once both CTAs' loads for it
+        // have landed; wait for them before the pair may exit
+        for (int s = 0; s < S; ++s)
+          if (armed_mask & (1u << s)) drain_wait(&full[s], (armed_parity >> s) & 1u, 100000000ull);
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    if (leader && lane == 0) {
+      const uint32_t idesc = idesc_f16(kBF16, p.a_mn != 0, p.b_mn != 0, kPairBM, kPairBN);
+      bool ok = true;
+      bool any_mma = false;
+      if (p.inject_stall) ok = mbar_wait(stall_bar, 0, wc);  // nothing arrives here
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
+      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * kPairBN;
+        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(sA + stage * PairCfg::kAHalfBytes);
+          const uint32_t b_addr = smem_u32(sB + stage * PairCfg::kBHalfBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / kUmmaK; ++k) {
+            const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024);
+            const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024);
+            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
+          }
+          any_mma = true;
+          mma_commit_pair(&empty[stage], 0x3);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        if (p.num_k_blocks == 0) {
+          mbar_arrive(&tmem_full[acc]);
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[acc]), 1));
+        } else {
+          mma_commit_pair(&tmem_full[acc], 0x3);
+        }
+      }
+      if (any_mma) {
+        // every MMA must have finished with both CTAs' TMEM before it is freed
+        mma_commit_pair(drain_bar, 0x1);
+        drain_wait(drain_bar, 0, 100000000ull);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (both CTAs)
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    uint8_t* stage_buf = sEpi + ew * 2 * PairCfg::kEpiBufBytes;
+    int buf = 0;
+    int it = 0;
+    const bool has_k = p.num_k_blocks > 0;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+      const int acc = it & 1;
+      if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
+      tc_fence_after();
+      int mb, nb;
+      tile_coords(t, p, mb, nb);
+      const int m0 = mb * kPairBM + (int)rank * 128;
+      const int n0 = nb * kPairBN;
+      const int grow = m0 + q * 32 + lane;
+      const bool row_ok = grow < p.M;
+#pragma unroll 1
+      for (int c = 0; c < kPairBN / kEpiCols; ++c) {
+        const int gcol0 = n0 + c * kEpiCols;
+        uint32_t r[32];
+        if (has_k) {
+          tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * kEpiCols, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
+        if (c == kPairBN / kEpiCols - 1) {
+          // this warp's accumulator rows are read: tell the even CTA's issuer
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+        }
+        uint32_t packed[16];
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed);
+        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane);
+      }
+    }
+    if (p.d_tma && lane == 0) bulk_wait_all();
+  }
+
+  __syncthreads();
+  cluster_sync();  // the pair's MMAs, remote arrivals and loads are all finished
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, PairCfg::kTmemCols);
+  }
+}
+
+}  // namespace ttc

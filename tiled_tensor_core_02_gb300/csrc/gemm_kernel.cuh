@@ -272,6 +272,102 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
   }
 }
 
+// ------------------------------------------------------------------ epilogue helpers
+// fp16/bf16 epilogue of one 32-column chunk of the calling thread's row:
+// v = alpha * acc (+ beta * C) (+ bias), activation, round to nearest even.
+template <bool kBF16>
+__device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32_t (&r)[32], bool row_ok,
+                                               int grow, int gcol0, uint32_t (&packed)[16]) {
+  float v[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
+  if (p.beta != 0.0f && row_ok) {
+    const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
+    const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
+                     (gcol0 + 32 <= p.N);
+    if (vec) {
+#pragma unroll
+      for (int u4 = 0; u4 < 4; ++u4) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(crow) + u4);
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+          v[u4 * 8 + 2 * h] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] & 0xFFFFu)),
+                                   v[u4 * 8 + 2 * h]);
+          v[u4 * 8 + 2 * h + 1] =
+              fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] >> 16)), v[u4 * 8 + 2 * h + 1]);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(crow + j)), v[j]);
+    }
+  }
+  if (p.bias != nullptr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
+  }
+  if (p.act != kActNone) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = apply_act(p.act, v[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 16; ++j) packed[j] = pack2<kBF16>(v[2 * j], v[2 * j + 1]);
+}
+
+// Writes one 32-column chunk of the calling thread's row: through a swizzled
+// shared-memory staging buffer and a TMA store of the warp's 32 x 32 block
+// (rows tile_row .. tile_row + 31), or with predicated stores when TMA cannot
+// describe D.  `buf` alternates between the warp's two staging buffers.
+template <int kOutBytes, int kPacked>
+__device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint32_t (&packed)[kPacked], bool row_ok,
+                                                int grow, int gcol0, int tile_row, uint8_t* stage_buf,
+                                                int buf_bytes, int& buf, int lane) {
+  if (p.d_tma) {
+    // staging buffer `buf` was last used two chunks ago; its store must
+    // have finished reading shared memory
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    uint8_t* sb = stage_buf + buf * buf_bytes;
+    if constexpr (kOutBytes == 2) {
+      // 64-byte rows, 64-byte swizzle
+      constexpr layout::SwizzleBytes64 swz{};
+#pragma unroll
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 64 + ch * 16))) =
+            make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+    } else {
+      // 128-byte rows, 128-byte swizzle
+      constexpr layout::SwizzleBytes128 swz{};
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 128 + ch * 16))) =
+            make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+    }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(&p.tmD, gcol0, tile_row, sb);
+      bulk_commit();
+    }
+    buf ^= 1;
+  } else if (row_ok) {
+    if constexpr (kOutBytes == 4) {
+      int32_t* dst = reinterpret_cast<int32_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N) dst[j] = (int32_t)packed[j];
+    } else {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N) dst[j] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+    }
+  }
+}
+
 template <int BN, int MODE>
 __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(const __grid_constant__ GemmParams p) {
   using Cfg = TileCfg<BN, MODE>;
@@ -666,86 +762,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             __syncwarp();
             if (lane == 0) mbar_arrive(&tmem_empty[acc]);
           }
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
-          if (p.beta != 0.0f && row_ok) {
-            const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
-            const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
-                             (gcol0 + 32 <= p.N);
-            if (vec) {
-#pragma unroll
-              for (int u4 = 0; u4 < 4; ++u4) {
-                const uint4 w = __ldg(reinterpret_cast<const uint4*>(crow) + u4);
-                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                  v[u4 * 8 + 2 * h] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] & 0xFFFFu)),
-                                           v[u4 * 8 + 2 * h]);
-                  v[u4 * 8 + 2 * h + 1] =
-                      fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] >> 16)), v[u4 * 8 + 2 * h + 1]);
-                }
-              }
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j)
-                if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(crow + j)), v[j]);
-            }
-          }
-          if (p.bias != nullptr) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
-          }
-          if (p.act != kActNone) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = apply_act(p.act, v[j]);
-          }
-#pragma unroll
-          for (int j = 0; j < 16; ++j) packed[j] = pack2<kBF16>(v[2 * j], v[2 * j + 1]);
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed);
         }
 
-        if (p.d_tma) {
-          // staging buffer `buf` was last used two chunks ago; its store must
-          // have finished reading shared memory
-          if (lane == 0) bulk_wait_read<1>();
-          __syncwarp();
-          uint8_t* sb = stage_buf + buf * Tr::kEpiBufBytes;
-          if constexpr (Tr::kOutBytes == 2) {
-            // 64-byte rows, 64-byte swizzle
-            constexpr layout::SwizzleBytes64 swz{};
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch)
-              *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 64 + ch * 16))) =
-                  make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-          } else {
-            // 128-byte rows, 128-byte swizzle
-            constexpr layout::SwizzleBytes128 swz{};
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(sb + swz((uint32_t)(lane * 128 + ch * 16))) =
-                  make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&p.tmD, gcol0, m0 + q * 32, sb);
-            bulk_commit();
-          }
-          buf ^= 1;
-        } else if (row_ok) {
-          if constexpr (Tr::kOutBytes == 4) {
-            int32_t* dst = reinterpret_cast<int32_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gcol0 + j < p.N) dst[j] = (int32_t)packed[j];
-          } else {
-            uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (gcol0 + j < p.N) dst[j] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-          }
-        }
+        epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, Tr::kEpiBufBytes, buf,
+                                       lane);
       }
       if constexpr (!kI8) ++unit;
     }

@@ -13,6 +13,10 @@ namespace ttc {
 template <int BN, int MODE>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
+// CTA-pair (2-SM) fp16/bf16 kernel, defined in inst_pair.cu.
+int pair_max_clusters(bool bf16);
+cudaError_t launch_pair(bool bf16, const GemmParams& p, int clusters, cudaStream_t stream);
+
 template <int BN, int MODE>
 int gemm_smem_bytes() {
   return TileCfg<BN, MODE>::kSmemBytes;
