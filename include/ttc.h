@@ -111,6 +111,8 @@ const char* ttc_status_string(ttc_status status);
  *   TTC_KNOB_PAIR: 0 lets the planner choose between the single-CTA kernel and
  *     the CTA-pair (2-SM, 256 x 256 tile) kernel; 1 uses the pair kernel
  *     whenever it applies (fp16/bf16 operands TMA can describe); 2 never.
+ *   TTC_KNOB_SWAP_AB: 0 lets the planner choose whether to compute D or
+ *     D^T = B^T A^T (for skinny problems); 1 always D^T; 2 always D.
  * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
  */
 typedef enum {
@@ -119,7 +121,8 @@ typedef enum {
   TTC_KNOB_FORCE_GENERIC_LOAD = 2,
   TTC_KNOB_FORCE_GENERIC_STORE = 3,
   TTC_KNOB_TILE_N = 4,
-  TTC_KNOB_PAIR = 5
+  TTC_KNOB_PAIR = 5,
+  TTC_KNOB_SWAP_AB = 6
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

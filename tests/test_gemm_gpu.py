@@ -23,7 +23,7 @@ def _built():
     from tiled_tensor_core_02_gb300 import _build
     _build.build()
     ttc.load()
-    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair"):
+    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -310,3 +310,43 @@ def test_pair_kernel_on_small_and_ragged(M, N, K):
         check_full(p, d, 1.0, 1.0)
     finally:
         ttc.ttc_set_knob("pair", 0)
+
+
+# ------------------------------------------------------------------ D^T = B^T A^T (skinny problems)
+
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+@pytest.mark.parametrize("act", ["none", "gelu_tanh"])
+def test_swap_ab_forced(la, lb, act):
+    ttc.ttc_set_knob("swap_ab", 1)
+    try:
+        p = synth.Problem(150, 300, 136, dtype="bf16", layoutA=la, layoutB=lb, seed=26, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 1.25, 0.5, act, ldd=304)
+        check_full(p, d, 1.25, 0.5, act)
+    finally:
+        ttc.ttc_set_knob("swap_ab", 0)
+
+
+def test_swap_ab_int8_with_c():
+    ttc.ttc_set_knob("swap_ab", 1)
+    try:
+        p = synth.Problem(70, 200, 300, dtype="i8", seed=27, distA="int8", distB="int8")
+        rng = np.random.default_rng(1)
+        c = rng.integers(-2**20, 2**20, size=(p.M, p.N)).astype(np.int32)
+        p.C_log = c
+        p.C, p.ldc = synth.to_layout(c, "row")
+        d = run(p, 1.0, 1.0)
+        check_full(p, d, 1.0, 1.0)
+    finally:
+        ttc.ttc_set_knob("swap_ab", 0)
+
+
+@pytest.mark.parametrize("swap", [1, 2], ids=["swap", "noswap"])
+def test_skinny_orientation_both_ways(swap):
+    ttc.ttc_set_knob("swap_ab", swap)
+    try:
+        p, a, b, act = synth.make(synth.ragged_workload(8192, 24, 4096, "row", "col"))
+        d = run(p, a, b, act)
+        check_full(p, d, a, b, act)
+    finally:
+        ttc.ttc_set_knob("swap_ab", 0)

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
@@ -28,6 +29,7 @@ std::atomic<int> g_force_generic_load{0};
 std::atomic<int> g_force_generic_store{0};
 std::atomic<int> g_force_tile_n{0};
 std::atomic<int> g_pair_mode{0};
+std::atomic<int> g_swap_mode{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -163,6 +165,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
       g_pair_mode.store((int)value);
       return TTC_OK;
+    case TTC_KNOB_SWAP_AB:
+      if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
+      g_swap_mode.store((int)value);
+      return TTC_OK;
   }
   return TTC_ERR_INVALID_ARG;
 }
@@ -243,6 +249,51 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   }
   if (M == 1 && !tma_ok(D, ldd, out_esize) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 16);
 
+  // ------------------------------------------------------------ orientation and tile width
+  // The kernel tile is 128 rows by bn columns.  A skinny problem gets few
+  // tiles, and a skinny HBM-bound problem needs many CTAs streaming at once,
+  // so pick the orientation (D itself, or D^T = B^T A^T with a transposed
+  // store) and tile width with the most tiles, up to one per SM; ties keep
+  // the wider tile, then the untransposed orientation.
+  const int forced_bn = g_force_tile_n.load();
+  const int swap_mode = g_swap_mode.load();
+  const int max_bn = dtype == TTC_I8 ? 128 : 256;
+  bool swap = swap_mode == 1;
+  int bn = forced_bn;
+  {
+    int best_score = -1;
+    for (int sw = 0; sw < 2; ++sw) {
+      if ((swap_mode == 1 && sw == 0) || (swap_mode == 2 && sw == 1)) continue;
+      const int64_t mk = sw ? N : M, nk = sw ? M : N;
+      // the kernel's B operand is MN-major when it is stored that way
+      const bool bk_mn = sw ? layoutA == TTC_COL_MAJOR : layoutB == TTC_ROW_MAJOR;
+      for (int cand = max_bn; cand >= 32; cand /= 2) {
+        if (forced_bn != 0 && cand != forced_bn) continue;
+        if (bk_mn && cand < 64) continue;
+        // a tile wider than the padded N only wastes work
+        if (forced_bn == 0 && cand > 32 && cand / 2 >= nk) continue;
+        const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + cand - 1) / cand);
+        const int score = (int)(tiles < dev->sm_count ? tiles : dev->sm_count);
+        if (score > best_score) {
+          best_score = score;
+          bn = cand;
+          swap = sw == 1;
+        }
+      }
+    }
+    if (best_score < 0) return TTC_ERR_UNSUPPORTED;
+  }
+  if (swap) {
+    // D^T (N x M, stored as D with the roles of ldd's axes exchanged) = B^T A^T:
+    // B^T is B read with the other layout, and likewise A^T
+    std::swap(M, N);
+    std::swap(A, B);
+    std::swap(lda, ldb);
+    const ttc_layout la = layoutA;
+    layoutA = layoutB == TTC_ROW_MAJOR ? TTC_COL_MAJOR : TTC_ROW_MAJOR;
+    layoutB = la == TTC_ROW_MAJOR ? TTC_COL_MAJOR : TTC_ROW_MAJOR;
+  }
+
   const bool a_mn = layoutA == TTC_COL_MAJOR;
   const bool b_mn = layoutB == TTC_ROW_MAJOR;
 
@@ -258,16 +309,8 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
   else
     mode = dtype == TTC_BF16 ? kModeGenBF16 : kModeGenF16;
-  const bool store_tma = tma_ok(D, ldd, out_esize) && !g_force_generic_store.load();
-
-  int bn = g_force_tile_n.load();
-  if (bn == 0) {
-    if (dtype == TTC_I8)
-      bn = N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
-    else
-      bn = N > 128 ? 256 : N > 64 ? 128 : (N > 32 || b_mn) ? 64 : 32;
-  }
-  if (bn == 16 || (b_mn && bn < 64) || (dtype == TTC_I8 && bn > 128)) return TTC_ERR_UNSUPPORTED;
+  const bool store_tma = !swap && tma_ok(D, ldd, out_esize) && !g_force_generic_store.load();
+  if (bn == 16 || (b_mn && bn < 64) || bn > max_bn) return TTC_ERR_UNSUPPORTED;
 
   static_assert(sizeof(GemmParams) <= 4096, "kernel parameter space");
   GemmParams prm;
@@ -282,10 +325,13 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
                       : encode_2d(&prm.tmB, d8, 1, B, N, K, ldb, bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE));
     if (!ok) return TTC_ERR_CUDA;
   }
+  // rows of A worth loading per tile: all 128, or only those that exist
+  const int a_rows = M >= kBM ? kBM : (int)round_up(M, 8);
+  prm.a_boxes = a_rows > 64 ? 2 : 1;
   if (K > 0 && (mode == kModeTmaF16 || mode == kModeTmaBF16)) {
     bool ok;
     if (!a_mn)
-      ok = encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B);
     else
       ok = encode_2d(&prm.tmA, dt, 2, A, M, K, lda, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
     if (!ok) return TTC_ERR_CUDA;
@@ -330,7 +376,9 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   prm.ldd = ldd;
   prm.bias = bias;
   prm.act = (int)act;
+  prm.stage_tx = (uint32_t)((!a_mn ? a_rows * kBK * 2 : prm.a_boxes * 64 * kBK * 2) + bn * kBK * 2);
   prm.d_tma = store_tma ? 1 : 0;
+  prm.d_trans = swap ? 1 : 0;
   prm.err = dev->err;
   prm.timeout_ns = (uint64_t)g_timeout_ns.load();
   prm.inject_stall = g_inject_stall.load();
@@ -338,7 +386,7 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   // CTA-pair kernel: fp16/bf16 operands staged by TMA, a 256 x 256 tile per
   // pair of SMs; chosen for problems at least one pair tile in each direction
   const int pair_mode = g_pair_mode.load();
-  const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && g_force_tile_n.load() == 0;
+  const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap;
   if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= kPairBN))) {
     const bool bf16 = dtype == TTC_BF16;
     int& clusters = dev->pair_clusters[bf16 ? 1 : 0];
@@ -348,9 +396,10 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     }
     if (clusters > 0) {
       if (K > 0) {
-        // B boxes cover this CTA's 128 columns of the pair tile
-        const bool ok = !b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
-                              : encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+        // each CTA loads whole 128-row A boxes and its 128 columns of the B tile
+        bool ok = a_mn || encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+        ok = ok && (!b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+                          : encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B));
         if (!ok) return TTC_ERR_CUDA;
       }
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);

@@ -79,6 +79,10 @@ struct GemmParams {
   const void* B;
   int64_t lda, ldb;
   int a_vec, b_vec;  // generic modes: 1 when 8-element groups may be read as one vector
+  int a_boxes;       // TMA modes: 64-row (MN-major) boxes of A per k-block, 1 or 2
+  uint32_t stage_tx; // TMA modes: bytes the loads of one k-block deliver.  When M < 128
+                     // only the rows that exist are loaded; the rest of the A tile keeps
+                     // stale data, which only reaches accumulator rows that are never stored
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
   int a_mn, b_mn;  // operand stored MN-major (A column-major / B row-major)
@@ -89,7 +93,9 @@ struct GemmParams {
   int64_t ldd;
   const float* bias;
   int act;
-  int d_tma;  // 1: D written by TMA store; 0: predicated st.global
+  int d_tma;    // 1: D written by TMA store; 0: predicated st.global
+  int d_trans;  // 1: the kernel computes D^T = B^T A^T: kernel element (i, j) is D[j * ldd + i],
+                //    C likewise, and the bias is indexed by the kernel row
   uint32_t* err;
   uint64_t timeout_ns;
   int inject_stall;
@@ -107,7 +113,7 @@ struct TileCfg {
   // int8 staging ring (staged mode): the raw int8 A and B tiles of one k-block
   static constexpr int kStage8Bytes = T::kStaged ? (kBM + BN) * kBK : 0;
   static constexpr int kStagesRaw = kStageBudget / (kStageBytes + kStage8Bytes);
-  static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
+  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kStages8 = T::kStaged ? kStages : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kSmemBytes =
@@ -281,7 +287,21 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
-  if (p.beta != 0.0f && row_ok) {
+  if (p.d_trans) {
+    if (row_ok) {
+      if (p.beta != 0.0f) {
+        const uint16_t* ccol = reinterpret_cast<const uint16_t*>(p.C) + grow;
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(ccol + (int64_t)(gcol0 + j) * p.ldc)), v[j]);
+      }
+      if (p.bias != nullptr) {
+        const float b = __ldg(p.bias + grow);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += b;
+      }
+    }
+  } else if (p.beta != 0.0f && row_ok) {
     const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
     const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
                      (gcol0 + 32 <= p.N);
@@ -304,7 +324,7 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
         if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(crow + j)), v[j]);
     }
   }
-  if (p.bias != nullptr) {
+  if (p.bias != nullptr && !p.d_trans) {
 #pragma unroll
     for (int j = 0; j < 32; ++j)
       if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
@@ -353,6 +373,20 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
       bulk_commit();
     }
     buf ^= 1;
+  } else if (row_ok && p.d_trans) {
+    // lanes hold consecutive kernel rows = consecutive elements of a D row
+    if constexpr (kOutBytes == 4) {
+      int32_t* dst = reinterpret_cast<int32_t*>(p.D) + grow;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N) dst[(int64_t)(gcol0 + j) * p.ldd] = (int32_t)packed[j];
+    } else {
+      uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + grow;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N)
+          dst[(int64_t)(gcol0 + j) * p.ldd] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
+    }
   } else if (row_ok) {
     if constexpr (kOutBytes == 4) {
       int32_t* dst = reinterpret_cast<int32_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
@@ -451,7 +485,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], Cfg::kStageBytes);
+            mbar_arrive_expect_tx(&full[stage], p.stage_tx);
             uint8_t* a = sA + stage * kABytes;
             uint8_t* b = sB + stage * Cfg::kBBytes;
             const int k0 = kb * kBK;
@@ -459,7 +493,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               tma_load_2d(a, &p.tmA, k0, m0, &full[stage], pol);
             } else {
               tma_load_2d(a, &p.tmA, m0, k0, &full[stage], pol);
-              tma_load_2d(a + kABytes / 2, &p.tmA, m0 + 64, k0, &full[stage], pol);
+              if (p.a_boxes > 1) tma_load_2d(a + kABytes / 2, &p.tmA, m0 + 64, k0, &full[stage], pol);
             }
             if (!p.b_mn) {
               tma_load_2d(b, &p.tmB, k0, n0, &full[stage], pol);
@@ -726,7 +760,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           int32_t v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = isum[c][j];
-          if (p.beta != 0.0f && row_ok) {
+          if (p.beta != 0.0f && row_ok && p.d_trans) {
+            const int32_t* ccol = reinterpret_cast<const int32_t*>(p.C) + grow;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (gcol0 + j < p.N) v[j] += __ldg(ccol + (int64_t)(gcol0 + j) * p.ldc);
+          } else if (p.beta != 0.0f && row_ok) {
             const int32_t* crow = reinterpret_cast<const int32_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
             const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
                              (gcol0 + 32 <= p.N);
