@@ -23,7 +23,8 @@ def _built():
     from tiled_tensor_core_02_gb300 import _build
     _build.build()
     ttc.load()
-    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab"):
+    for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab",
+              "split_k"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -349,4 +350,43 @@ def test_skinny_orientation_both_ways(swap):
         d = run(p, a, b, act)
         check_full(p, d, a, b, act)
     finally:
+        ttc.ttc_set_knob("swap_ab", 0)
+
+
+# ------------------------------------------------------------------ split-K across a cluster
+
+@pytest.mark.parametrize("split", [2, 3, 4, 8])
+@pytest.mark.parametrize("la,lb", [("row", "col"), ("col", "row")])
+def test_split_k_forced(split, la, lb):
+    # K = 1000 gives 16 k-blocks: uneven splits, and for 8 splits two blocks each
+    ttc.ttc_set_knob("split_k", split)
+    try:
+        p = synth.Problem(200, 200, 1000, dtype="bf16", layoutA=la, layoutB=lb, seed=28, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 1.0, 0.5, "relu")
+        check_full(p, d, 1.0, 0.5, "relu")
+    finally:
+        ttc.ttc_set_knob("split_k", 0)
+
+
+def test_split_k_more_splits_than_k_blocks():
+    # 2 k-blocks over 8 CTAs: six CTAs hold empty (zero) partial sums
+    ttc.ttc_set_knob("split_k", 8)
+    try:
+        p = synth.Problem(130, 90, 100, dtype="f16", seed=29, distC="uniform")
+        d = run(p, 1.0, 1.0)
+        check_full(p, d, 1.0, 1.0)
+    finally:
+        ttc.ttc_set_knob("split_k", 0)
+
+
+def test_split_k_generic_producer_and_swap():
+    ttc.ttc_set_knob("split_k", 4)
+    ttc.ttc_set_knob("swap_ab", 1)
+    try:
+        p = synth.Problem(40, 300, 777, dtype="bf16", seed=30, distC="uniform", lda=779, ldb=781)
+        d = run(p, 1.0, 1.0, ldd=303)
+        check_full(p, d, 1.0, 1.0)
+    finally:
+        ttc.ttc_set_knob("split_k", 0)
         ttc.ttc_set_knob("swap_ab", 0)

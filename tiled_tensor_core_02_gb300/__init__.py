@@ -27,7 +27,7 @@ DTYPE = {"f16": 0, "bf16": 1, "i8": 2}
 STATUS = {0: "TTC_OK", 1: "TTC_ERR_INVALID_ARG", 2: "TTC_ERR_UNSUPPORTED", 3: "TTC_ERR_CUDA",
           4: "TTC_ERR_TIMEOUT"}
 KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_generic_store": 3,
-        "tile_n": 4, "pair": 5, "swap_ab": 6}
+        "tile_n": 4, "pair": 5, "swap_ab": 6, "split_k": 7}
 
 # Every symbol the C header declares (checked by the test suite).
 EXPORTS = ("ttc_gemm", "ttc_get_device_error", "ttc_status_string", "ttc_set_knob",

@@ -30,6 +30,7 @@ std::atomic<int> g_force_generic_store{0};
 std::atomic<int> g_force_tile_n{0};
 std::atomic<int> g_pair_mode{0};
 std::atomic<int> g_swap_mode{0};
+std::atomic<int> g_split_k{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -169,6 +170,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
       g_swap_mode.store((int)value);
       return TTC_OK;
+    case TTC_KNOB_SPLIT_K:
+      if (value < 0 || value > 8) return TTC_ERR_INVALID_ARG;
+      g_split_k.store((int)value);
+      return TTC_OK;
   }
   return TTC_ERR_INVALID_ARG;
 }
@@ -283,6 +288,25 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     }
     if (best_score < 0) return TTC_ERR_UNSUPPORTED;
   }
+  // HBM-bound skinny problems (one side at most 64): stream the long operand
+  // through the 128-row side of the MMA, so every pipeline stage carries a
+  // full 16 KB of it, and split K across the CTAs of a cluster until the
+  // tiles fill the SMs.  Partial tiles are summed through distributed shared
+  // memory, with no workspace.
+  int ksplit = 1;
+  const int forced_split = g_split_k.load();
+  const int64_t nkb_total = (K + kBK - 1) / kBK;
+  if (dtype != TTC_I8 && forced_bn == 0 && swap_mode == 0 && (M < N ? M : N) <= 64 && nkb_total >= 8) {
+    swap = N > M;
+    const int64_t mk = swap ? N : M, nk = swap ? M : N;
+    const bool bk_mn = swap ? layoutA == TTC_COL_MAJOR : layoutB == TTC_ROW_MAJOR;
+    bn = (bk_mn || nk > 32) ? 64 : 32;
+    const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + bn - 1) / bn);
+    while (ksplit < 8 && tiles * ksplit * 2 <= dev->sm_count && nkb_total / (ksplit * 2) >= 4) ksplit *= 2;
+  }
+  if (forced_split > 0) ksplit = dtype == TTC_I8 ? 1 : forced_split;
+  if (ksplit > 1 && bn > 128) bn = 128;  // split-K exchange buffers exist for tiles up to 128 wide
+
   if (swap) {
     // D^T (N x M, stored as D with the roles of ldd's axes exchanged) = B^T A^T:
     // B^T is B read with the other layout, and likewise A^T
@@ -366,6 +390,8 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   prm.num_k_blocks = (int)((K + kBK - 1) / kBK);
   prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
   prm.group_m = prm.num_m_blocks < 16 ? prm.num_m_blocks : 16;
+  prm.ksplit = ksplit;
+  prm.kb_split = (int)((prm.num_k_blocks + ksplit - 1) / ksplit);
   prm.a_mn = a_mn;
   prm.b_mn = b_mn;
   prm.alpha = alpha;
@@ -386,7 +412,7 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   // CTA-pair kernel: fp16/bf16 operands staged by TMA, a 256 x 256 tile per
   // pair of SMs; chosen for problems at least one pair tile in each direction
   const int pair_mode = g_pair_mode.load();
-  const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap;
+  const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap && ksplit == 1;
   if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= kPairBN))) {
     const bool bf16 = dtype == TTC_BF16;
     int& clusters = dev->pair_clusters[bf16 ? 1 : 0];
@@ -413,8 +439,10 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     }
   }
 
-  const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
-  if (launch(mode, bn, prm, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+  const int max_clusters = dev->sm_count / ksplit > 0 ? dev->sm_count / ksplit : 1;
+  const int clusters = prm.num_tiles < max_clusters ? prm.num_tiles : max_clusters;
+  if (launch(mode, bn, prm, clusters * ksplit, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return TTC_ERR_CUDA;
   g_launches.fetch_add(1);
   return TTC_OK;
 }

@@ -85,6 +85,8 @@ struct GemmParams {
                      // stale data, which only reaches accumulator rows that are never stored
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+  int ksplit;     // CTAs per cluster that split one tile's k-blocks (1 = no split)
+  int kb_split;   // k-blocks per split (the last split may get fewer, or none)
   int a_mn, b_mn;  // operand stored MN-major (A column-major / B row-major)
   float alpha, beta;
   const void* C;
@@ -109,7 +111,12 @@ struct TileCfg {
   static constexpr int kEpiBytes = kEpiWarps * 2 * T::kEpiBufBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per block
-  static constexpr int kStageBudget = kSmemLimit - 1024 - kBarBytes - kEpiBytes;
+  // split-K partial-sum exchange (fp16/bf16 modes, tiles up to 128 wide): per
+  // epilogue warp two slots of 32 rows x 32 fp32 columns
+  static constexpr bool kSplitK = !T::kI8 && BN <= 128;
+  static constexpr int kRedSlotBytes = 32 * kEpiCols * 4;
+  static constexpr int kRedBytes = kSplitK ? kEpiWarps * 2 * kRedSlotBytes : 0;
+  static constexpr int kStageBudget = kSmemLimit - 1024 - kBarBytes - kEpiBytes - kRedBytes;
   // int8 staging ring (staged mode): the raw int8 A and B tiles of one k-block
   static constexpr int kStage8Bytes = T::kStaged ? (kBM + BN) * kBK : 0;
   static constexpr int kStagesRaw = kStageBudget / (kStageBytes + kStage8Bytes);
@@ -117,7 +124,7 @@ struct TileCfg {
   static constexpr int kStages8 = T::kStaged ? kStages : 0;
   static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
   static constexpr int kSmemBytes =
-      1024 /*align slack*/ + kStages * kStageBytes + kStages8 * kStage8Bytes + kEpiBytes + kBarBytes;
+      1024 /*align slack*/ + kStages * kStageBytes + kStages8 * kStage8Bytes + kEpiBytes + kRedBytes + kBarBytes;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole epilogue chunks");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
@@ -416,7 +423,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   uint8_t* s8 = sB + S * Cfg::kBBytes;  // int8 staging ring (staged mode only)
   constexpr int S8 = Cfg::kStages8;
   uint8_t* sEpi = s8 + S8 * Cfg::kStage8Bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + Cfg::kEpiBytes);
+  uint8_t* sRed = sEpi + Cfg::kEpiBytes;  // split-K partial sums (kSplitK only)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sRed + Cfg::kRedBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* tmem_full = bars + 2 * S;
@@ -425,15 +433,24 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   uint64_t* drain_bar = bars + 2 * S + 5;
   uint64_t* full8 = bars + 2 * S + 6;
   uint64_t* empty8 = full8 + S8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty8 + S8);
-  static_assert((2 * S + 6 + 2 * S8) * 8 + 4 <= Cfg::kBarBytes, "barrier area");
+  uint64_t* red_full = empty8 + S8;       // [warp][slot], in the leader: peers' partials written
+  uint64_t* red_empty = red_full + 2 * kEpiWarps;  // [warp][slot], in each peer: leader done reading
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red_empty + 2 * kEpiWarps);
+  static_assert((2 * S + 6 + 2 * S8 + 4 * kEpiWarps) * 8 + 4 <= Cfg::kBarBytes, "barrier area");
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const WaitCtx wc{p.err, p.timeout_ns};
+  // split-K: the CTAs of a cluster share each tile, CTA `rank` taking k-blocks [k_lo, k_hi)
+  const uint32_t rank = p.ksplit > 1 ? cluster_ctarank() : 0u;
+  const int cluster_id = blockIdx.x / p.ksplit;
+  const int num_clusters = gridDim.x / p.ksplit;
+  const int k_lo = min(p.num_k_blocks, (int)rank * p.kb_split);
+  const int k_hi = min(p.num_k_blocks, k_lo + p.kb_split);
+  const int nkb = k_hi - k_lo;
   // units per tile: int8 drains its accumulator every kI8ChunkKBlocks k-blocks
-  const int chunk_kb = kI8 ? kI8ChunkKBlocks : (p.num_k_blocks > 0 ? p.num_k_blocks : 1);
-  const int units_per_tile = p.num_k_blocks > 0 ? (p.num_k_blocks + chunk_kb - 1) / chunk_kb : 1;
+  const int chunk_kb = kI8 ? kI8ChunkKBlocks : (nkb > 0 ? nkb : 1);
+  const int units_per_tile = nkb > 0 ? (nkb + chunk_kb - 1) / chunk_kb : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -444,6 +461,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     for (int s = 0; s < S8; ++s) {
       mbar_init(&full8[s], 1);
       mbar_init(&empty8[s], 4);
+    }
+    for (int i = 0; i < 2 * kEpiWarps; ++i) {
+      mbar_init(&red_full[i], 32 * (p.ksplit > 1 ? p.ksplit - 1 : 1));
+      mbar_init(&red_empty[i], 32);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tmem_full[a], 1);
@@ -463,7 +484,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     tmem_relinquish();
   }
   tc_fence_before();
-  __syncthreads();
+  if (p.ksplit > 1)
+    cluster_sync();  // every CTA's barriers initialised before any remote arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -476,11 +500,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+        for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
           int mb, nb;
           tile_coords(t, p, mb, nb);
           const int m0 = mb * kBM, n0 = nb * BN;
-          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+          for (int kb = k_lo; kb < k_hi; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
@@ -525,11 +549,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           uint32_t ph8 = 0;
           uint32_t issued_mask = 0, issued_parity = 0;
           bool ok = true;
-          for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+          for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
             int mb, nb;
             tile_coords(t, p, mb, nb);
             const int m0 = mb * kBM, n0 = nb * BN;
-            for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+            for (int kb = k_lo; kb < k_hi; ++kb) {
               if (!mbar_wait(&empty8[st8], ph8 ^ 1u, wc)) {
                 ok = false;
                 break;
@@ -565,8 +589,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         int st8 = 0, stage = 0;
         uint32_t ph8 = 0, phase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
-          for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
+          for (int kb = k_lo; kb < k_hi; ++kb) {
             if (!mbar_wait(&full8[st8], ph8, wc) || !mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
@@ -604,12 +628,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       const int tid = threadIdx.x;  // 0..127
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
         bool ok = true;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb = k_lo; kb < k_hi; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
             break;
@@ -650,7 +674,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       int unit = 0;
       const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
       const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
-      for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+      for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
         for (int u = 0; ok && u < units_per_tile; ++u, ++unit) {
           const int acc = unit & 1;
           const uint32_t acc_phase = (unit >> 1) & 1;
@@ -660,8 +684,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + acc * BN;
-          const int kb0 = u * chunk_kb;
-          const int kb1 = min(p.num_k_blocks, kb0 + chunk_kb);
+          const int kb0 = k_lo + u * chunk_kb;
+          const int kb1 = min(k_hi, kb0 + chunk_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase, wc)) {
               ok = false;
@@ -704,10 +728,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     uint8_t* stage_buf = sEpi + ew * 2 * Tr::kEpiBufBytes;
     int buf = 0;
     int unit = 0;
-    const bool has_k = p.num_k_blocks > 0;
+    const bool has_k = nkb > 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.num_tiles; t += gridDim.x) {
+    int red_it = 0;  // split-K: partial-sum chunks exchanged so far
+    for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
       int mb, nb;
       tile_coords(t, p, mb, nb);
       const int m0 = mb * kBM, n0 = nb * BN;
@@ -801,6 +826,46 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             __syncwarp();
             if (lane == 0) mbar_arrive(&tmem_empty[acc]);
           }
+          if constexpr (Cfg::kSplitK) {
+            if (p.ksplit > 1) {
+              // split-K: peers hand their fp32 partial chunk to the leader (rank 0)
+              // through their own shared memory; the leader sums in rank order
+              const int slot = red_it & 1;
+              const uint32_t ph = (red_it >> 1) & 1;
+              ++red_it;
+              uint64_t* rf = &red_full[ew * 2 + slot];
+              uint64_t* re = &red_empty[ew * 2 + slot];
+              uint8_t* row = sRed + (ew * 2 + slot) * Cfg::kRedSlotBytes + lane * 128;
+              if (rank != 0) {
+                if (!mbar_wait_cluster(re, ph ^ 1u, wc)) {
+                  ok = false;
+                  break;
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)  // 16-byte chunk ch of the row, rotated by lane
+                  *reinterpret_cast<uint4*>(row + ((ch ^ (lane & 7)) << 4)) =
+                      make_uint4(r[4 * ch], r[4 * ch + 1], r[4 * ch + 2], r[4 * ch + 3]);
+                mbar_arrive_cluster(mapa_shared(smem_u32(rf), 0));
+                continue;
+              }
+              if (!mbar_wait_cluster(rf, ph, wc)) {
+                ok = false;
+                break;
+              }
+              for (int pr = 1; pr < p.ksplit; ++pr) {
+                const uint32_t src = mapa_shared(smem_u32(row), (uint32_t)pr);
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                  const uint4 w = ld_shared_cluster_v4(src + ((ch ^ (lane & 7)) << 4));
+                  r[4 * ch] = __float_as_uint(__uint_as_float(r[4 * ch]) + __uint_as_float(w.x));
+                  r[4 * ch + 1] = __float_as_uint(__uint_as_float(r[4 * ch + 1]) + __uint_as_float(w.y));
+                  r[4 * ch + 2] = __float_as_uint(__uint_as_float(r[4 * ch + 2]) + __uint_as_float(w.z));
+                  r[4 * ch + 3] = __float_as_uint(__uint_as_float(r[4 * ch + 3]) + __uint_as_float(w.w));
+                }
+              }
+              for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster(mapa_shared(smem_u32(re), (uint32_t)pr));
+            }
+          }
           epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed);
         }
 
@@ -808,11 +873,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
                                        lane);
       }
       if constexpr (!kI8) ++unit;
+      if (!ok) break;
     }
     if (p.d_tma && lane == 0) bulk_wait_all();
   }
 
   __syncthreads();
+  if (p.ksplit > 1) cluster_sync();  // no CTA leaves while a peer may still read its partials
   if (warp == Tr::kMmaWarp) {
     __syncwarp();
     tc_fence_after();

@@ -37,7 +37,22 @@ int gemm_smem_bytes() {
       if (e != cudaSuccess) return e;                                                                \
       attr_done[dev].store(true);                                                                    \
     }                                                                                                \
-    gemm_kernel<BN, MODE><<<grid, ModeTraits<MODE>::kThreads, smem, stream>>>(p);                    \
+    cudaLaunchConfig_t cfg = {};                                                                     \
+    cfg.gridDim = dim3(grid, 1, 1);                                                                  \
+    cfg.blockDim = dim3(ModeTraits<MODE>::kThreads, 1, 1);                                           \
+    cfg.dynamicSmemBytes = smem;                                                                     \
+    cfg.stream = stream;                                                                             \
+    cudaLaunchAttribute attr[1];                                                                     \
+    if (p.ksplit > 1) {                                                                              \
+      attr[0].id = cudaLaunchAttributeClusterDimension;                                              \
+      attr[0].val.clusterDim.x = p.ksplit;                                                           \
+      attr[0].val.clusterDim.y = 1;                                                                  \
+      attr[0].val.clusterDim.z = 1;                                                                  \
+      cfg.attrs = attr;                                                                              \
+      cfg.numAttrs = 1;                                                                              \
+    }                                                                                                \
+    e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE>, p);                                          \
+    if (e != cudaSuccess) return e;                                                                  \
     return cudaGetLastError();                                                                       \
   }
 
