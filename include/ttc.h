@@ -23,7 +23,7 @@
  *
  * Ownership.  Every pointer is caller-owned device memory.  The library keeps
  * no reference to any of it after the call returns and allocates no device
- * memory on this path.
+ * memory; ttc_gemm_ws uses only the workspace its caller passes.
  *
  * Asynchrony.  ttc_gemm only enqueues work on `stream` (a cudaStream_t; NULL
  * is the legacy default stream) and returns.  Calls on different host threads
@@ -48,6 +48,7 @@
 #ifndef TTC_H_
 #define TTC_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -81,6 +82,39 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K,
                     void* D, int64_t ldd,
                     float alpha, float beta, const float* bias,
                     ttc_act act, ttc_dtype dtype, void* stream);
+
+/*
+ * As ttc_gemm, with caller-provided device workspace.  An operand that TMA
+ * cannot read (a base not 16-byte aligned, or a pitch in bytes that is not a
+ * multiple of 16: the tight leading dimensions of odd-sized matrices) is first
+ * copied into the workspace with a padded pitch, on `stream`, so the GEMM runs
+ * on the TMA-staged path.  The workspace must be 256-byte aligned, at least
+ * ttc_gemm_workspace_size() bytes, and not touched by anything else until the
+ * work enqueued on `stream` has finished; its contents are scratch.  With a
+ * NULL, misaligned or too small workspace the call behaves exactly like
+ * ttc_gemm (operands TMA cannot read are then loaded with plain loads inside
+ * the GEMM kernel, which is correct but slower).
+ * The repacking follows the pitch rule of the PitchLinearStripminedThreadMap
+ * walkthrough (lpnh.cn/news/2469163), sections 4.4 and 6.3: 16-byte vector
+ * access needs a 16-byte-aligned start, so the pitch is padded.
+ */
+ttc_status ttc_gemm_ws(int64_t M, int64_t N, int64_t K,
+                       const void* A, int64_t lda, ttc_layout layoutA,
+                       const void* B, int64_t ldb, ttc_layout layoutB,
+                       const void* C, int64_t ldc,
+                       void* D, int64_t ldd,
+                       float alpha, float beta, const float* bias,
+                       ttc_act act, ttc_dtype dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes ttc_gemm_ws uses for these operands: 0 when TMA can read
+ * both (or for invalid or empty arguments).  Pure host computation.
+ */
+size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
+                               const void* A, int64_t lda, ttc_layout layoutA,
+                               const void* B, int64_t ldb, ttc_layout layoutB,
+                               ttc_dtype dtype);
 
 /*
  * Synchronizes `stream`, then returns and clears the device error word that

@@ -19,7 +19,7 @@ def to_dev(buf):
 
 
 def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_dev=None,
-        expect=0, stream=None):
+        expect=0, stream=None, workspace=None):
     """Runs ttc_gemm on problem p; returns the M x N output (storage type) as numpy."""
     out_np = np.int32 if p.dtype == "i8" else np.int16
     ldd = p.N if ldd is None else ldd
@@ -31,10 +31,19 @@ def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_d
         D = torch.full((max(p.M * ldd, 1),), -1, dtype=torch.int32 if out_np == np.int32 else torch.int16,
                        device="cuda")
     s = torch.cuda.current_stream().cuda_stream if stream is None else stream
-    st = ttc.ttc_gemm(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA], B.data_ptr(), p.ldb,
-                      LAY[p.layoutB], C.data_ptr() if (C is not None and beta != 0.0) else None,
-                      p.ldc, D.data_ptr(), ldd, alpha, beta,
-                      bias.data_ptr() if bias is not None else None, ttc.ACT[act], ttc.DTYPE[p.dtype], s)
+    args = (p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA], B.data_ptr(), p.ldb,
+            LAY[p.layoutB], C.data_ptr() if (C is not None and beta != 0.0) else None,
+            p.ldc, D.data_ptr(), ldd, alpha, beta,
+            bias.data_ptr() if bias is not None else None, ttc.ACT[act], ttc.DTYPE[p.dtype])
+    if workspace is None:
+        st = ttc.ttc_gemm(*args, s)
+    else:
+        # workspace: bytes to allocate (-1: exactly what the library asks for)
+        need = ttc.ttc_gemm_workspace_size(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
+                                           B.data_ptr(), p.ldb, LAY[p.layoutB], ttc.DTYPE[p.dtype])
+        nbytes = need if workspace < 0 else workspace
+        ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
+        st = ttc.ttc_gemm_ws(*args, ws.data_ptr() if nbytes else None, nbytes, s)
     assert st == expect, ttc.STATUS.get(st, st)
     if st != 0:
         return None

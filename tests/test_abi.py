@@ -90,3 +90,21 @@ def test_empty_problems_are_noops(lib):
     assert call(M=0) == 0
     assert call(N=0) == 0
     assert call(M=0, A=None, B=None, D=None) == 0
+
+
+def test_workspace_size_query(lib):
+    # aligned operands need nothing; an odd pitch needs one padded copy
+    assert ttc.ttc_gemm_workspace_size(64, 64, 64, P, 64, R, P, 64, C, BF16) == 0
+    # A row-major 4099 x 1023 and B column-major 1023 x 3001, tight pitches of
+    # 2046 bytes: copies of 4099 and 3001 rows of 1024 elements
+    n = ttc.ttc_gemm_workspace_size(4099, 3001, 1023, P, 1023, R, P, 1023, C, BF16)
+    r256 = lambda b: (b + 255) // 256 * 256
+    assert n == r256(4099 * 1024 * 2) + r256(3001 * 1024 * 2)
+    # int8: pitch must be a 16-byte multiple
+    assert ttc.ttc_gemm_workspace_size(64, 64, 64, P, 64, R, P, 64, C, I8) == 0
+    assert ttc.ttc_gemm_workspace_size(64, 64, 72, P, 72, R, P, 72, C, I8) == 2 * r256(64 * 80)
+    # misaligned base
+    assert ttc.ttc_gemm_workspace_size(64, 64, 64, P + 2, 64, R, P, 64, C, BF16) > 0
+    # empty or invalid problems
+    assert ttc.ttc_gemm_workspace_size(0, 64, 64, P, 63, R, P, 64, C, BF16) == 0
+    assert ttc.ttc_gemm_workspace_size(64, 64, 64, P, 63, 9, P, 64, C, BF16) == 0

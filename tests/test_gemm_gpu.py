@@ -390,3 +390,26 @@ def test_split_k_generic_producer_and_swap():
     finally:
         ttc.ttc_set_knob("split_k", 0)
         ttc.ttc_set_knob("swap_ab", 0)
+
+
+# ------------------------------------------------------------------ ttc_gemm_ws: repacked operands
+
+@pytest.mark.parametrize("shape", synth.RAGGED_SHAPES, ids=lambda s: "x".join(map(str, s)))
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_ragged_sweep_with_workspace(shape, la, lb):
+    p, a, b, act = synth.make(synth.ragged_workload(*shape, la, lb))
+    d = run(p, a, b, act, workspace=-1)
+    check_full(p, d, a, b, act)
+
+
+def test_workspace_int8_odd_pitch():
+    p = synth.Problem(300, 200, 72, dtype="i8", layoutA="row", layoutB="col", seed=31, distA="int8",
+                      distB="int8", lda=73, ldb=75)
+    d = run(p, 1.0, 0.0, workspace=-1)
+    check_full(p, d, 1.0, 0.0)
+
+
+def test_workspace_too_small_falls_back():
+    p = synth.Problem(257, 131, 97, dtype="bf16", seed=32, distC="uniform", lda=98, ldb=99)
+    d = run(p, 1.0, 1.0, workspace=64)
+    check_full(p, d, 1.0, 1.0)

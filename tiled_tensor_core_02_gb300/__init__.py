@@ -30,8 +30,8 @@ KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_gene
         "tile_n": 4, "pair": 5, "swap_ab": 6, "split_k": 7}
 
 # Every symbol the C header declares (checked by the test suite).
-EXPORTS = ("ttc_gemm", "ttc_get_device_error", "ttc_status_string", "ttc_set_knob",
-           "ttc_launch_count")
+EXPORTS = ("ttc_gemm", "ttc_gemm_ws", "ttc_gemm_workspace_size", "ttc_get_device_error",
+           "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
 
 _lib = None
 
@@ -57,6 +57,11 @@ def load():
     i64, vp, f, i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
     L.ttc_gemm.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp]
     L.ttc_gemm.restype = i
+    L.ttc_gemm_ws.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp,
+                              ctypes.c_size_t, vp]
+    L.ttc_gemm_ws.restype = i
+    L.ttc_gemm_workspace_size.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, i]
+    L.ttc_gemm_workspace_size.restype = ctypes.c_size_t
     L.ttc_get_device_error.argtypes = [vp]
     L.ttc_get_device_error.restype = i
     L.ttc_status_string.argtypes = [i]
@@ -76,6 +81,16 @@ def ttc_gemm(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, b
     """Pointers are ints (device addresses) or None; stream is a cudaStream_t as int or None."""
     return load().ttc_gemm(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta,
                            bias, act, dtype, stream)
+
+
+def ttc_gemm_ws(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act,
+                dtype, workspace, workspace_bytes, stream) -> int:
+    return load().ttc_gemm_ws(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta,
+                              bias, act, dtype, workspace, workspace_bytes, stream)
+
+
+def ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype) -> int:
+    return load().ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype)
 
 
 def ttc_get_device_error(stream=None) -> int:

@@ -14,6 +14,7 @@
 
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
+#include "repack.cuh"
 #include "ttc.h"
 #include "ttc_layout.hpp"
 
@@ -124,6 +125,60 @@ bool ranges_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_byt
   return a0 < b0 + (uintptr_t)b_bytes && b0 < a0 + (uintptr_t)a_bytes;
 }
 
+
+// A size-1 mode leaves its stride free: a 1 x K column-major A with lda = 1
+// is the same memory as a row-major one, and so on.  Rewrites such operands
+// to the layout whose contiguous mode is the long one.
+void canonicalise(int64_t M, int64_t N, int64_t K, ttc_layout& layoutA, int64_t& lda, ttc_layout& layoutB,
+                  int64_t& ldb) {
+  if (M == 1 && layoutA == TTC_COL_MAJOR && lda == 1) {
+    layoutA = TTC_ROW_MAJOR;
+    lda = round_up(K > 0 ? K : 1, 16);
+  } else if (K == 1 && layoutA == TTC_ROW_MAJOR && lda == 1) {
+    layoutA = TTC_COL_MAJOR;
+    lda = round_up(M, 16);
+  }
+  if (N == 1 && layoutB == TTC_ROW_MAJOR && ldb == 1) {
+    layoutB = TTC_COL_MAJOR;
+    ldb = round_up(K > 0 ? K : 1, 16);
+  } else if (K == 1 && layoutB == TTC_COL_MAJOR && ldb == 1) {
+    layoutB = TTC_ROW_MAJOR;
+    ldb = round_up(N, 16);
+  }
+}
+
+// Which operands ttc_gemm_ws copies into its workspace (those TMA cannot
+// describe), with their memory-order shape and the padded pitch of the copy.
+struct RepackPlan {
+  bool a = false, b = false;
+  int64_t a_rows = 0, a_cols = 0, a_ld = 0, b_rows = 0, b_cols = 0, b_ld = 0;
+  size_t a_off = 0, b_off = 0, bytes = 0;
+};
+
+RepackPlan plan_repack(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,
+                       const void* B, int64_t ldb, ttc_layout layoutB, int esize) {
+  RepackPlan r;
+  if (K == 0) return r;
+  const int64_t per16 = 16 / esize;
+  if (!tma_ok(A, lda, esize)) {
+    r.a = true;
+    r.a_rows = layoutA == TTC_ROW_MAJOR ? M : K;
+    r.a_cols = layoutA == TTC_ROW_MAJOR ? K : M;
+    r.a_ld = round_up(r.a_cols, per16);
+    r.a_off = 0;
+    r.bytes = (size_t)round_up(r.a_rows * r.a_ld * esize, 256);
+  }
+  if (!tma_ok(B, ldb, esize)) {
+    r.b = true;
+    r.b_rows = layoutB == TTC_ROW_MAJOR ? K : N;
+    r.b_cols = layoutB == TTC_ROW_MAJOR ? N : K;
+    r.b_ld = round_up(r.b_cols, per16);
+    r.b_off = r.bytes;
+    r.bytes += (size_t)round_up(r.b_rows * r.b_ld * esize, 256);
+  }
+  return r;
+}
+
 }  // namespace
 }  // namespace ttc
 
@@ -195,9 +250,10 @@ ttc_status ttc_get_device_error(void* stream) {
   return TTC_OK;
 }
 
-ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA, const void* B,
-                    int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D, int64_t ldd, float alpha,
-                    float beta, const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
+static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,
+                            const void* B, int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D,
+                            int64_t ldd, float alpha, float beta, const float* bias, ttc_act act, ttc_dtype dtype,
+                            void* workspace, size_t workspace_bytes, void* stream) {
   // ------------------------------------------------------------ validation
   if (M < 0 || N < 0 || K < 0) return TTC_ERR_INVALID_ARG;
   if ((layoutA != TTC_ROW_MAJOR && layoutA != TTC_COL_MAJOR) ||
@@ -236,23 +292,33 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
   if (st != TTC_OK) return st;
 
   // ------------------------------------------------------------ canonicalisation
-  // A size-1 mode leaves its stride free: a 1 x K column-major A with lda = 1
-  // is the same memory as a row-major one, and so on.
-  if (M == 1 && layoutA == TTC_COL_MAJOR && lda == 1) {
-    layoutA = TTC_ROW_MAJOR;
-    lda = round_up(K > 0 ? K : 1, 16);
-  } else if (K == 1 && layoutA == TTC_ROW_MAJOR && lda == 1) {
-    layoutA = TTC_COL_MAJOR;
-    lda = round_up(M, 16);
-  }
-  if (N == 1 && layoutB == TTC_ROW_MAJOR && ldb == 1) {
-    layoutB = TTC_COL_MAJOR;
-    ldb = round_up(K > 0 ? K : 1, 16);
-  } else if (K == 1 && layoutB == TTC_COL_MAJOR && ldb == 1) {
-    layoutB = TTC_ROW_MAJOR;
-    ldb = round_up(N, 16);
-  }
+  canonicalise(M, N, K, layoutA, lda, layoutB, ldb);
   if (M == 1 && !tma_ok(D, ldd, out_esize) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 16);
+
+  // ------------------------------------------------------------ workspace: repack what TMA cannot read
+  if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 && !g_force_generic_load.load()) {
+    const RepackPlan rp = plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, in_esize);
+    if (rp.bytes > 0 && rp.bytes <= workspace_bytes) {
+      uint8_t* ws = static_cast<uint8_t*>(workspace);
+      cudaStream_t s = static_cast<cudaStream_t>(stream);
+      if (rp.a) {
+        if (launch_repack(A, lda, rp.a_rows, rp.a_cols, ws + rp.a_off, rp.a_ld, in_esize, dev->sm_count, s) !=
+            cudaSuccess)
+          return TTC_ERR_CUDA;
+        g_launches.fetch_add(1);
+        A = ws + rp.a_off;
+        lda = rp.a_ld;
+      }
+      if (rp.b) {
+        if (launch_repack(B, ldb, rp.b_rows, rp.b_cols, ws + rp.b_off, rp.b_ld, in_esize, dev->sm_count, s) !=
+            cudaSuccess)
+          return TTC_ERR_CUDA;
+        g_launches.fetch_add(1);
+        B = ws + rp.b_off;
+        ldb = rp.b_ld;
+      }
+    }
+  }
 
   // ------------------------------------------------------------ orientation and tile width
   // The kernel tile is 128 rows by bn columns.  A skinny problem gets few
@@ -445,6 +511,31 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
     return TTC_ERR_CUDA;
   g_launches.fetch_add(1);
   return TTC_OK;
+}
+
+ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA, const void* B,
+                    int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D, int64_t ldd, float alpha,
+                    float beta, const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
+  return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, nullptr,
+                   0, stream);
+}
+
+ttc_status ttc_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA, const void* B,
+                       int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D, int64_t ldd, float alpha,
+                       float beta, const float* bias, ttc_act act, ttc_dtype dtype, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, workspace,
+                   workspace_bytes, stream);
+}
+
+size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,
+                               const void* B, int64_t ldb, ttc_layout layoutB, ttc_dtype dtype) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  if ((layoutA != TTC_ROW_MAJOR && layoutA != TTC_COL_MAJOR) || (layoutB != TTC_ROW_MAJOR && layoutB != TTC_COL_MAJOR))
+    return 0;
+  if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return 0;
+  canonicalise(M, N, K, layoutA, lda, layoutB, ldb);
+  return plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype == TTC_I8 ? 1 : 2).bytes;
 }
 
 }  // extern "C"

@@ -242,7 +242,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed);
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, stage_buf, lane);
         epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane);
       }
     }

@@ -288,9 +288,12 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
 // ------------------------------------------------------------------ epilogue helpers
 // fp16/bf16 epilogue of one 32-column chunk of the calling thread's row:
 // v = alpha * acc (+ beta * C) (+ bias), activation, round to nearest even.
+// `wbuf` is the warp's staging area; with D written by plain stores it is
+// free, and an unaligned C is then read through it, coalesced.
 template <bool kBF16>
 __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32_t (&r)[32], bool row_ok,
-                                               int grow, int gcol0, uint32_t (&packed)[16]) {
+                                               int grow, int gcol0, uint32_t (&packed)[16], uint8_t* wbuf,
+                                               int lane) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
@@ -308,11 +311,29 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
         for (int j = 0; j < 32; ++j) v[j] += b;
       }
     }
-  } else if (p.beta != 0.0f && row_ok) {
+  } else if (p.beta != 0.0f) {
     const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
     const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
                      (gcol0 + 32 <= p.N);
-    if (vec) {
+    if (!vec && !p.d_tma) {
+      // lane l reads column gcol0 + l of the warp's 32 rows (64 contiguous
+      // bytes per instruction) into a 32 x 34-halfword block, then each thread
+      // takes its own row (pitch 17 words: no bank conflicts either way)
+      uint16_t* w = reinterpret_cast<uint16_t*>(wbuf);
+      const int row0 = grow - lane;
+      const int col = gcol0 + lane;
+      const uint16_t* cbase = reinterpret_cast<const uint16_t*>(p.C);
+#pragma unroll 8
+      for (int rr = 0; rr < 32; ++rr) {
+        const int gr = row0 + rr;
+        w[rr * 34 + lane] = (gr < p.M && col < p.N) ? __ldg(cbase + (int64_t)gr * p.ldc + col) : (uint16_t)0;
+      }
+      __syncwarp();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(w[lane * 34 + j]), v[j]);
+      __syncwarp();
+    } else if (!row_ok) {
+    } else if (vec) {
 #pragma unroll
       for (int u4 = 0; u4 < 4; ++u4) {
         const uint4 w = __ldg(reinterpret_cast<const uint4*>(crow) + u4);
@@ -380,7 +401,32 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
       bulk_commit();
     }
     buf ^= 1;
-  } else if (row_ok && p.d_trans) {
+  } else if (!p.d_trans) {
+    // plain stores, coalesced through the warp's staging area (both buffers):
+    // each thread writes its row, then lane l stores column gcol0 + l of the
+    // warp's 32 rows
+    uint32_t* w = reinterpret_cast<uint32_t*>(stage_buf);
+    constexpr int kPitch = kOutBytes == 4 ? 33 : 17;  // words per staged row
+#pragma unroll
+    for (int j = 0; j < kPacked; ++j) w[lane * kPitch + j] = packed[j];
+    __syncwarp();
+    const int row0 = grow - lane;
+    const int col = gcol0 + lane;
+    if (col < p.N) {
+#pragma unroll 8
+      for (int rr = 0; rr < 32; ++rr) {
+        const int gr = row0 + rr;
+        if (gr < p.M) {
+          if constexpr (kOutBytes == 4)
+            reinterpret_cast<int32_t*>(p.D)[(int64_t)gr * p.ldd + col] = (int32_t)w[rr * 33 + lane];
+          else
+            reinterpret_cast<uint16_t*>(p.D)[(int64_t)gr * p.ldd + col] =
+                reinterpret_cast<const uint16_t*>(w)[rr * 34 + lane];
+        }
+      }
+    }
+    __syncwarp();
+  } else if (row_ok) {
     // lanes hold consecutive kernel rows = consecutive elements of a D row
     if constexpr (kOutBytes == 4) {
       int32_t* dst = reinterpret_cast<int32_t*>(p.D) + grow;
@@ -393,18 +439,6 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
       for (int j = 0; j < 32; ++j)
         if (gcol0 + j < p.N)
           dst[(int64_t)(gcol0 + j) * p.ldd] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
-    }
-  } else if (row_ok) {
-    if constexpr (kOutBytes == 4) {
-      int32_t* dst = reinterpret_cast<int32_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (gcol0 + j < p.N) dst[j] = (int32_t)packed[j];
-    } else {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + (int64_t)grow * p.ldd + gcol0;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        if (gcol0 + j < p.N) dst[j] = (uint16_t)((packed[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu);
     }
   }
 }
@@ -866,7 +900,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster(mapa_shared(smem_u32(re), (uint32_t)pr));
             }
           }
-          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed);
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, stage_buf, lane);
         }
 
         epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, Tr::kEpiBufBytes, buf,

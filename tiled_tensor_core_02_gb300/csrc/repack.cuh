@@ -1,0 +1,15 @@
+// Operand repacking into a padded-pitch workspace (see repack.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace ttc {
+
+// Copies `rows` rows of `cols` elements (elem_bytes = 1 or 2), `src_ld`
+// elements apart, to `dst` with pitch `dst_ld` (a multiple of 16 bytes;
+// `dst` 16-byte aligned).
+cudaError_t launch_repack(const void* src, int64_t src_ld, int64_t rows, int64_t cols, void* dst, int64_t dst_ld,
+                          int elem_bytes, int sm_count, cudaStream_t stream);
+
+}  // namespace ttc
