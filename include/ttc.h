@@ -41,6 +41,8 @@
  *   TTC_ERR_CUDA: a CUDA runtime or driver call failed (launch, device query).
  *   TTC_ERR_TIMEOUT: returned by ttc_get_device_error when a kernel's bounded
  *     wait ran out; the kernel then ended early and D is undefined.
+ *   TTC_ERR_SCRATCH_TOO_SMALL: ttc_gemm_static_scratch only: the operands need
+ *     more scratch than its fixed array holds.
  * M == 0 or N == 0 is a no-op returning TTC_OK.  K == 0 gives
  * D = act(beta * C + bias).  beta == 0 never reads C (NaNs in C do not
  * propagate).
@@ -60,7 +62,8 @@ typedef enum {
   TTC_ERR_INVALID_ARG = 1,
   TTC_ERR_UNSUPPORTED = 2,
   TTC_ERR_CUDA = 3,
-  TTC_ERR_TIMEOUT = 4
+  TTC_ERR_TIMEOUT = 4,
+  TTC_ERR_SCRATCH_TOO_SMALL = 5
 } ttc_status;
 
 typedef enum { TTC_ROW_MAJOR = 0, TTC_COL_MAJOR = 1 } ttc_layout;
@@ -115,6 +118,50 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, ttc_layout layoutA,
                                const void* B, int64_t ldb, ttc_layout layoutB,
                                ttc_dtype dtype);
+
+/*
+ * Size of the fixed device scratch array ttc_gemm_static_scratch uses: 16 MiB.
+ */
+#define TTC_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * ttc_gemm_ws for callers that cannot allocate device memory.  The pages this
+ * library follows have no counterpart of this entry point.
+ *
+ * Who needs it: code that may not call cudaMalloc at all, for example a plugin
+ * running inside a host application or framework that has reserved the
+ * device's memory for its own pool, or a latency-critical path where the
+ * implicit device-wide synchronisation of cudaMalloc/cudaFree is not
+ * acceptable.  Such a caller cannot hand ttc_gemm_ws a workspace.
+ *
+ * What it does: exactly ttc_gemm_ws, with the workspace taken from a fixed
+ * array of TTC_STATIC_SCRATCH_BYTES in device memory that the library
+ * declares statically.  That array exists on every GPU that loads the library
+ * and stays allocated until the process exits.  This call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).
+ *
+ * Limit: a problem whose operands need more scratch than
+ * TTC_STATIC_SCRATCH_BYTES (ttc_gemm_workspace_size() tells how much) is
+ * rejected with TTC_ERR_SCRATCH_TOO_SMALL before any work is enqueued; operands
+ * TMA can read need no scratch at all.
+ *
+ * Set-up: the first call on a device looks up the array's device address on
+ * that device (with that device current) and caches it; make that first call
+ * before any stream capture on the device.
+ *
+ * Sharing: every call uses the same array, which keeps whatever the previous
+ * call left there; nothing in it has to start at zero (each call overwrites
+ * all the scratch it reads).  Calls whose work overlaps on the GPU (concurrent
+ * streams, or another host thread) race on the array: order them, for example
+ * by issuing them on one stream.
+ */
+ttc_status ttc_gemm_static_scratch(int64_t M, int64_t N, int64_t K,
+                                   const void* A, int64_t lda, ttc_layout layoutA,
+                                   const void* B, int64_t ldb, ttc_layout layoutB,
+                                   const void* C, int64_t ldc,
+                                   void* D, int64_t ldd,
+                                   float alpha, float beta, const float* bias,
+                                   ttc_act act, ttc_dtype dtype, void* stream);
 
 /*
  * Synchronizes `stream`, then returns and clears the device error word that

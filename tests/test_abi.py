@@ -108,3 +108,11 @@ def test_workspace_size_query(lib):
     # empty or invalid problems
     assert ttc.ttc_gemm_workspace_size(0, 64, 64, P, 63, R, P, 64, C, BF16) == 0
     assert ttc.ttc_gemm_workspace_size(64, 64, 64, P, 63, 9, P, 64, C, BF16) == 0
+
+
+def test_static_scratch_rejects_oversized_problems(lib):
+    # 4099 x 8192 bf16 with an odd pitch needs ~64 MiB of repacked A: beyond the
+    # fixed 16 MiB, refused before any device work
+    st = ttc.ttc_gemm_static_scratch(4099, 64, 8191, P, 8191, R, P, 8191, C, None, 64, P * 2, 64, 1.0, 0.0,
+                                     None, 0, BF16, None)
+    assert st == 5 and ttc.ttc_status_string(st) == "TTC_ERR_SCRATCH_TOO_SMALL"

@@ -25,13 +25,14 @@ ROW_MAJOR, COL_MAJOR = 0, 1
 ACT = {"none": 0, "relu": 1, "gelu_tanh": 2}
 DTYPE = {"f16": 0, "bf16": 1, "i8": 2}
 STATUS = {0: "TTC_OK", 1: "TTC_ERR_INVALID_ARG", 2: "TTC_ERR_UNSUPPORTED", 3: "TTC_ERR_CUDA",
-          4: "TTC_ERR_TIMEOUT"}
+          4: "TTC_ERR_TIMEOUT", 5: "TTC_ERR_SCRATCH_TOO_SMALL"}
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_generic_store": 3,
         "tile_n": 4, "pair": 5, "swap_ab": 6, "split_k": 7}
 
 # Every symbol the C header declares (checked by the test suite).
-EXPORTS = ("ttc_gemm", "ttc_gemm_ws", "ttc_gemm_workspace_size", "ttc_get_device_error",
-           "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
+EXPORTS = ("ttc_gemm", "ttc_gemm_ws", "ttc_gemm_workspace_size", "ttc_gemm_static_scratch",
+           "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
 
 _lib = None
 
@@ -60,6 +61,9 @@ def load():
     L.ttc_gemm_ws.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp,
                               ctypes.c_size_t, vp]
     L.ttc_gemm_ws.restype = i
+    L.ttc_gemm_static_scratch.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f,
+                                          vp, i, i, vp]
+    L.ttc_gemm_static_scratch.restype = i
     L.ttc_gemm_workspace_size.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, i]
     L.ttc_gemm_workspace_size.restype = ctypes.c_size_t
     L.ttc_get_device_error.argtypes = [vp]
@@ -87,6 +91,14 @@ def ttc_gemm_ws(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha
                 dtype, workspace, workspace_bytes, stream) -> int:
     return load().ttc_gemm_ws(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta,
                               bias, act, dtype, workspace, workspace_bytes, stream)
+
+
+def ttc_gemm_static_scratch(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta,
+                            bias, act, dtype, stream) -> int:
+    """ttc_gemm_ws with the library's fixed device scratch array: for callers
+    that cannot allocate device memory (see include/ttc.h)."""
+    return load().ttc_gemm_static_scratch(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd,
+                                          alpha, beta, bias, act, dtype, stream)
 
 
 def ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype) -> int:

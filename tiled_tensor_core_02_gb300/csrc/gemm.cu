@@ -193,6 +193,7 @@ const char* ttc_status_string(ttc_status s) {
     case TTC_ERR_UNSUPPORTED: return "TTC_ERR_UNSUPPORTED";
     case TTC_ERR_CUDA: return "TTC_ERR_CUDA";
     case TTC_ERR_TIMEOUT: return "TTC_ERR_TIMEOUT";
+    case TTC_ERR_SCRATCH_TOO_SMALL: return "TTC_ERR_SCRATCH_TOO_SMALL";
   }
   return "TTC_UNKNOWN_STATUS";
 }
@@ -539,3 +540,44 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, i
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation entry point
+// Scratch for ttc_gemm_static_scratch: a fixed array in device memory that
+// exists on every GPU that loads this library, for as long as the process
+// lives.  Host code never dereferences the symbol itself (on the host it only
+// names the array); the device address comes from cudaGetSymbolAddress, once
+// per device, below.
+static __device__ __align__(256) uint8_t g_static_scratch[TTC_STATIC_SCRATCH_BYTES];
+
+namespace {
+void* g_static_scratch_ptr[kMaxDevices] = {};
+std::mutex g_static_scratch_mu;
+
+// Device address of g_static_scratch on the current device (nullptr on error).
+void* static_scratch_address() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_static_scratch_mu);
+  if (g_static_scratch_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) return nullptr;
+    g_static_scratch_ptr[dev] = ptr;
+  }
+  return g_static_scratch_ptr[dev];
+}
+}  // namespace
+
+extern "C" ttc_status ttc_gemm_static_scratch(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                              ttc_layout layoutA, const void* B, int64_t ldb, ttc_layout layoutB,
+                                              const void* C, int64_t ldc, void* D, int64_t ldd, float alpha,
+                                              float beta, const float* bias, ttc_act act, ttc_dtype dtype,
+                                              void* stream) {
+  // The scratch this call needs is a pure host computation; refuse before any
+  // device work when it exceeds the fixed array.
+  if (ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype) > (size_t)TTC_STATIC_SCRATCH_BYTES)
+    return TTC_ERR_SCRATCH_TOO_SMALL;
+  void* scratch = static_scratch_address();
+  if (scratch == nullptr) return TTC_ERR_CUDA;
+  return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, scratch,
+                   (size_t)TTC_STATIC_SCRATCH_BYTES, stream);
+}
