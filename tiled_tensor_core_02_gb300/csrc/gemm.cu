@@ -321,19 +321,31 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     }
   }
 
-  // ------------------------------------------------------------ orientation and tile width
-  // The kernel tile is 128 rows by bn columns.  A skinny problem gets few
-  // tiles, and a skinny HBM-bound problem needs many CTAs streaming at once,
-  // so pick the orientation (D itself, or D^T = B^T A^T with a transposed
-  // store) and tile width with the most tiles, up to one per SM; ties keep
+  // ------------------------------------------------------------ orientation, tile width, K split
+  // The kernel tile is 128 rows by bn columns.  Score each orientation (D
+  // itself, or D^T = B^T A^T with a transposed store) and tile width by the
+  // CTAs it can keep busy, counting a split of K over a cluster of up to 8
+  // CTAs when the tiles alone cannot fill the SMs, weighted by how fast one
+  // CTA runs at that width: a narrow tile re-reads its A operand from shared
+  // memory for fewer columns, so it reaches a smaller share of the tensor rate
+  // (relative rates 1, 0.7, 0.45, 0.3 for widths 256, 128, 64, 32).  Ties keep
   // the wider tile, then the untransposed orientation.
   const int forced_bn = g_force_tile_n.load();
   const int swap_mode = g_swap_mode.load();
+  const int forced_split = g_split_k.load();
   const int max_bn = dtype == TTC_I8 ? 128 : 256;
+  const int64_t nkb_total = (K + kBK - 1) / kBK;
   bool swap = swap_mode == 1;
   int bn = forced_bn;
+  int ksplit = 1;
+  auto split_for = [&](int64_t tiles, int cand) {
+    int sp = 1;
+    if (dtype == TTC_I8 || cand > 128) return sp;  // split-K exchange buffers exist up to width 128
+    while (sp < 8 && tiles * sp * 2 <= dev->sm_count && nkb_total / (sp * 2) >= 2) sp *= 2;
+    return sp;
+  };
   {
-    int best_score = -1;
+    double best_score = -1.0;
     for (int sw = 0; sw < 2; ++sw) {
       if ((swap_mode == 1 && sw == 0) || (swap_mode == 2 && sw == 1)) continue;
       const int64_t mk = sw ? N : M, nk = sw ? M : N;
@@ -345,11 +357,15 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
         // a tile wider than the padded N only wastes work
         if (forced_bn == 0 && cand > 32 && cand / 2 >= nk) continue;
         const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + cand - 1) / cand);
-        const int score = (int)(tiles < dev->sm_count ? tiles : dev->sm_count);
-        if (score > best_score) {
+        const int sp = forced_bn == 0 ? split_for(tiles, cand) : 1;
+        const double rate = cand == 256 ? 1.0 : cand == 128 ? 0.7 : cand == 64 ? 0.45 : 0.3;
+        const double ctas = (double)(tiles * sp < dev->sm_count ? tiles * sp : dev->sm_count);
+        const double score = ctas * rate;
+        if (score > best_score + 1e-9) {
           best_score = score;
           bn = cand;
           swap = sw == 1;
+          ksplit = sp;
         }
       }
     }
@@ -360,15 +376,13 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // full 16 KB of it, and split K across the CTAs of a cluster until the
   // tiles fill the SMs.  Partial tiles are summed through distributed shared
   // memory, with no workspace.
-  int ksplit = 1;
-  const int forced_split = g_split_k.load();
-  const int64_t nkb_total = (K + kBK - 1) / kBK;
   if (dtype != TTC_I8 && forced_bn == 0 && swap_mode == 0 && (M < N ? M : N) <= 64 && nkb_total >= 8) {
     swap = N > M;
     const int64_t mk = swap ? N : M, nk = swap ? M : N;
     const bool bk_mn = swap ? layoutA == TTC_COL_MAJOR : layoutB == TTC_ROW_MAJOR;
     bn = (bk_mn || nk > 32) ? 64 : 32;
     const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + bn - 1) / bn);
+    ksplit = 1;
     while (ksplit < 8 && tiles * ksplit * 2 <= dev->sm_count && nkb_total / (ksplit * 2) >= 4) ksplit *= 2;
   }
   if (forced_split > 0) ksplit = dtype == TTC_I8 ? 1 : forced_split;
@@ -480,7 +494,9 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // pair of SMs; chosen for problems at least one pair tile in each direction
   const int pair_mode = g_pair_mode.load();
   const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap && ksplit == 1;
-  if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= kPairBN))) {
+  const int64_t pair_tiles = ((M + kPairBM - 1) / kPairBM) * ((N + kPairBN - 1) / kPairBN);
+  if (pair_ok && pair_mode != 2 &&
+      (pair_mode == 1 || (M >= kPairBM && N >= kPairBN && pair_tiles * 4 >= dev->sm_count))) {
     const bool bf16 = dtype == TTC_BF16;
     int& clusters = dev->pair_clusters[bf16 ? 1 : 0];
     if (clusters < 0) {

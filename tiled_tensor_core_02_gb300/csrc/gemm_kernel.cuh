@@ -323,11 +323,15 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
       const int row0 = grow - lane;
       const int col = gcol0 + lane;
       const uint16_t* cbase = reinterpret_cast<const uint16_t*>(p.C);
-#pragma unroll 8
+      // all 32 loads in flight before the first use: one memory latency per chunk
+      uint16_t cv[32];
+#pragma unroll
       for (int rr = 0; rr < 32; ++rr) {
         const int gr = row0 + rr;
-        w[rr * 34 + lane] = (gr < p.M && col < p.N) ? __ldg(cbase + (int64_t)gr * p.ldc + col) : (uint16_t)0;
+        cv[rr] = (gr < p.M && col < p.N) ? __ldg(cbase + (int64_t)gr * p.ldc + col) : (uint16_t)0;
       }
+#pragma unroll
+      for (int rr = 0; rr < 32; ++rr) w[rr * 34 + lane] = cv[rr];
       __syncwarp();
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(w[lane * 34 + j]), v[j]);
