@@ -72,18 +72,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const int num_pairs = gridDim.x >> 1;
   const WaitCtx wc{p.err, p.timeout_ns};
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+  if (warp == 0) {
+    // the lanes of warp 0 initialise the barriers between them
+    for (int s = lane; s < S; s += 32) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], 2 * kEpiWarps);
+    if (lane < 2) {
+      mbar_init(&tmem_full[lane], 1);
+      mbar_init(&tmem_empty[lane], 2 * kEpiWarps);
     }
-    mbar_init(stall_bar, 1);
-    mbar_init(drain_bar, 1);
+    if (lane == 0) {
+      mbar_init(stall_bar, 1);
+      mbar_init(drain_bar, 1);
+    }
     fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
     prefetch_tmap(&p.tmA);
     prefetch_tmap(&p.tmB);
     if (p.d_tma) prefetch_tmap(&p.tmD);

@@ -490,27 +490,32 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   const int chunk_kb = kI8 ? kI8ChunkKBlocks : (nkb > 0 ? nkb : 1);
   const int units_per_tile = nkb > 0 ? (nkb + chunk_kb - 1) / chunk_kb : 1;
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+  if (warp == 0) {
+    // the lanes of warp 0 initialise the barriers between them
+    for (int s = lane; s < S; s += 32) {
       // generic: one arrive per plain-load warp; staged: one per converter warp
       mbar_init(&full[s], Tr::kTmaLoad ? 1 : 4);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < S8; ++s) {
+    for (int s = lane; s < S8; s += 32) {
       mbar_init(&full8[s], 1);
       mbar_init(&empty8[s], 4);
     }
-    for (int i = 0; i < 2 * kEpiWarps; ++i) {
-      mbar_init(&red_full[i], 32 * (p.ksplit > 1 ? p.ksplit - 1 : 1));
-      mbar_init(&red_empty[i], 32);
+    if (lane < 2 * kEpiWarps) {
+      mbar_init(&red_full[lane], 32 * (p.ksplit > 1 ? p.ksplit - 1 : 1));
+      mbar_init(&red_empty[lane], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tmem_full[a], 1);
-      mbar_init(&tmem_empty[a], kEpiWarps);
+    if (lane < 2) {
+      mbar_init(&tmem_full[lane], 1);
+      mbar_init(&tmem_empty[lane], kEpiWarps);
     }
-    mbar_init(stall_bar, 1);
-    mbar_init(drain_bar, 1);
+    if (lane == 0) {
+      mbar_init(stall_bar, 1);
+      mbar_init(drain_bar, 1);
+    }
     fence_barrier_init();
+  }
+  if (threadIdx.x == 0) {
     if constexpr (Tr::kTmaLoad || Tr::kStaged) {
       prefetch_tmap(&p.tmA);
       prefetch_tmap(&p.tmB);
@@ -892,16 +897,24 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               }
               for (int pr = 1; pr < p.ksplit; ++pr) {
                 const uint32_t src = mapa_shared(smem_u32(row), (uint32_t)pr);
+                // all eight remote loads in flight before the first use
+                uint4 w[8];
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) w[ch] = ld_shared_cluster_v4(src + ((ch ^ (lane & 7)) << 4));
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                  const uint4 w = ld_shared_cluster_v4(src + ((ch ^ (lane & 7)) << 4));
-                  r[4 * ch] = __float_as_uint(__uint_as_float(r[4 * ch]) + __uint_as_float(w.x));
-                  r[4 * ch + 1] = __float_as_uint(__uint_as_float(r[4 * ch + 1]) + __uint_as_float(w.y));
-                  r[4 * ch + 2] = __float_as_uint(__uint_as_float(r[4 * ch + 2]) + __uint_as_float(w.z));
-                  r[4 * ch + 3] = __float_as_uint(__uint_as_float(r[4 * ch + 3]) + __uint_as_float(w.w));
+                  r[4 * ch] = __float_as_uint(__uint_as_float(r[4 * ch]) + __uint_as_float(w[ch].x));
+                  r[4 * ch + 1] = __float_as_uint(__uint_as_float(r[4 * ch + 1]) + __uint_as_float(w[ch].y));
+                  r[4 * ch + 2] = __float_as_uint(__uint_as_float(r[4 * ch + 2]) + __uint_as_float(w[ch].z));
+                  r[4 * ch + 3] = __float_as_uint(__uint_as_float(r[4 * ch + 3]) + __uint_as_float(w[ch].w));
                 }
               }
-              for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster(mapa_shared(smem_u32(re), (uint32_t)pr));
+              // the peers' slots may be reused: every lane's loads above have
+              // returned (their values are summed), so one relaxed arrive per
+              // warp and peer suffices; a release here would fence each arrive
+              __syncwarp();
+              if (lane == 0)
+                for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(re), (uint32_t)pr));
             }
           }
           epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, stage_buf, lane);
