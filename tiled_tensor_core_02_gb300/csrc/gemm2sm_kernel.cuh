@@ -221,14 +221,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
       const int acc = it & 1;
-      if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
-      tc_fence_after();
       int mb, nb;
       tile_coords(t, p, mb, nb);
       const int m0 = mb * kPairBM + (int)rank * 128;
       const int n0 = nb * kPairBN;
       const int grow = m0 + q * 32 + lane;
       const bool row_ok = grow < p.M;
+      // the first chunk's C is fetched before waiting for the accumulator
+      CChunk16 cc;
+      c_fetch16(p, c_path(p, n0), grow, n0, lane, cc);
+      if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
+      tc_fence_after();
 #pragma unroll 1
       for (int c = 0; c < kPairBN / kEpiCols; ++c) {
         const int gcol0 = n0 + c * kEpiCols;
@@ -247,7 +250,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, stage_buf, lane);
+        const int cpath = c_path(p, gcol0);
+        uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, PairCfg::kEpiBufBytes, lane);
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane);
+        if (c + 1 < kPairBN / kEpiCols) c_fetch16(p, c_path(p, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
         epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane);
       }
     }

@@ -286,80 +286,117 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
 }
 
 // ------------------------------------------------------------------ epilogue helpers
+// How one 32-column chunk of fp16/bf16 C is read (the same for the whole warp).
+enum CPath : int {
+  kCNone = 0,   // beta == 0: C is not read
+  kCVec = 1,    // each thread loads its own row's 64 bytes as four 16-byte vectors
+  kCCoop = 2,   // C is not 16-byte aligned: lane l loads column gcol0 + l of the warp's
+                // 32 rows (one 64-byte segment per instruction), transposed in shared memory
+  kCTrans = 3,  // D^T orientation: lanes already hold consecutive elements of a C row
+};
+
+__device__ __forceinline__ int c_path(const GemmParams& p, int gcol0) {
+  if (p.beta == 0.0f) return kCNone;
+  if (p.d_trans) return kCTrans;
+  const bool vec =
+      ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && (gcol0 + 32 <= p.N);
+  return vec ? kCVec : kCCoop;
+}
+
+// C values of one chunk, fetched one chunk ahead of their use so that the
+// load latency overlaps the previous chunk's work.
+struct CChunk16 {
+  uint4 v[4];       // kCVec: this thread's row, 32 values
+  uint16_t e[32];   // kCCoop: column (gcol0 + lane) of the warp's 32 rows (kept unpacked: the
+                    // loads are not waited on until the values are staged, a chunk later)
+};
+
+__device__ __forceinline__ void c_fetch16(const GemmParams& p, int path, int grow, int gcol0, int lane,
+                                          CChunk16& cc) {
+  if (path == kCVec) {
+    if (grow < p.M) {
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.C) +
+                                                        (int64_t)grow * p.ldc + gcol0);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cc.v[u] = __ldg(src + u);
+    } else {
+#pragma unroll
+      for (int u = 0; u < 4; ++u) cc.v[u] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  } else if (path == kCCoop) {
+    const int row0 = grow - lane;
+    const int col = gcol0 + lane;
+    const uint16_t* cbase = reinterpret_cast<const uint16_t*>(p.C);
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+      const int g = row0 + rr;
+      cc.e[rr] = (g < p.M && col < p.N) ? __ldg(cbase + (int64_t)g * p.ldc + col) : (uint16_t)0;
+    }
+  }
+}
+
 // fp16/bf16 epilogue of one 32-column chunk of the calling thread's row:
 // v = alpha * acc (+ beta * C) (+ bias), activation, round to nearest even.
-// `wbuf` is the warp's staging area; with D written by plain stores it is
-// free, and an unaligned C is then read through it, coalesced.
+// `cc` holds this chunk's C as fetched by c_fetch16 for `cpath`; kCCoop
+// transposes it through `cstage`, 2 KB of shared memory the warp owns for the
+// call (32 x 32 16-bit values, 16-byte words XOR-swizzled by row so that both
+// the column-wise writes and the row-wise reads are free of bank conflicts).
 template <bool kBF16>
 __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32_t (&r)[32], bool row_ok,
-                                               int grow, int gcol0, uint32_t (&packed)[16], uint8_t* wbuf,
-                                               int lane) {
+                                               int grow, int gcol0, uint32_t (&packed)[16], int cpath,
+                                               const CChunk16& cc, uint8_t* cstage, int lane) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
-  if (p.d_trans) {
+  if (cpath == kCTrans) {
     if (row_ok) {
-      if (p.beta != 0.0f) {
-        const uint16_t* ccol = reinterpret_cast<const uint16_t*>(p.C) + grow;
+      const uint16_t* ccol = reinterpret_cast<const uint16_t*>(p.C) + grow;
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(ccol + (int64_t)(gcol0 + j) * p.ldc)), v[j]);
-      }
-      if (p.bias != nullptr) {
-        const float b = __ldg(p.bias + grow);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] += b;
-      }
+      for (int j = 0; j < 32; ++j)
+        if (gcol0 + j < p.N)
+          v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(ccol + (int64_t)(gcol0 + j) * p.ldc)), v[j]);
     }
-  } else if (p.beta != 0.0f) {
-    const uint16_t* crow = reinterpret_cast<const uint16_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
-    const bool vec = ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
-                     (gcol0 + 32 <= p.N);
-    if (!vec && !p.d_tma) {
-      // lane l reads column gcol0 + l of the warp's 32 rows (64 contiguous
-      // bytes per instruction) into a 32 x 34-halfword block, then each thread
-      // takes its own row (pitch 17 words: no bank conflicts either way)
-      uint16_t* w = reinterpret_cast<uint16_t*>(wbuf);
-      const int row0 = grow - lane;
-      const int col = gcol0 + lane;
-      const uint16_t* cbase = reinterpret_cast<const uint16_t*>(p.C);
-      // all 32 loads in flight before the first use: one memory latency per chunk
-      uint16_t cv[32];
-#pragma unroll
-      for (int rr = 0; rr < 32; ++rr) {
-        const int gr = row0 + rr;
-        cv[rr] = (gr < p.M && col < p.N) ? __ldg(cbase + (int64_t)gr * p.ldc + col) : (uint16_t)0;
-      }
-#pragma unroll
-      for (int rr = 0; rr < 32; ++rr) w[rr * 34 + lane] = cv[rr];
-      __syncwarp();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(w[lane * 34 + j]), v[j]);
-      __syncwarp();
-    } else if (!row_ok) {
-    } else if (vec) {
+  } else if (cpath == kCVec) {
+    if (row_ok) {
 #pragma unroll
       for (int u4 = 0; u4 < 4; ++u4) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(crow) + u4);
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const uint32_t ws[4] = {cc.v[u4].x, cc.v[u4].y, cc.v[u4].z, cc.v[u4].w};
 #pragma unroll
         for (int h = 0; h < 4; ++h) {
-          v[u4 * 8 + 2 * h] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] & 0xFFFFu)),
-                                   v[u4 * 8 + 2 * h]);
+          v[u4 * 8 + 2 * h] =
+              fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] & 0xFFFFu)), v[u4 * 8 + 2 * h]);
           v[u4 * 8 + 2 * h + 1] =
               fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(ws[h] >> 16)), v[u4 * 8 + 2 * h + 1]);
         }
       }
+    }
+  } else if (cpath == kCCoop) {
+    uint16_t* w16 = reinterpret_cast<uint16_t*>(cstage);
+#pragma unroll
+    for (int rr = 0; rr < 32; ++rr) {
+      const int word = rr * 16 + ((lane >> 1) ^ ((rr >> 1) & 15));
+      w16[word * 2 + (lane & 1)] = cc.e[rr];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const int word = lane * 16 + ((j >> 1) ^ ((lane >> 1) & 15));
+      v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(w16[word * 2 + (j & 1)]), v[j]);
+    }
+    __syncwarp();
+  }
+  if (p.bias != nullptr) {
+    if (p.d_trans) {
+      if (row_ok) {
+        const float b = __ldg(p.bias + grow);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] += b;
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        if (gcol0 + j < p.N) v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(__ldg(crow + j)), v[j]);
+        if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
     }
-  }
-  if (p.bias != nullptr && !p.d_trans) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j)
-      if (gcol0 + j < p.N) v[j] += __ldg(p.bias + gcol0 + j);
   }
   if (p.act != kActNone) {
 #pragma unroll
@@ -367,6 +404,18 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) packed[j] = pack2<kBF16>(v[2 * j], v[2 * j + 1]);
+}
+
+// Shared memory the kCCoop path may use for one chunk: with TMA stores, the
+// staging buffer the next store will use, once its previous store has
+// finished reading it; with plain stores, the warp's first staging buffer.
+__device__ __forceinline__ uint8_t* c_stage_buffer(const GemmParams& p, int cpath, uint8_t* stage_buf, int buf,
+                                                   int buf_bytes, int lane) {
+  if (cpath != kCCoop) return nullptr;
+  if (!p.d_tma) return stage_buf;
+  if (lane == 0) bulk_wait_read<1>();
+  __syncwarp();
+  return stage_buf + buf * buf_bytes;
 }
 
 // Writes one 32-column chunk of the calling thread's row: through a swizzled
@@ -811,7 +860,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           if (lane == 0) mbar_arrive(&tmem_empty[acc]);
         }
         if (!ok) break;
-      } else {
+      }
+      // fp16/bf16: the first chunk's C is fetched before waiting for the
+      // accumulator, so its latency overlaps the mainloop
+      const bool writes_out = p.ksplit == 1 || rank == 0;
+      CChunk16 cc;
+      if constexpr (!kI8) {
+        if (writes_out) c_fetch16(p, c_path(p, n0), grow, n0, lane, cc);
         if (!mbar_wait(&tmem_full[unit & 1], (unit >> 1) & 1, wc)) break;
         tc_fence_after();
       }
@@ -917,7 +972,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
                 for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(re), (uint32_t)pr));
             }
           }
-          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, stage_buf, lane);
+          const int cpath = c_path(p, gcol0);
+          uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, Tr::kEpiBufBytes, lane);
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane);
+          if (c + 1 < BN / kEpiCols) c_fetch16(p, c_path(p, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
         }
 
         epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, Tr::kEpiBufBytes, buf,
