@@ -261,6 +261,9 @@ WORKLOADS = {
     # int8 x int8 -> int32 8192^3, uniform integers in [-128, 127], seed 3
     "i8_8192": dict(M=8192, N=8192, K=8192, dtype="i8", layoutA="row", layoutB="col", seed=3,
                     distA="int8", distB="int8", alpha=1.0, beta=0.0, act="none"),
+    # int8 4096^3: a smaller case of the int8 recipe, for profiling
+    "i8_4096": dict(M=4096, N=4096, K=4096, dtype="i8", layoutA="row", layoutB="col", seed=3,
+                    distA="int8", distB="int8", alpha=1.0, beta=0.0, act="none"),
     # bf16 8192^3 (the headline throughput shape), same recipe as bf16_4096 but alpha=1 beta=0
     "bf16_8192": dict(M=8192, N=8192, K=8192, dtype="bf16", layoutA="row", layoutB="col", seed=1,
                       distA="uniform", distB="uniform", alpha=1.0, beta=0.0, act="none"),
