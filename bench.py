@@ -249,6 +249,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pair", type=int, default=0, choices=[0, 1, 2],
                     help="kernel choice: 0 planner, 1 CTA-pair kernel where it applies, 2 single-CTA kernel")
+    ap.add_argument("--pair-tile-n", type=int, default=0, choices=[0, 256, 192, 128],
+                    help="CTA-pair tile width: 0 planner, else forced")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload)
@@ -268,6 +270,7 @@ def main():
     barrier(world)
     ttc.load()
     ttc.ttc_set_knob("pair", args.pair)
+    ttc.ttc_set_knob("pair_tile_n", args.pair_tile_n)
 
     p, alpha, beta, act = synth.make(spec)
     M, N, K = p.M, p.N, p.K

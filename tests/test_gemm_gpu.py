@@ -24,7 +24,7 @@ def _built():
     _build.build()
     ttc.load()
     for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab",
-              "split_k"):
+              "split_k", "pair_tile_n"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -413,3 +413,20 @@ def test_workspace_too_small_falls_back():
     p = synth.Problem(257, 131, 97, dtype="bf16", seed=32, distC="uniform", lda=98, ldb=99)
     d = run(p, 1.0, 1.0, workspace=64)
     check_full(p, d, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("width", [192, 128])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_pair_tile_widths(width, la, lb):
+    if width == 192 and lb == "row":
+        pytest.skip("192-wide pair tiles take a column-major B only")
+    ttc.ttc_set_knob("pair", 1)
+    ttc.ttc_set_knob("pair_tile_n", width)
+    try:
+        p = synth.Problem(520, 700, 200, dtype="bf16", layoutA=la, layoutB=lb, seed=33, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 1.0, 0.5, "gelu_tanh")
+        check_full(p, d, 1.0, 0.5, "gelu_tanh")
+    finally:
+        ttc.ttc_set_knob("pair_tile_n", 0)
+        ttc.ttc_set_knob("pair", 0)

@@ -32,6 +32,7 @@ std::atomic<int> g_force_tile_n{0};
 std::atomic<int> g_pair_mode{0};
 std::atomic<int> g_swap_mode{0};
 std::atomic<int> g_split_k{0};
+std::atomic<int> g_pair_tile_n{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -39,7 +40,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  int pair_clusters[2] = {-1, -1};  // resident CTA pairs (fp16, bf16); -1: not queried yet
+  int pair_clusters[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // resident CTA pairs [bf16][width 256/192/128]
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -229,6 +230,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
     case TTC_KNOB_SPLIT_K:
       if (value < 0 || value > 8) return TTC_ERR_INVALID_ARG;
       g_split_k.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_PAIR_TILE_N:
+      if (value != 0 && value != 256 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
+      g_pair_tile_n.store((int)value);
       return TTC_OK;
   }
   return TTC_ERR_INVALID_ARG;
@@ -494,29 +499,54 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // pair of SMs; chosen for problems at least one pair tile in each direction
   const int pair_mode = g_pair_mode.load();
   const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap && ksplit == 1;
-  const int64_t pair_tiles = ((M + kPairBM - 1) / kPairBM) * ((N + kPairBN - 1) / kPairBN);
-  if (pair_ok && pair_mode != 2 &&
-      (pair_mode == 1 || (M >= kPairBM && N >= kPairBN && pair_tiles * 4 >= dev->sm_count))) {
+  if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= 256))) {
     const bool bf16 = dtype == TTC_BF16;
-    int& clusters = dev->pair_clusters[bf16 ? 1 : 0];
-    if (clusters < 0) {
-      std::lock_guard<std::mutex> lk(g_mu);
-      if (clusters < 0) clusters = pair_max_clusters(bf16);
+    // Pair tile width: the one whose tiles fill the resident pairs best,
+    // weighted by the width's measured relative rate (a narrower tile stages
+    // more A per column: 1, 0.87, 0.64 for 256, 192, 128 on bf16 8192^3) and by the share of its last
+    // column of tiles that lies inside N.  192 needs a K-major B (its half,
+    // 96 columns, is not a whole number of 64-column MN-major slabs).
+    const int forced_pbn = g_pair_tile_n.load();
+    int pbn = 0, clusters = 0;
+    double best = -1.0;
+    const int widths[3] = {256, 192, 128};
+    for (int wi = 0; wi < 3; ++wi) {
+      const int w = widths[wi];
+      if ((forced_pbn != 0 && w != forced_pbn) || (b_mn && w == 192)) continue;
+      int& cl = dev->pair_clusters[bf16 ? 1 : 0][wi];
+      if (cl < 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (cl < 0) cl = pair_max_clusters(bf16, w);
+      }
+      if (cl <= 0) continue;
+      const int64_t nb = (N + w - 1) / w;
+      const int64_t tiles = ((M + kPairBM - 1) / kPairBM) * nb;
+      const int64_t waves = (tiles + cl - 1) / cl;
+      const double fill = (double)tiles / (double)(waves * cl);
+      const double inside = (double)N / (double)(nb * w);
+      const double rate = w == 256 ? 1.0 : w == 192 ? 0.87 : 0.64;
+      const double score = fill * inside * rate;
+      if (score > best + 1e-9) {
+        best = score;
+        pbn = w;
+        clusters = cl;
+      }
     }
-    if (clusters > 0) {
+    const int64_t pair_tiles = pbn ? ((M + kPairBM - 1) / kPairBM) * ((N + pbn - 1) / pbn) : 0;
+    if (pbn != 0 && (pair_mode == 1 || pair_tiles * 4 >= dev->sm_count)) {
       if (K > 0) {
-        // each CTA loads whole 128-row A boxes and its 128 columns of the B tile
+        // each CTA loads whole 128-row A boxes and its pbn / 2 columns of the B tile
         bool ok = a_mn || encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-        ok = ok && (!b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+        ok = ok && (!b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, pbn / 2, CU_TENSOR_MAP_SWIZZLE_128B)
                           : encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B));
         if (!ok) return TTC_ERR_CUDA;
       }
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
-      prm.num_n_blocks = (int)((N + kPairBN - 1) / kPairBN);
+      prm.num_n_blocks = (int)((N + pbn - 1) / pbn);
       prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
       prm.group_m = prm.num_m_blocks < 8 ? prm.num_m_blocks : 8;
       const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
-      if (launch_pair(bf16, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+      if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       return TTC_OK;
     }

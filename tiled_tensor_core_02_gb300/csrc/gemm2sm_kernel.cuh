@@ -26,12 +26,15 @@
 namespace ttc {
 
 constexpr int kPairBM = 256;
-constexpr int kPairBN = 256;
 constexpr int kPairThreads = 192;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..5 epilogue
 
+// Pair tile 256 x BN (BN = 256, 192 or 128): each CTA stages 128 A rows and
+// BN / 2 B columns per k-block.
+template <int BN>
 struct PairCfg {
-  static constexpr int kAHalfBytes = 128 * kBK * 2;  // 16 KiB
-  static constexpr int kBHalfBytes = 128 * kBK * 2;  // 16 KiB
+  static constexpr int kBHalf = BN / 2;
+  static constexpr int kAHalfBytes = 128 * kBK * 2;     // 16 KiB
+  static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // 16 / 12 / 8 KiB
   static constexpr int kStageBytes = kAHalfBytes + kBHalfBytes;
   static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
@@ -39,15 +42,18 @@ struct PairCfg {
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesRaw = (kSmemLimit - 1024 - kBarBytes - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
-  static constexpr int kTmemCols = 2 * kPairBN;  // two accumulators
+  static constexpr int kTmemCols = 2 * BN > 256 ? 512 : 256;  // two accumulators, a power of two
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
+  static_assert(BN == 256 || BN == 192 || BN == 128, "pair tile width");
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
-template <bool kBF16>
+template <int BN, bool kBF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
+  using PairCfg = ttc::PairCfg<BN>;
+  constexpr int kPairBN = BN;
   constexpr int S = PairCfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -114,7 +120,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         int mb, nb;
         tile_coords(t, p, mb, nb);
         const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
-        const int n0 = nb * kPairBN + (int)rank * 128;  // this CTA's B columns
+        const int n0 = nb * kPairBN + (int)rank * PairCfg::kBHalf;  // this CTA's B columns
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
@@ -138,8 +144,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (!p.b_mn) {
             tma_load_2d_pair(b, &p.tmB, k0, n0, full_leader, pol);
           } else {
-            tma_load_2d_pair(b, &p.tmB, n0, k0, full_leader, pol);
-            tma_load_2d_pair(b + 8192, &p.tmB, n0 + 64, k0, full_leader, pol);
+#pragma unroll
+            for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
+              tma_load_2d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, full_leader, pol);
           }
           if (++stage == S) {
             stage = 0;

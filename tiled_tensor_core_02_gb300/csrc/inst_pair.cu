@@ -8,7 +8,7 @@
 namespace ttc {
 
 namespace {
-template <bool kBF16>
+template <int BN, bool kBF16>
 cudaError_t set_smem_attr() {
   static std::atomic<bool> done[64];
   int dev = 0;
@@ -16,37 +16,51 @@ cudaError_t set_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev].load()) {
-    e = cudaFuncSetAttribute(gemm_pair_kernel<kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<BN, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg<BN>::kSmemBytes);
     if (e != cudaSuccess) return e;
     done[dev].store(true);
   }
   return cudaSuccess;
 }
-}  // namespace
 
-// Largest number of CTA pairs that can be resident at once (0 on error).
-int pair_max_clusters(bool bf16) {
-  cudaError_t e = bf16 ? set_smem_attr<true>() : set_smem_attr<false>();
-  if (e != cudaSuccess) return 0;
+template <int BN, bool kBF16>
+int max_clusters() {
+  if (set_smem_attr<BN, kBF16>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<BN>::kSmemBytes;
   int n = 0;
-  e = bf16 ? cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<true>, &cfg)
-           : cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<false>, &cfg);
-  return e == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, kBF16>, &cfg) == cudaSuccess ? n : 0;
 }
 
-cudaError_t launch_pair(bool bf16, const GemmParams& p, int clusters, cudaStream_t stream) {
-  cudaError_t e = bf16 ? set_smem_attr<true>() : set_smem_attr<false>();
+template <int BN, bool kBF16>
+cudaError_t launch(const GemmParams& p, int clusters, cudaStream_t stream) {
+  const cudaError_t e = set_smem_attr<BN, kBF16>();
   if (e != cudaSuccess) return e;
-  if (bf16)
-    gemm_pair_kernel<true><<<2 * clusters, kPairThreads, PairCfg::kSmemBytes, stream>>>(p);
-  else
-    gemm_pair_kernel<false><<<2 * clusters, kPairThreads, PairCfg::kSmemBytes, stream>>>(p);
+  gemm_pair_kernel<BN, kBF16><<<2 * clusters, kPairThreads, PairCfg<BN>::kSmemBytes, stream>>>(p);
   return cudaGetLastError();
+}
+}  // namespace
+
+// Largest number of CTA pairs that can be resident at once (0 on error).
+int pair_max_clusters(bool bf16, int bn) {
+  switch (bn) {
+    case 256: return bf16 ? max_clusters<256, true>() : max_clusters<256, false>();
+    case 192: return bf16 ? max_clusters<192, true>() : max_clusters<192, false>();
+    case 128: return bf16 ? max_clusters<128, true>() : max_clusters<128, false>();
+  }
+  return 0;
+}
+
+cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream) {
+  switch (bn) {
+    case 256: return bf16 ? launch<256, true>(p, clusters, stream) : launch<256, false>(p, clusters, stream);
+    case 192: return bf16 ? launch<192, true>(p, clusters, stream) : launch<192, false>(p, clusters, stream);
+    case 128: return bf16 ? launch<128, true>(p, clusters, stream) : launch<128, false>(p, clusters, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace ttc
