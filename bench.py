@@ -251,6 +251,7 @@ def main():
                     help="kernel choice: 0 planner, 1 CTA-pair kernel where it applies, 2 single-CTA kernel")
     ap.add_argument("--pair-tile-n", type=int, default=0, choices=[0, 256, 192, 128],
                     help="CTA-pair tile width: 0 planner, else forced")
+    ap.add_argument("--group-m", type=int, default=0, help="tile rows per rasterization group (0: default)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload)
@@ -271,6 +272,7 @@ def main():
     ttc.load()
     ttc.ttc_set_knob("pair", args.pair)
     ttc.ttc_set_knob("pair_tile_n", args.pair_tile_n)
+    ttc.ttc_set_knob("group_m", args.group_m)
 
     p, alpha, beta, act = synth.make(spec)
     M, N, K = p.M, p.N, p.K

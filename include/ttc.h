@@ -194,6 +194,8 @@ const char* ttc_status_string(ttc_status status);
  *     whenever it applies (fp16/bf16 operands TMA can describe); 2 never.
  *   TTC_KNOB_SWAP_AB: 0 lets the planner choose whether to compute D or
  *     D^T = B^T A^T (for skinny problems); 1 always D^T; 2 always D.
+ *   TTC_KNOB_GROUP_M: tile rasterization: consecutive tiles walk this many
+ *     tile rows per column of tiles (0: 16 for single CTAs, 8 for pairs).
  *   TTC_KNOB_PAIR_TILE_N: 0 lets the planner choose the CTA-pair tile width;
  *     256, 192 or 128 forces it (192 only with a column-major B).
  *   TTC_KNOB_SPLIT_K: 0 lets the planner choose; 1..8 splits every tile's K
@@ -210,7 +212,8 @@ typedef enum {
   TTC_KNOB_PAIR = 5,
   TTC_KNOB_SWAP_AB = 6,
   TTC_KNOB_SPLIT_K = 7,
-  TTC_KNOB_PAIR_TILE_N = 8
+  TTC_KNOB_PAIR_TILE_N = 8,
+  TTC_KNOB_GROUP_M = 9
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

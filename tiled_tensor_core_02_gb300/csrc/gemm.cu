@@ -33,6 +33,7 @@ std::atomic<int> g_pair_mode{0};
 std::atomic<int> g_swap_mode{0};
 std::atomic<int> g_split_k{0};
 std::atomic<int> g_pair_tile_n{0};
+std::atomic<int> g_group_m{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -230,6 +231,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
     case TTC_KNOB_SPLIT_K:
       if (value < 0 || value > 8) return TTC_ERR_INVALID_ARG;
       g_split_k.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_GROUP_M:
+      if (value < 0 || value > 64) return TTC_ERR_INVALID_ARG;
+      g_group_m.store((int)value);
       return TTC_OK;
     case TTC_KNOB_PAIR_TILE_N:
       if (value != 0 && value != 256 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
@@ -475,7 +480,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   prm.num_n_blocks = (int)((N + bn - 1) / bn);
   prm.num_k_blocks = (int)((K + kBK - 1) / kBK);
   prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
-  prm.group_m = prm.num_m_blocks < 16 ? prm.num_m_blocks : 16;
+  const int gm1 = g_group_m.load() > 0 ? g_group_m.load() : 16;
+  prm.group_m = prm.num_m_blocks < gm1 ? prm.num_m_blocks : gm1;
   prm.ksplit = ksplit;
   prm.kb_split = (int)((prm.num_k_blocks + ksplit - 1) / ksplit);
   prm.a_mn = a_mn;
@@ -544,7 +550,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
       prm.num_n_blocks = (int)((N + pbn - 1) / pbn);
       prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
-      prm.group_m = prm.num_m_blocks < 8 ? prm.num_m_blocks : 8;
+      const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
+      prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
       const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
       if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
