@@ -359,6 +359,97 @@ inline Layout logical_product(const Layout& a, const Layout& b) {
   return make_layout({a, composition(complement(a, a.size() * b.cosize()), b)});
 }
 
+// ------------------------------------------------------------------ per-mode tiling
+// Top-level mode i of a layout (the whole layout for a rank-1 leaf).
+inline Layout mode(const Layout& l, size_t i) {
+  if (l.shape.leaf) {
+    if (i != 0) throw std::out_of_range("mode index");
+    return l;
+  }
+  return Layout(l.shape.c.at(i), l.stride.c.at(i));
+}
+
+inline size_t rank(const Layout& l) { return l.shape.rank(); }
+
+// logical_divide applied to each top-level mode with its own tiler:
+// result mode i = (tile_i, rest_i).
+inline Layout logical_divide_by_mode(const Layout& l, const std::vector<Layout>& tilers) {
+  if (tilers.size() != rank(l)) throw std::invalid_argument("one tiler per mode");
+  std::vector<Layout> out;
+  for (size_t i = 0; i < tilers.size(); ++i) out.push_back(logical_divide(mode(l, i), tilers[i]));
+  return make_layout(out);
+}
+
+// zipped_divide: the per-mode divide with the tile modes gathered first and
+// the rest modes second: ((tile_0, tile_1, ...), (rest_0, rest_1, ...)).
+// Mode 0 walks one tile, mode 1 picks the tile.
+inline Layout zipped_divide(const Layout& l, const std::vector<Layout>& tilers) {
+  const Layout d = logical_divide_by_mode(l, tilers);
+  std::vector<Layout> tiles, rests;
+  for (size_t i = 0; i < tilers.size(); ++i) {
+    const Layout m = mode(d, i);
+    tiles.push_back(mode(m, 0));
+    rests.push_back(mode(m, 1));
+  }
+  return make_layout({make_layout(tiles), make_layout(rests)});
+}
+
+// tiled_divide: as zipped_divide, with the rest modes flattened into
+// top-level modes: ((tile_0, tile_1, ...), rest_0, rest_1, ...), so a tile is
+// picked by one index per mode (the way the transpose kernel of "4.21 What
+// is CuTe?" indexes (make_coord(_, _), blockIdx.x, blockIdx.y)).
+inline Layout tiled_divide(const Layout& l, const std::vector<Layout>& tilers) {
+  const Layout z = zipped_divide(l, tilers);
+  std::vector<Layout> out{mode(z, 0)};
+  const Layout rests = mode(z, 1);
+  for (size_t i = 0; i < rank(rests); ++i) out.push_back(mode(rests, i));
+  return make_layout(out);
+}
+
+// The per-mode position of the thread whose index (thr's value) is `idx`:
+// one flat (colexicographic) coordinate per top-level mode of `thr`.
+inline std::vector<int64_t> thread_coordinate(const Layout& thr, int64_t idx) {
+  for (int64_t i = 0; i < thr.size(); ++i) {
+    if (thr(i) != idx) continue;
+    std::vector<int64_t> c;
+    int64_t rest = i;
+    for (size_t m = 0; m < rank(thr); ++m) {
+      const int64_t n = product(mode(thr, m).shape);
+      c.push_back(rest % n);
+      rest /= n;
+    }
+    return c;
+  }
+  throw std::invalid_argument("index not in the thread layout's image");
+}
+
+// local_partition(tile, thr, idx): the elements of `tile` thread `idx` of the
+// thread layout `thr` owns when the tile is split into thr's shape, thread
+// (i, j, ...) taking elements (i + T_0 a, j + T_1 b, ...).  Returned as the
+// offset of the thread's first element plus the layout of its elements over
+// (a, b, ...).  Needs tile extents that the thread extents divide.
+struct Partition {
+  int64_t offset;
+  Layout layout;
+};
+
+inline Partition local_partition(const Layout& tile, const Layout& thr, int64_t idx) {
+  if (rank(tile) != rank(thr)) throw std::invalid_argument("tile and thread layout ranks differ");
+  std::vector<Layout> tilers;
+  for (size_t i = 0; i < rank(thr); ++i) {
+    const int64_t t = product(mode(thr, i).shape);
+    if (product(mode(tile, i).shape) % t != 0) throw std::invalid_argument("thread extent does not divide tile");
+    tilers.push_back(Layout(IntTuple(t), IntTuple(1)));
+  }
+  const Layout z = zipped_divide(tile, tilers);
+  const std::vector<int64_t> c = thread_coordinate(thr, idx);
+  // offset of the thread's element in tile 0: the tile mode evaluated at c
+  const Layout tm = mode(z, 0);
+  int64_t off = 0;
+  for (size_t i = 0; i < rank(thr); ++i) off += mode(tm, i)(c[i]);
+  return Partition{off, mode(z, 1)};
+}
+
 // The strip-mined thread map as a layout (thread, vector element, iteration)
 // -> offset in a row-major tile of pitch `cols`:
 //   ((column_groups, threads / column_groups), vec, iterations)

@@ -151,3 +151,40 @@ def stripmined_predicate(rows, cols, threads, vec, extent_rows, extent_cols, tid
     vector's first column < extent_cols (row_stride from the tile, sec. 4.3)."""
     r, c = stripmined_coords(rows, cols, threads, vec, tid, it)
     return r < extent_rows and c < extent_cols
+
+
+# ---------------------------------------------------------------- per-mode tiling
+
+def zipped_divide_table(shape, stride, tilers):
+    """zipped_divide of a rank-r layout by r contiguous tilers (t_i:1), from the
+    definition: element (within-tile coordinate w, tile coordinate q) sits at
+    per-mode coordinate w_i + t_i * q_i.  Domain: ((t_0, .., t_r-1), (n_0/t_0, ..)),
+    colexicographic.  Returns (domain shape, table)."""
+    modes = [(s, d) for s, d in zip(shape, stride)]
+    rests = [size(m[0]) // t for m, t in zip(modes, tilers)]
+    dom = (tuple(tilers), tuple(rests))
+    tab = []
+    for i in range(size(dom)):
+        crd = idx2crd(i, dom)
+        w, q = crd
+        val = 0
+        for k, (s, d) in enumerate(modes):
+            val += evaluate(s, d, w[k] + tilers[k] * q[k])
+        tab.append(val)
+    return dom, tab
+
+
+def local_partition_offsets(tile_shape, tile_stride, thr_shape, thr_stride, idx):
+    """Offsets of the tile elements thread `idx` owns: the thread at position
+    (c_0, c_1, ..) of the thread grid (the coordinate whose thread-layout value
+    is idx) owns per-mode coordinates c_k + T_k * a_k, walked colexicographically
+    over a.  From the definition on "4.21 What is CuTe?" (local_partition)."""
+    pos = next(i for i in range(size(thr_shape)) if evaluate(thr_shape, thr_stride, i) == idx)
+    c = idx2crd(pos, tuple(size(s) for s in thr_shape))
+    T = [size(s) for s in thr_shape]
+    reps = tuple(size(s) // t for s, t in zip(tile_shape, T))
+    out = []
+    for a_i in range(size(reps)):
+        a = idx2crd(a_i, reps)
+        out.append(sum(evaluate(s, d, c[k] + T[k] * a[k]) for k, (s, d) in enumerate(zip(tile_shape, tile_stride))))
+    return out

@@ -8,6 +8,9 @@
 //   product <sA> <dA> <sB> <dB>            -> "<shape>:<stride> | values"
 //   stripmined <rows> <cols> <threads> <vec> -> "<shape>:<stride> | values"
 //   swizzle <B> <off>                      -> Swizzle<B,4,3>(off)
+//   zdivide|tdivide <sL> <dL> <t0> <t1>    -> zipped / tiled divide of a rank-2 layout by
+//                                            the tilers t0:1, t1:1  ("<shape>:<stride> | values")
+//   partition <sT> <dT> <sThr> <dThr> <i>  -> "<offset> | values" of local_partition
 // Errors print "error <message>".
 #include <iostream>
 #include <sstream>
@@ -57,6 +60,23 @@ int main() {
         in >> r >> c >> t >> v;
         Layout l = stripmined_layout(StripMined{r, c, t, v});
         std::cout << to_string(l) << " | " << values(l) << "\n";
+      } else if (cmd == "zdivide" || cmd == "tdivide") {
+        std::string sl, dl;
+        int64_t t0, t1;
+        in >> sl >> dl >> t0 >> t1;
+        Layout l(parse_int_tuple(sl), parse_int_tuple(dl));
+        std::vector<Layout> tl{Layout(IntTuple(t0), IntTuple(1)), Layout(IntTuple(t1), IntTuple(1))};
+        Layout r = cmd == "zdivide" ? zipped_divide(l, tl) : tiled_divide(l, tl);
+        std::cout << to_string(r) << " | " << values(r) << "\n";
+      } else if (cmd == "partition") {
+        std::string st, dt, sh, dh;
+        int64_t idx;
+        in >> st >> dt >> sh >> dh >> idx;
+        Partition pt = local_partition(Layout(parse_int_tuple(st), parse_int_tuple(dt)),
+                                       Layout(parse_int_tuple(sh), parse_int_tuple(dh)), idx);
+        std::string v;
+        for (int64_t i = 0; i < pt.layout.size(); ++i) v += (i ? " " : "") + std::to_string(pt.offset + pt.layout(i));
+        std::cout << pt.offset << " | " << v << "\n";
       } else if (cmd == "swizzle") {
         int b;
         uint32_t off;
