@@ -87,6 +87,30 @@ ttc_status ttc_gemm(int64_t M, int64_t N, int64_t K,
                     ttc_act act, ttc_dtype dtype, void* stream);
 
 /*
+ * Strided batched GEMM: for b in [0, batch),
+ *   D_b = act(alpha * A_b * B_b + beta * C_b + bias)
+ * where operand X_b starts strideX elements after X_0 (X = A, B, C, D) and
+ * every matrix has the layout and leading dimension given, as in ttc_gemm.
+ * A stride of 0 shares that operand among all batches (e.g. one B for every
+ * A_b); bias is shared.  The batches form one launch: their tiles are walked
+ * together by the persistent kernels.  The pages name batched layouts as a
+ * use of layout composition ("Advanced CUTLASS Architecture and Kernel
+ * Optimization", Functional Composition: a layout for matrices composed with
+ * one for how matrices are batched).
+ * Errors as ttc_gemm, plus TTC_ERR_INVALID_ARG for a negative batch or stride,
+ * or (batch > 1) a strideD below (M - 1) * ldd + N so that D batches would
+ * overlap; a C that aliases D in place needs strideC == strideD.  batch == 0
+ * is a no-op.  batch > 65535 is TTC_ERR_UNSUPPORTED.
+ */
+ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, int64_t strideA, ttc_layout layoutA,
+                                    const void* B, int64_t ldb, int64_t strideB, ttc_layout layoutB,
+                                    const void* C, int64_t ldc, int64_t strideC,
+                                    void* D, int64_t ldd, int64_t strideD,
+                                    float alpha, float beta, const float* bias,
+                                    ttc_act act, ttc_dtype dtype, void* stream);
+
+/*
  * As ttc_gemm, with caller-provided device workspace.  An operand that TMA
  * cannot read (a base not 16-byte aligned, or a pitch in bytes that is not a
  * multiple of 16: the tight leading dimensions of odd-sized matrices) is first

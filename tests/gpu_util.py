@@ -53,3 +53,42 @@ def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_d
     if out_np == np.int16:
         d = d.view(np.uint16)
     return d[: p.M * ldd].reshape(p.M, ldd)[:, : p.N] if p.M else d[:0].reshape(0, p.N)
+
+
+def run_batched(probs, strides, alpha=1.0, beta=0.0, act="none", share_b=False, ldd=None):
+    """Packs a list of same-shaped problems into strided buffers (stride in
+    elements per operand: dict with keys A, B, C, D; B's stride 0 when
+    share_b), runs ttc_gemm_strided_batched, and returns one output per batch."""
+    p0 = probs[0]
+    nb = len(probs)
+    out_np = np.int32 if p0.dtype == "i8" else np.int16
+    ldd = p0.N if ldd is None else ldd
+
+    def pack(bufs, stride, dtype):
+        n = max((len(bufs) - 1) * stride + max(b.size for b in bufs), 1)
+        big = np.zeros(n, dtype=dtype)
+        for i, b in enumerate(bufs):
+            big[i * stride:i * stride + b.size] = b
+        return big
+
+    A = to_dev(pack([q.A for q in probs], strides["A"], probs[0].A.dtype))
+    sB = 0 if share_b else strides["B"]
+    B = to_dev(pack([q.B for q in (probs[:1] if share_b else probs)], sB, probs[0].B.dtype))
+    C = to_dev(pack([q.C for q in probs], strides["C"], probs[0].C.dtype)) if p0.C is not None else None
+    bias = to_dev(p0.bias) if p0.bias is not None else None
+    sD = strides["D"]
+    D = torch.full((max((nb - 1) * sD + p0.M * ldd, 1),), -1,
+                   dtype=torch.int32 if out_np == np.int32 else torch.int16, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    st = ttc.ttc_gemm_strided_batched(nb, p0.M, p0.N, p0.K, A.data_ptr(), p0.lda, strides["A"], LAY[p0.layoutA],
+                                      B.data_ptr(), p0.ldb, sB, LAY[p0.layoutB],
+                                      C.data_ptr() if (C is not None and beta != 0.0) else None, p0.ldc,
+                                      strides["C"], D.data_ptr(), ldd, sD, alpha, beta,
+                                      bias.data_ptr() if bias is not None else None, ttc.ACT[act],
+                                      ttc.DTYPE[p0.dtype], s)
+    assert st == 0, ttc.STATUS.get(st, st)
+    assert ttc.ttc_get_device_error(s) == 0
+    d = D.cpu().numpy()
+    if out_np == np.int16:
+        d = d.view(np.uint16)
+    return [d[i * sD:i * sD + p0.M * ldd].reshape(p0.M, ldd)[:, :p0.N] for i in range(nb)]

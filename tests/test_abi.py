@@ -116,3 +116,15 @@ def test_static_scratch_rejects_oversized_problems(lib):
     st = ttc.ttc_gemm_static_scratch(4099, 64, 8191, P, 8191, R, P, 8191, C, None, 64, P * 2, 64, 1.0, 0.0,
                                      None, 0, BF16, None)
     assert st == 5 and ttc.ttc_status_string(st) == "TTC_ERR_SCRATCH_TOO_SMALL"
+
+
+def test_batched_validation(lib):
+    sb = ttc.ttc_gemm_strided_batched
+    # negative batch or stride; overlapping D batches; in-place C needs equal strides
+    assert sb(-1, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 1
+    assert sb(2, 64, 64, 64, P, 64, -5, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 1
+    assert sb(2, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4000, 1.0, 0.0, None, 0, BF16, None) == 1
+    assert sb(2, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, P * 2, 64, 0, P * 2, 64, 4096, 1.0, 1.0, None, 0, BF16, None) == 1
+    # empty batch is a no-op
+    assert sb(0, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 0
+    assert sb(70000, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 2

@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 import tiled_tensor_core_02_gb300 as ttc
-from gpu_util import run, to_dev
+from gpu_util import run, run_batched, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -430,3 +430,76 @@ def test_pair_tile_widths(width, la, lb):
     finally:
         ttc.ttc_set_knob("pair_tile_n", 0)
         ttc.ttc_set_knob("pair", 0)
+
+
+# ------------------------------------------------------------------ strided batched GEMM
+
+def batch_problems(nb, M, N, K, dtype="bf16", la="row", lb="col", seed=50, share_b=False, **kw):
+    probs = [synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=seed + i, **kw) for i in range(nb)]
+    if share_b:
+        for q in probs[1:]:
+            q.B, q.B_log = probs[0].B, probs[0].B_log
+    # one shared bias for every batch
+    for q in probs[1:]:
+        q.bias = probs[0].bias
+    return probs
+
+
+def check_batches(probs, outs, alpha, beta, act="none"):
+    for q, d in zip(probs, outs):
+        check_full(q, d, alpha, beta, act)
+
+
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_batched_all_layouts(la, lb):
+    probs = batch_problems(3, 200, 300, 150, la=la, lb=lb, distC="uniform", dist_bias="normal:0.5")
+    p0 = probs[0]
+    strides = {"A": p0.A.size + 64, "B": p0.B.size + 128, "C": p0.C.size + 8, "D": 200 * 300 + 64}
+    outs = run_batched(probs, strides, 1.0, 0.5, "gelu_tanh")
+    check_batches(probs, outs, 1.0, 0.5, "gelu_tanh")
+
+
+def test_batched_shared_b():
+    probs = batch_problems(4, 256, 192, 128, share_b=True)
+    p0 = probs[0]
+    strides = {"A": p0.A.size, "B": 0, "C": 0, "D": 256 * 192}
+    outs = run_batched(probs, strides, 1.0, 0.0, share_b=True)
+    check_batches(probs, outs, 1.0, 0.0)
+
+
+def test_batched_odd_strides_use_plain_loads():
+    probs = batch_problems(3, 130, 70, 90, distC="uniform")
+    p0 = probs[0]
+    strides = {"A": p0.A.size + 3, "B": p0.B.size + 5, "C": p0.C.size + 7, "D": 130 * 70 + 9}
+    outs = run_batched(probs, strides, 1.0, 1.0)
+    check_batches(probs, outs, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+def test_batched_large_tiles(pair):
+    ttc.ttc_set_knob("pair", pair)
+    try:
+        probs = batch_problems(2, 520, 600, 200, distC="uniform", dist_bias="normal:0.5")
+        p0 = probs[0]
+        strides = {"A": p0.A.size, "B": p0.B.size, "C": p0.C.size, "D": 520 * 600}
+        outs = run_batched(probs, strides, 1.0, 1.0, "relu")
+        check_batches(probs, outs, 1.0, 1.0, "relu")
+    finally:
+        ttc.ttc_set_knob("pair", 0)
+
+
+def test_batched_int8():
+    probs = batch_problems(3, 150, 130, 300, dtype="i8", distA="int8", distB="int8")
+    p0 = probs[0]
+    strides = {"A": p0.A.size + 16, "B": p0.B.size + 32, "C": 0, "D": 150 * 130 + 4}
+    outs = run_batched(probs, strides, 1.0, 0.0)
+    check_batches(probs, outs, 1.0, 0.0)
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (1024, 24, 1024)])
+def test_batched_skinny_split_and_transpose(M, N, K):
+    probs = batch_problems(3, M, N, K, distC="uniform")
+    p0 = probs[0]
+    strides = {"A": p0.A.size, "B": p0.B.size, "C": p0.C.size, "D": M * N}
+    outs = run_batched(probs, strides, 1.0, 1.0)
+    check_batches(probs, outs, 1.0, 1.0)

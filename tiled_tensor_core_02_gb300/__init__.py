@@ -32,7 +32,8 @@ KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_gene
         "group_m": 9}
 
 # Every symbol the C header declares (checked by the test suite).
-EXPORTS = ("ttc_gemm", "ttc_gemm_ws", "ttc_gemm_workspace_size", "ttc_gemm_static_scratch",
+EXPORTS = ("ttc_gemm", "ttc_gemm_strided_batched", "ttc_gemm_ws", "ttc_gemm_workspace_size",
+           "ttc_gemm_static_scratch",
            "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
 
 _lib = None
@@ -59,6 +60,9 @@ def load():
     i64, vp, f, i = ctypes.c_int64, ctypes.c_void_p, ctypes.c_float, ctypes.c_int
     L.ttc_gemm.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp]
     L.ttc_gemm.restype = i
+    L.ttc_gemm_strided_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, i, vp, i64, i64, i, vp, i64, i64,
+                                           vp, i64, i64, f, f, vp, i, i, vp]
+    L.ttc_gemm_strided_batched.restype = i
     L.ttc_gemm_ws.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp,
                               ctypes.c_size_t, vp]
     L.ttc_gemm_ws.restype = i
@@ -86,6 +90,13 @@ def ttc_gemm(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, b
     """Pointers are ints (device addresses) or None; stream is a cudaStream_t as int or None."""
     return load().ttc_gemm(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta,
                            bias, act, dtype, stream)
+
+
+def ttc_gemm_strided_batched(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, strideB, layoutB, C, ldc,
+                             strideC, D, ldd, strideD, alpha, beta, bias, act, dtype, stream) -> int:
+    return load().ttc_gemm_strided_batched(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, strideB,
+                                           layoutB, C, ldc, strideC, D, ldd, strideD, alpha, beta, bias,
+                                           act, dtype, stream)
 
 
 def ttc_gemm_ws(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act,

@@ -78,21 +78,38 @@ ttc_status device_info(DeviceInfo** out) {
   return TTC_OK;
 }
 
-// 2-D tensor map over a row-major-in-memory view: `inner` contiguous
-// elements, `outer` rows `pitch_elems` apart.
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
-               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer,
-               CUtensorMapSwizzle sw) {
-  cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {pitch_elems * (uint64_t)esize};
-  cuuint32_t box[2] = {box_inner, box_outer};
-  cuuint32_t estr[2] = {1, 1};
-  return g_encode(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+// Batch layout of one operand for the 3-D tensor maps: `count` batches
+// `stride` elements apart (count 1 for an unbatched or shared operand).
+struct BatchDim {
+  uint64_t count = 1;
+  uint64_t stride = 0;
+};
+
+// 3-D tensor map over a row-major-in-memory view: `inner` contiguous
+// elements, `outer` rows `pitch_elems` apart, and the batch dimension.  Boxes
+// are box_inner x box_outer x 1.
+bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+               uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
+               BatchDim bd = BatchDim()) {
+  const uint64_t pitch = pitch_elems * (uint64_t)esize;
+  // one batch: a stride past the matrix (any 16-byte multiple is accepted)
+  const uint64_t bstride = bd.count > 1 ? bd.stride * (uint64_t)esize : (pitch * outer + 15) / 16 * 16;
+  cuuint64_t dims[3] = {inner, outer, bd.count};
+  cuuint64_t strides[2] = {pitch, bstride};
+  cuuint32_t box[3] = {box_inner, box_outer, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 bool tma_ok(const void* p, int64_t ld, int esize) {
   return (reinterpret_cast<uintptr_t>(p) % 16 == 0) && ((ld * esize) % 16 == 0) && ld * esize < (1ll << 40);
+}
+
+// A batch stride TMA can step by: none needed (one batch, or shared), or a
+// 16-byte multiple.
+bool tma_batch_ok(int64_t batch, int64_t stride, int esize) {
+  return batch <= 1 || stride == 0 || ((stride * esize) % 16 == 0 && stride * esize < (1ll << 40));
 }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -264,15 +281,16 @@ ttc_status ttc_get_device_error(void* stream) {
 static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,
                             const void* B, int64_t ldb, ttc_layout layoutB, const void* C, int64_t ldc, void* D,
                             int64_t ldd, float alpha, float beta, const float* bias, ttc_act act, ttc_dtype dtype,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+                            void* workspace, size_t workspace_bytes, void* stream, int64_t batch = 1,
+                            int64_t sA = 0, int64_t sB = 0, int64_t sC = 0, int64_t sD = 0) {
   // ------------------------------------------------------------ validation
-  if (M < 0 || N < 0 || K < 0) return TTC_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 0 || batch < 0 || sA < 0 || sB < 0 || sC < 0 || sD < 0) return TTC_ERR_INVALID_ARG;
   if ((layoutA != TTC_ROW_MAJOR && layoutA != TTC_COL_MAJOR) ||
       (layoutB != TTC_ROW_MAJOR && layoutB != TTC_COL_MAJOR))
     return TTC_ERR_INVALID_ARG;
   if (act != TTC_ACT_NONE && act != TTC_ACT_RELU && act != TTC_ACT_GELU_TANH) return TTC_ERR_INVALID_ARG;
   if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return TTC_ERR_INVALID_ARG;
-  if (M == 0 || N == 0) return TTC_OK;
+  if (M == 0 || N == 0 || batch == 0) return TTC_OK;
   const int64_t a_min = layoutA == TTC_ROW_MAJOR ? K : M;
   const int64_t b_min = layoutB == TTC_ROW_MAJOR ? N : K;
   if (lda < (a_min > 1 ? a_min : 1) || ldb < (b_min > 1 ? b_min : 1) || ldd < N) return TTC_ERR_INVALID_ARG;
@@ -283,14 +301,17 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (beta != 0.0f) {
     const int64_t c_bytes = ((M - 1) * ldc + N) * out_esize;
     const int64_t d_bytes = ((M - 1) * ldd + N) * out_esize;
-    const bool in_place = (C == D) && (ldc == ldd);
+    const bool in_place = (C == D) && (ldc == ldd) && (sC == sD);
     if (!in_place && ranges_overlap(C, c_bytes, D, d_bytes)) return TTC_ERR_INVALID_ARG;
   }
+  // the batches of D may not overlap one another
+  if (batch > 1 && sD < (M - 1) * ldd + N) return TTC_ERR_INVALID_ARG;
   if (dtype == TTC_I8 &&
       (bias != nullptr || act != TTC_ACT_NONE || alpha != 1.0f || (beta != 0.0f && beta != 1.0f)))
     return TTC_ERR_UNSUPPORTED;
   const int64_t lim = 0x7FFFFFFFll;
-  if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim || ldd > lim) return TTC_ERR_UNSUPPORTED;
+  if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim || ldd > lim || batch > 65535)
+    return TTC_ERR_UNSUPPORTED;
   const int in_esize = dtype == TTC_I8 ? 1 : 2;
   // every pointer must be aligned to its element type
   if ((K > 0 && (reinterpret_cast<uintptr_t>(A) % in_esize || reinterpret_cast<uintptr_t>(B) % in_esize)) ||
@@ -307,7 +328,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (M == 1 && !tma_ok(D, ldd, out_esize) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 16);
 
   // ------------------------------------------------------------ workspace: repack what TMA cannot read
-  if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 && !g_force_generic_load.load()) {
+  if (batch == 1 && workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
+      !g_force_generic_load.load()) {
     const RepackPlan rp = plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, in_esize);
     if (rp.bytes > 0 && rp.bytes <= workspace_bytes) {
       uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -366,7 +388,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
         if (bk_mn && cand < 64) continue;
         // a tile wider than the padded N only wastes work
         if (forced_bn == 0 && cand > 32 && cand / 2 >= nk) continue;
-        const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + cand - 1) / cand);
+        const int64_t tiles = batch * ((mk + kBM - 1) / kBM) * ((nk + cand - 1) / cand);
         const int sp = forced_bn == 0 ? split_for(tiles, cand) : 1;
         const double rate = cand == 256 ? 1.0 : cand == 128 ? 0.7 : cand == 64 ? 0.45 : 0.3;
         const double ctas = (double)(tiles * sp < dev->sm_count ? tiles * sp : dev->sm_count);
@@ -391,7 +413,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     const int64_t mk = swap ? N : M, nk = swap ? M : N;
     const bool bk_mn = swap ? layoutA == TTC_COL_MAJOR : layoutB == TTC_ROW_MAJOR;
     bn = (bk_mn || nk > 32) ? 64 : 32;
-    const int64_t tiles = ((mk + kBM - 1) / kBM) * ((nk + bn - 1) / bn);
+    const int64_t tiles = batch * ((mk + kBM - 1) / kBM) * ((nk + bn - 1) / bn);
     ksplit = 1;
     while (ksplit < 8 && tiles * ksplit * 2 <= dev->sm_count && nkb_total / (ksplit * 2) >= 4) ksplit *= 2;
   }
@@ -404,6 +426,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     std::swap(M, N);
     std::swap(A, B);
     std::swap(lda, ldb);
+    std::swap(sA, sB);
     const ttc_layout la = layoutA;
     layoutA = layoutB == TTC_ROW_MAJOR ? TTC_COL_MAJOR : TTC_ROW_MAJOR;
     layoutB = la == TTC_ROW_MAJOR ? TTC_COL_MAJOR : TTC_ROW_MAJOR;
@@ -414,9 +437,11 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
 
   // ------------------------------------------------------------ plan
   const bool load_tma = dtype != TTC_I8 && !g_force_generic_load.load() &&
-                        (K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2)));
+                        (K == 0 || (tma_ok(A, lda, 2) && tma_ok(B, ldb, 2) && tma_batch_ok(batch, sA, 2) &&
+                                    tma_batch_ok(batch, sB, 2)));
   const bool load_tma_i8 = dtype == TTC_I8 && !g_force_generic_load.load() &&
-                           (K == 0 || (tma_ok(A, lda, 1) && tma_ok(B, ldb, 1)));
+                           (K == 0 || (tma_ok(A, lda, 1) && tma_ok(B, ldb, 1) && tma_batch_ok(batch, sA, 1) &&
+                                       tma_batch_ok(batch, sB, 1)));
   int mode;
   if (dtype == TTC_I8)
     mode = load_tma_i8 ? kModeI8Tma : kModeI8;
@@ -424,7 +449,12 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
   else
     mode = dtype == TTC_BF16 ? kModeGenBF16 : kModeGenF16;
-  const bool store_tma = !swap && tma_ok(D, ldd, out_esize) && !g_force_generic_store.load();
+  const bool store_tma =
+      !swap && tma_ok(D, ldd, out_esize) && tma_batch_ok(batch, sD, out_esize) && !g_force_generic_store.load();
+  // batch dimensions of the tensor maps: a shared operand (stride 0) keeps one batch
+  const BatchDim bdA{batch > 1 && sA != 0 ? (uint64_t)batch : 1u, (uint64_t)sA};
+  const BatchDim bdB{batch > 1 && sB != 0 ? (uint64_t)batch : 1u, (uint64_t)sB};
+  const BatchDim bdD{batch > 1 ? (uint64_t)batch : 1u, (uint64_t)sD};
   if (bn == 16 || (b_mn && bn < 64) || bn > max_bn) return TTC_ERR_UNSUPPORTED;
 
   static_assert(sizeof(GemmParams) <= 4096, "kernel parameter space");
@@ -434,10 +464,10 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (K > 0 && mode == kModeI8Tma) {
     // raw int8 tiles, unswizzled: K-major boxes of 64 k x rows, MN-major boxes of rows x 64 k
     const CUtensorMapDataType d8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    bool ok = !a_mn ? encode_2d(&prm.tmA, d8, 1, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE)
-                    : encode_2d(&prm.tmA, d8, 1, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok = ok && (!b_mn ? encode_2d(&prm.tmB, d8, 1, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_NONE)
-                      : encode_2d(&prm.tmB, d8, 1, B, N, K, ldb, bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE));
+    bool ok = !a_mn ? encode_3d(&prm.tmA, d8, 1, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE, bdA)
+                    : encode_3d(&prm.tmA, d8, 1, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, bdA);
+    ok = ok && (!b_mn ? encode_3d(&prm.tmB, d8, 1, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_NONE, bdB)
+                      : encode_3d(&prm.tmB, d8, 1, B, N, K, ldb, bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, bdB));
     if (!ok) return TTC_ERR_CUDA;
   }
   // rows of A worth loading per tile: all 128, or only those that exist
@@ -446,21 +476,21 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (K > 0 && (mode == kModeTmaF16 || mode == kModeTmaBF16)) {
     bool ok;
     if (!a_mn)
-      ok = encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_3d(&prm.tmA, dt, 2, A, K, M, lda, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
     else
-      ok = encode_2d(&prm.tmA, dt, 2, A, M, K, lda, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_3d(&prm.tmA, dt, 2, A, M, K, lda, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
     if (!ok) return TTC_ERR_CUDA;
     if (!b_mn)
-      ok = encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_3d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
     else
-      ok = encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B);
+      ok = encode_3d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
     if (!ok) return TTC_ERR_CUDA;
   }
   if (store_tma) {
     const bool ok = dtype == TTC_I8
-                        ? encode_2d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32,
-                                    CU_TENSOR_MAP_SWIZZLE_128B)
-                        : encode_2d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+                        ? encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_128B, bdD)
+                        : encode_3d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B, bdD);
     if (!ok) return TTC_ERR_CUDA;
   }
 
@@ -479,7 +509,15 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   prm.num_m_blocks = (int)((M + kBM - 1) / kBM);
   prm.num_n_blocks = (int)((N + bn - 1) / bn);
   prm.num_k_blocks = (int)((K + kBK - 1) / kBK);
-  prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
+  prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+  prm.num_tiles = (int)batch * prm.tiles_per_batch;
+  prm.batch = (int)batch;
+  prm.a_bc = bdA.count > 1 ? 1 : 0;
+  prm.b_bc = bdB.count > 1 ? 1 : 0;
+  prm.a_bs = sA;
+  prm.b_bs = sB;
+  prm.c_bs = sC;
+  prm.d_bs = sD;
   const int gm1 = g_group_m.load() > 0 ? g_group_m.load() : 16;
   prm.group_m = prm.num_m_blocks < gm1 ? prm.num_m_blocks : gm1;
   prm.ksplit = ksplit;
@@ -526,7 +564,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       }
       if (cl <= 0) continue;
       const int64_t nb = (N + w - 1) / w;
-      const int64_t tiles = ((M + kPairBM - 1) / kPairBM) * nb;
+      const int64_t tiles = batch * ((M + kPairBM - 1) / kPairBM) * nb;
       const int64_t waves = (tiles + cl - 1) / cl;
       const double fill = (double)tiles / (double)(waves * cl);
       const double inside = (double)N / (double)(nb * w);
@@ -538,18 +576,19 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
         clusters = cl;
       }
     }
-    const int64_t pair_tiles = pbn ? ((M + kPairBM - 1) / kPairBM) * ((N + pbn - 1) / pbn) : 0;
+    const int64_t pair_tiles = pbn ? batch * ((M + kPairBM - 1) / kPairBM) * ((N + pbn - 1) / pbn) : 0;
     if (pbn != 0 && (pair_mode == 1 || pair_tiles * 4 >= dev->sm_count)) {
       if (K > 0) {
         // each CTA loads whole 128-row A boxes and its pbn / 2 columns of the B tile
-        bool ok = a_mn || encode_2d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-        ok = ok && (!b_mn ? encode_2d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, pbn / 2, CU_TENSOR_MAP_SWIZZLE_128B)
-                          : encode_2d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B));
+        bool ok = a_mn || encode_3d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
+        ok = ok && (!b_mn ? encode_3d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, pbn / 2, CU_TENSOR_MAP_SWIZZLE_128B, bdB)
+                          : encode_3d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdB));
         if (!ok) return TTC_ERR_CUDA;
       }
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
       prm.num_n_blocks = (int)((N + pbn - 1) / pbn);
-      prm.num_tiles = prm.num_m_blocks * prm.num_n_blocks;
+ prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+      prm.num_tiles = (int)batch * prm.tiles_per_batch;
       const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
       const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
@@ -580,6 +619,15 @@ ttc_status ttc_gemm_ws(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
                        size_t workspace_bytes, void* stream) {
   return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, workspace,
                    workspace_bytes, stream);
+}
+
+ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                    int64_t strideA, ttc_layout layoutA, const void* B, int64_t ldb,
+                                    int64_t strideB, ttc_layout layoutB, const void* C, int64_t ldc,
+                                    int64_t strideC, void* D, int64_t ldd, int64_t strideD, float alpha, float beta,
+                                    const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
+  return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, nullptr,
+                   0, stream, batch, strideA, strideB, strideC, strideD);
 }
 
 size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,

@@ -117,8 +117,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t armed_mask = 0, armed_parity = 0;
       bool ok = true;
       for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
-        int mb, nb;
-        tile_coords(t, p, mb, nb);
+        int bz, mb, nb;
+        tile_coords(t, p, bz, mb, nb);
+        const int za = bz * p.a_bc, zb = bz * p.b_bc;
         const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
         const int n0 = nb * kPairBN + (int)rank * PairCfg::kBHalf;  // this CTA's B columns
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
@@ -136,17 +137,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           uint8_t* b = sB + stage * PairCfg::kBHalfBytes;
           const int k0 = kb * kBK;
           if (!p.a_mn) {
-            tma_load_2d_pair(a, &p.tmA, k0, m0, full_leader, pol);
+            tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol);
           } else {
-            tma_load_2d_pair(a, &p.tmA, m0, k0, full_leader, pol);
-            tma_load_2d_pair(a + 8192, &p.tmA, m0 + 64, k0, full_leader, pol);
+            tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol);
+            tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol);
           }
           if (!p.b_mn) {
-            tma_load_2d_pair(b, &p.tmB, k0, n0, full_leader, pol);
+            tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol);
           } else {
 #pragma unroll
             for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
-              tma_load_2d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, full_leader, pol);
+              tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol);
           }
           if (++stage == S) {
             stage = 0;
@@ -228,15 +229,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
       const int acc = it & 1;
-      int mb, nb;
-      tile_coords(t, p, mb, nb);
+      int bz, mb, nb;
+      tile_coords(t, p, bz, mb, nb);
       const int m0 = mb * kPairBM + (int)rank * 128;
       const int n0 = nb * kPairBN;
       const int grow = m0 + q * 32 + lane;
       const bool row_ok = grow < p.M;
+      const EpiPtrs ep = epi_ptrs(p, bz, 2);
       // the first chunk's C is fetched before waiting for the accumulator
       CChunk16 cc;
-      c_fetch16(p, c_path(p, n0), grow, n0, lane, cc);
+      c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
       if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
       tc_fence_after();
 #pragma unroll 1
@@ -257,11 +259,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
-        const int cpath = c_path(p, gcol0);
+        const int cpath = c_path(p, ep, gcol0);
         uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, PairCfg::kEpiBufBytes, lane);
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane);
-        if (c + 1 < kPairBN / kEpiCols) c_fetch16(p, c_path(p, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
-        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane);
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
+        if (c + 1 < kPairBN / kEpiCols)
+          c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
+        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane,
+                           ep);
       }
     }
     if (p.d_tma && lane == 0) bulk_wait_all();

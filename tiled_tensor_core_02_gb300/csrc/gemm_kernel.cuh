@@ -85,6 +85,12 @@ struct GemmParams {
                      // stale data, which only reaches accumulator rows that are never stored
   int M, N, K;
   int num_m_blocks, num_n_blocks, num_k_blocks, num_tiles, group_m;
+  // strided batches: tiles [b * tiles_per_batch, (b + 1) * tiles_per_batch) belong
+  // to batch b; operand x of batch b starts x_bs elements after batch 0 (plain
+  // loads and stores); TMA boxes take batch coordinate b * a_bc (b_bc), 0 for an
+  // operand shared by every batch
+  int batch, tiles_per_batch, a_bc, b_bc;
+  int64_t a_bs, b_bs, c_bs, d_bs;
   int ksplit;     // CTAs per cluster that split one tile's k-blocks (1 = no split)
   int kb_split;   // k-blocks per split (the last split may get fewer, or none)
   int a_mn, b_mn;  // operand stored MN-major (A column-major / B row-major)
@@ -131,7 +137,9 @@ struct TileCfg {
   static_assert((2 * BN & (2 * BN - 1)) == 0, "TMEM allocation is a power of two");
 };
 
-__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& mb, int& nb) {
+__device__ __forceinline__ void tile_coords(int t, const GemmParams& p, int& bz, int& mb, int& nb) {
+  bz = t / p.tiles_per_batch;
+  t -= bz * p.tiles_per_batch;
   const int per_group = p.group_m * p.num_n_blocks;
   const int g = t / per_group;
   const int first_m = g * p.group_m;
@@ -295,11 +303,27 @@ enum CPath : int {
   kCTrans = 3,  // D^T orientation: lanes already hold consecutive elements of a C row
 };
 
-__device__ __forceinline__ int c_path(const GemmParams& p, int gcol0) {
+// The C and D of the batch a tile belongs to, and its batch index (the TMA
+// store's third coordinate).
+struct EpiPtrs {
+  const void* C;
+  void* D;
+  int bz;
+};
+
+__device__ __forceinline__ EpiPtrs epi_ptrs(const GemmParams& p, int bz, int out_bytes) {
+  EpiPtrs e;
+  e.C = p.C ? static_cast<const void*>(static_cast<const char*>(p.C) + (int64_t)bz * p.c_bs * out_bytes) : nullptr;
+  e.D = static_cast<char*>(p.D) + (int64_t)bz * p.d_bs * out_bytes;
+  e.bz = bz;
+  return e;
+}
+
+__device__ __forceinline__ int c_path(const GemmParams& p, const EpiPtrs& e, int gcol0) {
   if (p.beta == 0.0f) return kCNone;
   if (p.d_trans) return kCTrans;
   const bool vec =
-      ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) && (gcol0 + 32 <= p.N);
+      ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(e.C) & 15) == 0) && (gcol0 + 32 <= p.N);
   return vec ? kCVec : kCCoop;
 }
 
@@ -311,11 +335,11 @@ struct CChunk16 {
                     // loads are not waited on until the values are staged, a chunk later)
 };
 
-__device__ __forceinline__ void c_fetch16(const GemmParams& p, int path, int grow, int gcol0, int lane,
-                                          CChunk16& cc) {
+__device__ __forceinline__ void c_fetch16(const GemmParams& p, const EpiPtrs& e, int path, int grow, int gcol0,
+                                          int lane, CChunk16& cc) {
   if (path == kCVec) {
     if (grow < p.M) {
-      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.C) +
+      const uint4* src = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(e.C) +
                                                         (int64_t)grow * p.ldc + gcol0);
 #pragma unroll
       for (int u = 0; u < 4; ++u) cc.v[u] = __ldg(src + u);
@@ -326,7 +350,7 @@ __device__ __forceinline__ void c_fetch16(const GemmParams& p, int path, int gro
   } else if (path == kCCoop) {
     const int row0 = grow - lane;
     const int col = gcol0 + lane;
-    const uint16_t* cbase = reinterpret_cast<const uint16_t*>(p.C);
+    const uint16_t* cbase = reinterpret_cast<const uint16_t*>(e.C);
 #pragma unroll
     for (int rr = 0; rr < 32; ++rr) {
       const int g = row0 + rr;
@@ -344,13 +368,14 @@ __device__ __forceinline__ void c_fetch16(const GemmParams& p, int path, int gro
 template <bool kBF16>
 __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32_t (&r)[32], bool row_ok,
                                                int grow, int gcol0, uint32_t (&packed)[16], int cpath,
-                                               const CChunk16& cc, uint8_t* cstage, int lane) {
+                                               const CChunk16& cc, uint8_t* cstage, int lane,
+                                               const EpiPtrs& e) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
   if (cpath == kCTrans) {
     if (row_ok) {
-      const uint16_t* ccol = reinterpret_cast<const uint16_t*>(p.C) + grow;
+      const uint16_t* ccol = reinterpret_cast<const uint16_t*>(e.C) + grow;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (gcol0 + j < p.N)
@@ -425,7 +450,7 @@ __device__ __forceinline__ uint8_t* c_stage_buffer(const GemmParams& p, int cpat
 template <int kOutBytes, int kPacked>
 __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint32_t (&packed)[kPacked], bool row_ok,
                                                 int grow, int gcol0, int tile_row, uint8_t* stage_buf,
-                                                int buf_bytes, int& buf, int lane) {
+                                                int buf_bytes, int& buf, int lane, const EpiPtrs& e) {
   if (p.d_tma) {
     // staging buffer `buf` was last used two chunks ago; its store must
     // have finished reading shared memory
@@ -450,7 +475,7 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) {
-      tma_store_2d(&p.tmD, gcol0, tile_row, sb);
+      tma_store_3d(&p.tmD, gcol0, tile_row, e.bz, sb);
       bulk_commit();
     }
     buf ^= 1;
@@ -471,9 +496,9 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
         const int gr = row0 + rr;
         if (gr < p.M) {
           if constexpr (kOutBytes == 4)
-            reinterpret_cast<int32_t*>(p.D)[(int64_t)gr * p.ldd + col] = (int32_t)w[rr * 33 + lane];
+            reinterpret_cast<int32_t*>(e.D)[(int64_t)gr * p.ldd + col] = (int32_t)w[rr * 33 + lane];
           else
-            reinterpret_cast<uint16_t*>(p.D)[(int64_t)gr * p.ldd + col] =
+            reinterpret_cast<uint16_t*>(e.D)[(int64_t)gr * p.ldd + col] =
                 reinterpret_cast<const uint16_t*>(w)[rr * 34 + lane];
         }
       }
@@ -482,12 +507,12 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
   } else if (row_ok) {
     // lanes hold consecutive kernel rows = consecutive elements of a D row
     if constexpr (kOutBytes == 4) {
-      int32_t* dst = reinterpret_cast<int32_t*>(p.D) + grow;
+      int32_t* dst = reinterpret_cast<int32_t*>(e.D) + grow;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (gcol0 + j < p.N) dst[(int64_t)(gcol0 + j) * p.ldd] = (int32_t)packed[j];
     } else {
-      uint16_t* dst = reinterpret_cast<uint16_t*>(p.D) + grow;
+      uint16_t* dst = reinterpret_cast<uint16_t*>(e.D) + grow;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         if (gcol0 + j < p.N)
@@ -593,9 +618,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         uint32_t issued_mask = 0, issued_parity = 0;
         bool ok = true;
         for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-          int mb, nb;
-          tile_coords(t, p, mb, nb);
+          int bz, mb, nb;
+          tile_coords(t, p, bz, mb, nb);
           const int m0 = mb * kBM, n0 = nb * BN;
+          const int za = bz * p.a_bc, zb = bz * p.b_bc;
           for (int kb = k_lo; kb < k_hi; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
@@ -606,17 +632,17 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* b = sB + stage * Cfg::kBBytes;
             const int k0 = kb * kBK;
             if (!p.a_mn) {
-              tma_load_2d(a, &p.tmA, k0, m0, &full[stage], pol);
+              tma_load_3d(a, &p.tmA, k0, m0, za, &full[stage], pol);
             } else {
-              tma_load_2d(a, &p.tmA, m0, k0, &full[stage], pol);
-              if (p.a_boxes > 1) tma_load_2d(a + kABytes / 2, &p.tmA, m0 + 64, k0, &full[stage], pol);
+              tma_load_3d(a, &p.tmA, m0, k0, za, &full[stage], pol);
+              if (p.a_boxes > 1) tma_load_3d(a + kABytes / 2, &p.tmA, m0 + 64, k0, za, &full[stage], pol);
             }
             if (!p.b_mn) {
-              tma_load_2d(b, &p.tmB, k0, n0, &full[stage], pol);
+              tma_load_3d(b, &p.tmB, k0, n0, zb, &full[stage], pol);
             } else {
 #pragma unroll
               for (int h = 0; h < BN / 64; ++h)
-                tma_load_2d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, &full[stage], pol);
+                tma_load_3d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, &full[stage], pol);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -642,9 +668,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           uint32_t issued_mask = 0, issued_parity = 0;
           bool ok = true;
           for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-            int mb, nb;
-            tile_coords(t, p, mb, nb);
+            int bz, mb, nb;
+            tile_coords(t, p, bz, mb, nb);
             const int m0 = mb * kBM, n0 = nb * BN;
+            const int za = bz * p.a_bc, zb = bz * p.b_bc;
             for (int kb = k_lo; kb < k_hi; ++kb) {
               if (!mbar_wait(&empty8[st8], ph8 ^ 1u, wc)) {
                 ok = false;
@@ -655,13 +682,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               uint8_t* b = a + kBM * kBK;
               const int k0 = kb * kBK;
               if (!p.a_mn)
-                tma_load_2d(a, &p.tmA, k0, m0, &full8[st8], pol);
+                tma_load_3d(a, &p.tmA, k0, m0, za, &full8[st8], pol);
               else
-                tma_load_2d(a, &p.tmA, m0, k0, &full8[st8], pol);
+                tma_load_3d(a, &p.tmA, m0, k0, za, &full8[st8], pol);
               if (!p.b_mn)
-                tma_load_2d(b, &p.tmB, k0, n0, &full8[st8], pol);
+                tma_load_3d(b, &p.tmB, k0, n0, zb, &full8[st8], pol);
               else
-                tma_load_2d(b, &p.tmB, n0, k0, &full8[st8], pol);
+                tma_load_3d(b, &p.tmB, n0, k0, zb, &full8[st8], pol);
               issued_mask |= 1u << st8;
               issued_parity = (issued_parity & ~(1u << st8)) | (ph8 << st8);
               if (++st8 == S8) {
@@ -721,9 +748,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       int stage = 0;
       uint32_t phase = 0;
       for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
-        int mb, nb;
-        tile_coords(t, p, mb, nb);
+        int bz, mb, nb;
+        tile_coords(t, p, bz, mb, nb);
         const int m0 = mb * kBM, n0 = nb * BN;
+        constexpr int kInBytes = kI8 ? 1 : 2;
+        const void* Ab = static_cast<const char*>(p.A) + (int64_t)bz * p.a_bs * kInBytes;
+        const void* Bb = static_cast<const char*>(p.B) + (int64_t)bz * p.b_bs * kInBytes;
         bool ok = true;
         for (int kb = k_lo; kb < k_hi; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
@@ -734,13 +764,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           uint8_t* b = sB + stage * Cfg::kBBytes;
           const int k0 = kb * kBK;
           if (!p.a_mn)
-            generic_load_tile<kBM, kBK, kI8>(a, p.A, p.lda, m0, k0, p.M, p.K, p.a_vec, tid);
+            generic_load_tile<kBM, kBK, kI8>(a, Ab, p.lda, m0, k0, p.M, p.K, p.a_vec, tid);
           else
-            generic_load_tile<kBK, kBM, kI8>(a, p.A, p.lda, k0, m0, p.K, p.M, p.a_vec, tid);
+            generic_load_tile<kBK, kBM, kI8>(a, Ab, p.lda, k0, m0, p.K, p.M, p.a_vec, tid);
           if (!p.b_mn) {
-            generic_load_tile<BN, kBK, kI8>(b, p.B, p.ldb, n0, k0, p.N, p.K, p.b_vec, tid);
+            generic_load_tile<BN, kBK, kI8>(b, Bb, p.ldb, n0, k0, p.N, p.K, p.b_vec, tid);
           } else {
-            if constexpr (BN >= 64) generic_load_tile<kBK, BN, kI8>(b, p.B, p.ldb, k0, n0, p.K, p.N, p.b_vec, tid);
+            if constexpr (BN >= 64) generic_load_tile<kBK, BN, kI8>(b, Bb, p.ldb, k0, n0, p.K, p.N, p.b_vec, tid);
           }
           // generic-proxy writes must be visible to the tensor core (async proxy)
           fence_proxy_async_smem();
@@ -825,11 +855,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     bool ok = true;
     int red_it = 0;  // split-K: partial-sum chunks exchanged so far
     for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-      int mb, nb;
-      tile_coords(t, p, mb, nb);
+      int bz, mb, nb;
+      tile_coords(t, p, bz, mb, nb);
       const int m0 = mb * kBM, n0 = nb * BN;
       const int grow = m0 + row_in_tile;
       const bool row_ok = grow < p.M;
+      const EpiPtrs ep = epi_ptrs(p, bz, Tr::kOutBytes);
 
       // int8: exact int32 sums of the per-chunk partials, held in registers
       int32_t isum[kI8 ? BN / kEpiCols : 1][32];
@@ -866,7 +897,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       const bool writes_out = p.ksplit == 1 || rank == 0;
       CChunk16 cc;
       if constexpr (!kI8) {
-        if (writes_out) c_fetch16(p, c_path(p, n0), grow, n0, lane, cc);
+        if (writes_out) c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
         if (!mbar_wait(&tmem_full[unit & 1], (unit >> 1) & 1, wc)) break;
         tc_fence_after();
       }
@@ -884,13 +915,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = isum[c][j];
           if (p.beta != 0.0f && row_ok && p.d_trans) {
-            const int32_t* ccol = reinterpret_cast<const int32_t*>(p.C) + grow;
+            const int32_t* ccol = reinterpret_cast<const int32_t*>(ep.C) + grow;
 #pragma unroll
             for (int j = 0; j < 32; ++j)
               if (gcol0 + j < p.N) v[j] += __ldg(ccol + (int64_t)(gcol0 + j) * p.ldc);
           } else if (p.beta != 0.0f && row_ok) {
-            const int32_t* crow = reinterpret_cast<const int32_t*>(p.C) + (int64_t)grow * p.ldc + gcol0;
-            const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(p.C) & 15) == 0) &&
+            const int32_t* crow = reinterpret_cast<const int32_t*>(ep.C) + (int64_t)grow * p.ldc + gcol0;
+            const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(ep.C) & 15) == 0) &&
                              (gcol0 + 32 <= p.N);
             if (vec) {
 #pragma unroll
@@ -972,14 +1003,15 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
                 for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(re), (uint32_t)pr));
             }
           }
-          const int cpath = c_path(p, gcol0);
+          const int cpath = c_path(p, ep, gcol0);
           uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, Tr::kEpiBufBytes, lane);
-          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane);
-          if (c + 1 < BN / kEpiCols) c_fetch16(p, c_path(p, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
+          if (c + 1 < BN / kEpiCols)
+            c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
         }
 
         epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, Tr::kEpiBufBytes, buf,
-                                       lane);
+                                       lane, ep);
       }
       if constexpr (!kI8) ++unit;
       if (!ok) break;
