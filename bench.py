@@ -49,15 +49,18 @@ def workload_spec(name):
 
 
 def algorithmic_bytes(spec):
-    """Bytes the GEMM must move at least once: A, B, D, plus C when beta != 0 and the bias."""
+    """Bytes the GEMM must move at least once: A, B, D, plus C when beta != 0 and the bias
+    (for every batch of a batched workload; the bias once)."""
+    return spec.get("batch", 1) * single_problem_bytes(spec) + (spec["N"] * 4 if spec.get("dist_bias") else 0)
+
+
+def single_problem_bytes(spec):
     M, N, K = spec["M"], spec["N"], spec["K"]
     ein = 1 if spec["dtype"] == "i8" else 2
     eout = 4 if spec["dtype"] == "i8" else 2
     b = (M * K + K * N) * ein + M * N * eout
     if spec.get("beta", 0.0) != 0.0:
         b += M * N * eout
-    if spec.get("dist_bias"):
-        b += N * 4
     return b
 
 
@@ -229,7 +232,8 @@ DTYPE_NAME = {"bf16": "bf16", "f16": "f16", "i8": "int8"}
 
 
 def config_of(spec, name, world):
-    return {"workload": name, "M": spec["M"], "N": spec["N"], "K": spec["K"], "dtype": spec["dtype"],
+    return {"workload": name, "batch": spec.get("batch", 1), "M": spec["M"], "N": spec["N"], "K": spec["K"],
+            "dtype": spec["dtype"],
             "layoutA": spec["layoutA"], "layoutB": spec["layoutB"], "alpha": spec["alpha"],
             "beta": spec["beta"], "act": spec["act"], "bias": bool(spec.get("dist_bias")),
             "seed": spec["seed"], "parallelism": f"replicas{world}" if world > 1 else "single",
@@ -276,17 +280,25 @@ def main():
 
     p, alpha, beta, act = synth.make(spec)
     M, N, K = p.M, p.N, p.K
-    flops = 2.0 * M * N * K
+    nbatch = spec.get("batch", 1)
+    flops = 2.0 * M * N * K * nbatch
     esz_out = 4 if p.dtype == "i8" else 2
 
     def dev(a):
         a = np.ascontiguousarray(a)
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
 
-    A, B = dev(p.A), dev(p.B)
-    C = dev(p.C) if p.C is not None else None
+    if nbatch > 1:
+        # batches packed back to back (strides = one matrix each)
+        probs = synth.make_batch(spec)
+        A = dev(np.concatenate([q.A for q in probs]))
+        B = dev(np.concatenate([q.B for q in probs]))
+        C = dev(np.concatenate([q.C for q in probs])) if p.C is not None else None
+    else:
+        A, B = dev(p.A), dev(p.B)
+        C = dev(p.C) if p.C is not None else None
     bias = dev(p.bias) if p.bias is not None else None
-    D = torch.empty(M * N, dtype=torch.int32 if p.dtype == "i8" else torch.int16, device="cuda")
+    D = torch.empty(nbatch * M * N, dtype=torch.int32 if p.dtype == "i8" else torch.int16, device="cuda")
     need_flush = algorithmic_bytes(spec) <= 2 * 129e6
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda") if need_flush else None
     stream = torch.cuda.current_stream()
@@ -301,6 +313,15 @@ def main():
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
 
     def step(Ap=A, Bp=B, Cp=C, Dp=D):
+        if nbatch > 1:
+            st = ttc.ttc_gemm_strided_batched(
+                nbatch, M, N, K, Ap.data_ptr(), p.lda, p.A.size, lay[p.layoutA], Bp.data_ptr(), p.ldb, p.B.size,
+                lay[p.layoutB], Cp.data_ptr() if (Cp is not None and beta != 0.0) else None, p.ldc,
+                p.C.size if p.C is not None else 0, Dp.data_ptr(), N, M * N, alpha, beta,
+                bias.data_ptr() if bias is not None else None, ttc.ACT[act], ttc.DTYPE[p.dtype], s)
+            if st != 0:
+                raise ttc.TTCError(st)
+            return
         st = ttc.ttc_gemm_ws(M, N, K, Ap.data_ptr(), p.lda, lay[p.layoutA], Bp.data_ptr(), p.ldb,
                              lay[p.layoutB], Cp.data_ptr() if (Cp is not None and beta != 0.0) else None,
                              p.ldc, Dp.data_ptr(), N, alpha, beta,

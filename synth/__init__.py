@@ -261,6 +261,10 @@ WORKLOADS = {
     # int8 x int8 -> int32 8192^3, uniform integers in [-128, 127], seed 3
     "i8_8192": dict(M=8192, N=8192, K=8192, dtype="i8", layoutA="row", layoutB="col", seed=3,
                     distA="int8", distB="int8", alpha=1.0, beta=0.0, act="none"),
+    # strided batched bf16: 32 independent 1024^3 GEMMs in one call, uniform[-1,1], seeds 5..36
+    "bf16_batched_32x1024": dict(M=1024, N=1024, K=1024, dtype="bf16", layoutA="row", layoutB="col",
+                                 seed=5, distA="uniform", distB="uniform", alpha=1.0, beta=0.0,
+                                 act="none", batch=32),
     # int8 4096^3: a smaller case of the int8 recipe, for profiling
     "i8_4096": dict(M=4096, N=4096, K=4096, dtype="i8", layoutA="row", layoutB="col", seed=3,
                     distA="int8", distB="int8", alpha=1.0, beta=0.0, act="none"),
@@ -301,8 +305,16 @@ def all_workload_names():
 
 
 def make(spec, **override):
-    """Build the synth.Problem for a workload dict; returns (problem, alpha, beta, act)."""
+    """Build the synth.Problem for a workload dict; returns (problem, alpha, beta, act).
+    A batched workload returns the problem of batch 0 (see make_batch)."""
     s = dict(spec)
     s.update(override)
+    s.pop("batch", None)
     alpha, beta, act = s.pop("alpha"), s.pop("beta"), s.pop("act")
     return Problem(**s), alpha, beta, act
+
+
+def make_batch(spec):
+    """The problems of a batched workload: batch b drawn from seed + b."""
+    n = spec.get("batch", 1)
+    return [make(spec, seed=spec["seed"] + b)[0] for b in range(n)]
