@@ -42,10 +42,13 @@ def load_peaks():
 
 def workload_spec(name):
     import synth
+    if name in synth.TRANSPOSE_WORKLOADS:
+        return dict(synth.TRANSPOSE_WORKLOADS[name], kind="transpose")
     try:
         return synth.workload(name)
     except (KeyError, ValueError):
-        raise SystemExit(f"unknown workload {name}; choose from {synth.all_workload_names()}")
+        names = synth.all_workload_names() + sorted(synth.TRANSPOSE_WORKLOADS)
+        raise SystemExit(f"unknown workload {name}; choose from {names}")
 
 
 def algorithmic_bytes(spec):
@@ -260,6 +263,9 @@ def main():
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload)
     name = args.workload
+    if spec.get("kind") == "transpose":
+        return run_transpose_reference(args, spec, name) if args.impl == "reference" else \
+            run_transpose(args, spec, name)
     if args.impl == "reference":
         return run_reference(args, spec, name)
 
@@ -482,28 +488,237 @@ def main():
     return 0
 
 
-def kernel_source_hash():
+def kernel_source_hash(kind="gemm"):
+    """Hash of the sources the workload's kernel is built from: the transpose
+    kernel's own two files, or every other file under csrc/ for the GEMM."""
     import glob
     import hashlib
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "tiled_tensor_core_02_gb300", "csrc", "*"))):
+        is_t = os.path.basename(f).startswith("transpose.")
+        if is_t != (kind == "transpose"):
+            continue
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def load_traffic(name):
-    """DRAM bytes (read + write) per launch of the GEMM kernel from the committed
-    ncu summary; None when there is none or the kernel sources changed since."""
+def load_traffic(name, kind="gemm"):
+    """DRAM bytes (read + write) per launch of the workload's kernel from the
+    committed ncu summary; None when there is none or the kernel sources
+    changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f).get(name)
     except (OSError, ValueError):
         return None
-    if not d or d.get("source_hash") != kernel_source_hash():
+    if not d or d.get("source_hash") != kernel_source_hash(kind):
         return None
     return d.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- transpose workload
+
+T_METRIC = "transpose GB/s (read + write), 1 GPU"
+T_DTYPE = {1: "u8", 2: "bf16 bits (u16)", 4: "f32 bits (u32)", 8: "u64"}
+
+
+def t_config(spec, name, world):
+    return {"workload": name, "rows": spec["rows"], "cols": spec["cols"], "elem_bytes": spec["elem_bytes"],
+            "seed": spec["seed"], "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+def oracle_transpose_rate(spec, budget_s):
+    """Times oracle.transpose on whole source rows, growing the sample until it
+    takes about the budget.  Returns (bytes/s, description, seconds)."""
+    import oracle
+    import synth
+    rows, cols, eb = spec["rows"], spec["cols"], spec["elem_bytes"]
+    n = 1
+    while True:
+        src = synth.transpose_input(n, cols, eb, seed=spec["seed"])
+        t0 = time.perf_counter()
+        oracle.transpose(src, n, cols, cols, n)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= rows:
+            break
+        n = min(rows, n * 4)
+    if dt < budget_s and n < rows:
+        n = int(min(rows, max(1, n * budget_s / max(dt, 1e-6))))
+        src = synth.transpose_input(n, cols, eb, seed=spec["seed"])
+        t0 = time.perf_counter()
+        oracle.transpose(src, n, cols, cols, n)
+        dt = time.perf_counter() - t0
+    nbytes = 2.0 * n * cols * eb
+    return nbytes / dt, f"{n} source rows x {cols} cols ({nbytes / 1e6:.1f} MB moved) in {dt:.2f} s", dt
+
+
+def run_transpose_reference(args, spec, name):
+    """The oracle's transpose, as it stands, on a bounded sample (rank 0 only)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import oracle
+    import synth
+    rows, cols, eb = spec["rows"], spec["cols"], spec["elem_bytes"]
+    rate, _, _ = oracle_transpose_rate(spec, 2.0)
+    per_step_s = min(10.0, max(0.01, 90.0 / max(1, args.steps + args.warmup)))
+    n = int(max(1, min(rows, rate * per_step_s / (2.0 * cols * eb))))
+    src = synth.transpose_input(n, cols, eb, seed=spec["seed"])
+    rates, t_all = [], None
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            t_all = time.perf_counter()
+        t0 = time.perf_counter()
+        oracle.transpose(src, n, cols, cols, n)
+        if i >= args.warmup:
+            rates.append(2.0 * n * cols * eb / (time.perf_counter() - t0))
+    wall = time.perf_counter() - t_all
+    value = statistics.median(rates) / 1e9
+    line = {
+        "impl": "reference", "metric": T_METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": T_DTYPE[eb],
+        "data": "synthetic", "config": t_config(spec, name, world),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} source rows x {cols} cols per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_transpose(args, spec, name):
+    """Out-of-place transpose of a rows x cols matrix, one ttc_transpose call per step."""
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup()
+    import synth
+    import tiled_tensor_core_02_gb300 as ttc
+    from tiled_tensor_core_02_gb300 import _build
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    ttc.load()
+    rows, cols, eb = spec["rows"], spec["cols"], spec["elem_bytes"]
+    tdt = {1: torch.uint8, 2: torch.int16, 4: torch.int32, 8: torch.int64}[eb]
+    sdt = {1: np.uint8, 2: np.int16, 4: np.int32, 8: np.int64}[eb]
+    src_np = synth.transpose_input(rows, cols, eb, seed=spec["seed"])
+    S = torch.from_numpy(src_np.view(sdt)).cuda()
+    D = torch.empty(rows * cols, dtype=tdt, device="cuda")
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+    nbytes = 2.0 * rows * cols * eb
+
+    def step(Sp=S, Dp=D):
+        st = ttc.ttc_transpose(rows, cols, Sp.data_ptr(), cols, Dp.data_ptr(), rows, eb, s)
+        if st != 0:
+            raise ttc.TTCError(st, "ttc_transpose")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = ttc.ttc_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = ttc.ttc_launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+    achieved = nbytes / (statistics.mean(kern_ms) * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "peak_source": f"{peak_src} hbm_gbs",
+                "traffic": load_traffic(name, "transpose"), "alg_bytes": nbytes,
+                "kernel_ms_mean": statistics.mean(kern_ms), "kernel_ms_median": statistics.median(kern_ms),
+                "kernel_ms_min": min(kern_ms)}
+
+    # end to end: upload the source from pinned memory, transpose, read back;
+    # copies on their own streams overlap the neighbouring steps' kernels
+    hS = torch.empty(S.numel(), dtype=tdt, pin_memory=True).copy_(S)
+    hD = [torch.empty(D.numel(), dtype=tdt, pin_memory=True) for _ in range(2)]
+    dS = [torch.empty_like(S) for _ in range(2)]
+    dD = [D, torch.empty_like(D)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_done, comp_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    used_once = [False, False]
+
+    def e2e_step(i):
+        j = i & 1
+        with torch.cuda.stream(s_in):
+            if used_once[j]:
+                s_in.wait_event(comp_done[j])
+            dS[j].copy_(hS, non_blocking=True)
+            in_done[j].record(s_in)
+        stream.wait_event(in_done[j])
+        if used_once[j]:
+            stream.wait_event(out_done[j])
+        step(dS[j], dD[j])
+        comp_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[j])
+            hD[j].copy_(dD[j], non_blocking=True)
+            out_done[j].record(s_out)
+        used_once[j] = True
+
+    e2e_steps = max(4, min(args.e2e_steps, 20))
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_event(out_done[0])
+    stream.wait_event(out_done[1])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = nbytes * e2e_steps * world / (e2e_ms * 1e-3) / 1e9
+    if not torch.equal(hD[(e2e_steps - 1) & 1], D.cpu()):
+        raise SystemExit("end-to-end result differs from the device-timed result")
+    if ttc.ttc_get_device_error(s) != 0:
+        raise SystemExit("device error")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, _ = oracle_transpose_rate(spec, args.cpu_budget)
+        cpu = {"value": rate / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": T_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": T_DTYPE[eb], "data": "synthetic",
+            "config": t_config(spec, name, world), "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": rows * cols * eb,
+                    "d2h_bytes_per_step": rows * cols * eb},
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":

@@ -111,6 +111,20 @@ ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t
                                     ttc_act act, ttc_dtype dtype, void* stream);
 
 /*
+ * Out-of-place transpose: dst (cols x rows, row-major, pitch ldd) = src
+ * (rows x cols, row-major, pitch lds)^T, for elements of elem_bytes = 1, 2,
+ * 4 or 8 bytes (bit copies).  The layout-only transpose kernel of "4.21 What
+ * is CuTe?" (gpu-glossary-zh): a tile split among a row-major (8, 32) thread
+ * grid and written back through the transposed view.  Asynchronous on
+ * `stream`; allocates nothing.  TTC_ERR_INVALID_ARG for negative sizes, an
+ * unsupported element size, NULL pointers, lds < cols, ldd < rows, pointers
+ * not aligned to the element size, or overlapping source and destination.
+ * rows == 0 or cols == 0 is a no-op.
+ */
+ttc_status ttc_transpose(int64_t rows, int64_t cols, const void* src, int64_t lds,
+                         void* dst, int64_t ldd, int elem_bytes, void* stream);
+
+/*
  * As ttc_gemm, with caller-provided device workspace.  An operand that TMA
  * cannot read (a base not 16-byte aligned, or a pitch in bytes that is not a
  * multiple of 16: the tight leading dimensions of odd-sized matrices) is first

@@ -191,3 +191,17 @@ def freivalds_vector(N, seed):
     from synth import splitmix64
     x = splitmix64(seed + 3000, 0, N)
     return np.where((x >> np.uint64(63)) == 1, -1.0, 1.0)
+
+
+# ---------------------------------------------------------------- transpose
+
+def transpose(src, rows, cols, lds, ldd):
+    """dst[j * ldd + i] = src[i * lds + j]: the definition, element by element.
+    src is a flat array of any element type; returns a flat dst of
+    cols * ldd elements (padding left zero)."""
+    dst = np.zeros(max(cols * ldd, 0), dtype=src.dtype)
+    for i in range(rows):
+        row = src[i * lds:i * lds + cols]
+        for j in range(cols):
+            dst[j * ldd + i] = row[j]
+    return dst

@@ -318,3 +318,25 @@ def make_batch(spec):
     """The problems of a batched workload: batch b drawn from seed + b."""
     n = spec.get("batch", 1)
     return [make(spec, seed=spec["seed"] + b)[0] for b in range(n)]
+
+
+# ---------------------------------------------------------------- transpose inputs
+
+ELEM_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
+
+# Out-of-place transpose workloads: rows x cols source, element size in bytes.
+# The CuTe transpose page runs its kernel on a float matrix and names no size;
+# 16384 x 16384 fp32 (1 GiB each way) is well beyond the 129 MB L2.
+TRANSPOSE_WORKLOADS = {
+    "transpose_f32_16384": dict(rows=16384, cols=16384, elem_bytes=4, seed=21),
+    "transpose_bf16_16384": dict(rows=16384, cols=16384, elem_bytes=2, seed=22),
+}
+
+
+def transpose_input(rows: int, cols: int, elem_bytes: int, seed: int, lds: int | None = None) -> np.ndarray:
+    """rows x cols source of random bit patterns, row-major with pitch lds,
+    as a flat unsigned array (padding filled with random bits too)."""
+    lds = cols if lds is None else lds
+    n = rows * lds if rows else 0
+    raw = Stream(seed).raw(n)
+    return raw.astype(ELEM_DTYPE[elem_bytes]) if elem_bytes < 8 else raw

@@ -128,3 +128,16 @@ def test_batched_validation(lib):
     # empty batch is a no-op
     assert sb(0, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 0
     assert sb(70000, 64, 64, 64, P, 64, 0, R, P, 64, 0, C, None, 64, 0, P * 2, 64, 4096, 1.0, 0.0, None, 0, BF16, None) == 2
+
+
+def test_transpose_validation(lib):
+    t = ttc.ttc_transpose
+    assert t(-1, 4, P, 4, P * 2, 4, 4, None) == 1
+    assert t(4, 4, P, 4, P * 2, 4, 3, None) == 1            # element size
+    assert t(4, 4, None, 4, P * 2, 4, 4, None) == 1         # null source
+    assert t(4, 8, P, 7, P * 2, 4, 4, None) == 1            # lds < cols
+    assert t(8, 4, P, 4, P * 2, 7, 4, None) == 1            # ldd < rows
+    assert t(4, 4, P + 2, 4, P * 2, 4, 4, None) == 1        # misaligned for 4-byte elements
+    assert t(64, 64, P, 64, P + 1024, 64, 4, None) == 1     # overlapping ranges
+    assert t(0, 64, None, 64, None, 0, 4, None) == 0        # empty is a no-op
+    assert t(64, 0, None, 0, None, 64, 2, None) == 0

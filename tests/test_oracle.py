@@ -244,3 +244,26 @@ def test_synth_layouts_hold_same_logical_matrix():
         assert np.array_equal(p.A_log, ps[0].A_log) and np.array_equal(p.B_log, ps[0].B_log)
         assert np.array_equal(synth.from_layout(p.A, 13, 11, p.layoutA, p.lda), p.A_log)
         assert np.array_equal(synth.from_layout(p.B, 11, 9, p.layoutB, p.ldb), p.B_log)
+
+
+# ---------------------------------------------------------------- transpose
+
+def test_transpose_worked_example():
+    # 2 x 3 source with pitch 4 (the 4th column is padding) -> 3 x 2 with pitch 3
+    src = np.array([1, 2, 3, 99,
+                    4, 5, 6, 99], dtype=np.uint32)
+    dst = oracle.transpose(src, 2, 3, lds=4, ldd=3)
+    assert dst.tolist() == [1, 4, 0,
+                            2, 5, 0,
+                            3, 6, 0]
+
+
+@pytest.mark.parametrize("rows,cols,eb", [(1, 1, 1), (7, 3, 2), (33, 65, 4), (64, 1, 8), (1, 70, 2)])
+def test_transpose_matches_numpy_and_is_an_involution(rows, cols, eb):
+    src = synth.transpose_input(rows, cols, eb, seed=rows * 131 + cols, lds=cols + 3)
+    dst = oracle.transpose(src, rows, cols, lds=cols + 3, ldd=rows + 1)
+    logical = src.reshape(rows, cols + 3)[:, :cols]
+    assert np.array_equal(dst.reshape(cols, rows + 1)[:, :rows], logical.T)
+    assert not dst.reshape(cols, rows + 1)[:, rows:].any()
+    back = oracle.transpose(dst, cols, rows, lds=rows + 1, ldd=cols)
+    assert np.array_equal(back.reshape(rows, cols), logical)

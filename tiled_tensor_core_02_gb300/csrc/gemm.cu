@@ -15,6 +15,7 @@
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
 #include "repack.cuh"
+#include "transpose.cuh"
 #include "ttc.h"
 #include "ttc_layout.hpp"
 
@@ -628,6 +629,26 @@ ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t
                                     const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
   return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, nullptr,
                    0, stream, batch, strideA, strideB, strideC, strideD);
+}
+
+ttc_status ttc_transpose(int64_t rows, int64_t cols, const void* src, int64_t lds, void* dst, int64_t ldd,
+                         int elem_bytes, void* stream) {
+  if (rows < 0 || cols < 0) return TTC_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8) return TTC_ERR_INVALID_ARG;
+  if (rows == 0 || cols == 0) return TTC_OK;
+  if (src == nullptr || dst == nullptr || lds < cols || ldd < rows) return TTC_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(src) % elem_bytes || reinterpret_cast<uintptr_t>(dst) % elem_bytes)
+    return TTC_ERR_INVALID_ARG;
+  if (ranges_overlap(src, ((rows - 1) * lds + cols) * elem_bytes, dst, ((cols - 1) * ldd + rows) * elem_bytes))
+    return TTC_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  ttc_status st = device_info(&dev);
+  if (st != TTC_OK) return st;
+  if (launch_transpose(src, lds, dst, ldd, rows, cols, elem_bytes, dev->sm_count, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return TTC_OK;
 }
 
 size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA,
