@@ -330,6 +330,8 @@ ELEM_DTYPE = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
 TRANSPOSE_WORKLOADS = {
     "transpose_f32_16384": dict(rows=16384, cols=16384, elem_bytes=4, seed=21),
     "transpose_bf16_16384": dict(rows=16384, cols=16384, elem_bytes=2, seed=22),
+    # the small case profiled with the full ncu section set (256 MiB each way)
+    "transpose_f32_8192": dict(rows=8192, cols=8192, elem_bytes=4, seed=23),
 }
 
 
