@@ -1,4 +1,5 @@
-"""CPU oracle for the tiled GEMM and for the layout algebra.
+"""CPU oracle for the tiled GEMM, the implicit-GEMM convolution, the transpose
+and the layout algebra.
 
 TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import this package.  The product (the CUDA
@@ -8,7 +9,9 @@ calls anything here, and nothing here imports the product.
 Contents
   * ``gemm_oracle.c`` (built into ``liboracle.so`` with gcc): the plain
     per-element GEMM definition, fp64 (fp16/bf16) / int64 (int8) accumulation,
-    fp64 epilogue.  Bound through ctypes below.
+    fp64 epilogue; and the plain per-element 2-D convolution (NHWC x KRSC,
+    stride / padding / dilation, zero taps outside the input) with the same
+    epilogue.  Bound through ctypes below.
   * ``layout.py``: the layout-algebra definitions (crd2idx, composition,
     complement, logical_divide) in plain Python.
   * the parity checker: the float tolerance, the sampling rule for large
@@ -71,6 +74,10 @@ def lib():
         L.oracle_act.argtypes = [ctypes.c_int, ctypes.c_double]
         L.oracle_act.restype = ctypes.c_double
         L.oracle_num_cpus.restype = ctypes.c_int
+        L.oracle_conv2d_elements.argtypes = [i64] * 13 + [vp, vp, vp, i64, f, f, vp, i, i, i64, vp, vp, vp, vp, i]
+        L.oracle_conv2d_elements.restype = i
+        L.oracle_conv_out_extent.argtypes = [i64] * 5
+        L.oracle_conv_out_extent.restype = i64
         _lib = L
     return _lib
 
@@ -205,3 +212,41 @@ def transpose(src, rows, cols, lds, ldd):
         for j in range(cols):
             dst[j * ldd + i] = row[j]
     return dst
+
+
+# ---------------------------------------------------------------- convolution
+
+def conv_out_extent(n, pad, dil, taps, stride):
+    return lib().oracle_conv_out_extent(n, pad, dil, taps, stride)
+
+
+def conv_elements(cp, mm, kk, alpha=1.0, beta=0.0, act="none", use_bias=True, nthreads=0):
+    """r and S_abs for output elements (mm[e], kk[e]) of synth.ConvProblem cp
+    (row m = (n P + p) Q + q, column k = output channel).  Returns (r, sabs, threads)."""
+    mm = np.ascontiguousarray(mm, dtype=np.int64)
+    kk = np.ascontiguousarray(kk, dtype=np.int64)
+    n = mm.size
+    r = np.empty(n, dtype=np.float64)
+    sabs = np.empty(n, dtype=np.float64)
+    X = np.ascontiguousarray(cp.X)
+    Wt = np.ascontiguousarray(cp.Wt)
+    C = None if (beta == 0.0 or cp.Cm is None) else np.ascontiguousarray(cp.Cm)
+    if beta != 0.0 and C is None:
+        raise ValueError("beta != 0 needs C")
+    bias = cp.bias if (use_bias and cp.bias is not None) else None
+    if bias is not None:
+        bias = np.ascontiguousarray(bias, dtype=np.float32)
+    used = lib().oracle_conv2d_elements(*cp.dims(), _ptr(X), _ptr(Wt), _ptr(C), cp.ldc, float(alpha),
+                                        float(beta), _ptr(bias), ACT[act], DTYPE[cp.dtype], n, _ptr(mm),
+                                        _ptr(kk), _ptr(r), _ptr(sabs), int(nthreads))
+    if used < 0:
+        raise ValueError("empty convolution output")
+    return r, sabs, used
+
+
+def conv_full(cp, **kw):
+    """The whole (N P Q) x K result (r, sabs) as float64 arrays."""
+    M, K = cp.M, cp.K
+    mm, kk = np.meshgrid(np.arange(M, dtype=np.int64), np.arange(K, dtype=np.int64), indexing="ij")
+    r, s, _ = conv_elements(cp, mm.ravel(), kk.ravel(), **kw)
+    return r.reshape(M, K), s.reshape(M, K)

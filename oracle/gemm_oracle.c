@@ -198,3 +198,116 @@ void oracle_matvec(int64_t rows, int64_t cols, const void* X, int64_t ld, int la
     y[i] = s;
   }
 }
+
+/*
+ * 2-D convolution, forward (cross-correlation), from its textbook definition.
+ * The PitchLinearStripminedThreadMap walkthrough (lpnh.cn/news/2469163),
+ * section 5.2, describes the implicit-GEMM view of it: one GEMM dimension is
+ * the output pixel, the other the filter tap x channel combination, and the
+ * loads follow the filter's sliding window.  The pages give no formula; this
+ * is the standard one:
+ *   P = (H + 2 ph - dh (R - 1) - 1) / sh + 1,  Q = (W + 2 pw - dw (S - 1) - 1) / sw + 1
+ *   acc[n, p, q, k] = sum over r < R, s < S, c < C of
+ *                     x[n, p sh - ph + r dh, q sw - pw + s dw, c] * w[k, r, s, c]
+ * where taps that fall outside the H x W input contribute nothing (zero
+ * padding).  x is NHWC and w is KRSC, both tightly packed.  The output is the
+ * (N P Q) x K matrix with row m = (n P + p) Q + q, and the GEMM's epilogue
+ * applies: act(alpha acc + beta C[m, k] + bias[k]) (C row-major, pitch ldc,
+ * read only when beta != 0).  fp16/bf16 inputs widen exactly to double; one
+ * sequential loop over (r, s, c) per element; S_abs = sum |x w| as for the GEMM.
+ */
+typedef struct {
+  int64_t N, H, W, C, K, R, S, P, Q;
+  int64_t ph, pw, sh, sw, dh, dw;
+  const void* X;
+  const void* Wt;
+  const void* Cm;
+  int64_t ldc;
+  float alpha, beta;
+  const float* bias;
+  int act, dtype;
+  int64_t n;
+  const int64_t* mm;
+  const int64_t* kk;
+  double* r;
+  double* sabs;
+} conv_job;
+
+typedef struct {
+  const conv_job* job;
+  int64_t lo, hi;
+} conv_slice;
+
+int64_t oracle_conv_out_extent(int64_t in, int64_t pad, int64_t dil, int64_t taps, int64_t stride) {
+  int64_t span = in + 2 * pad - dil * (taps - 1) - 1;
+  return span < 0 ? 0 : span / stride + 1;
+}
+
+static void conv_one(const conv_job* g, int64_t m, int64_t k, double* r, double* sabs) {
+  const int64_t n = m / (g->P * g->Q);
+  const int64_t p = (m / g->Q) % g->P;
+  const int64_t q = m % g->Q;
+  double s = 0.0, a_abs = 0.0;
+  for (int64_t rr = 0; rr < g->R; ++rr) {
+    const int64_t h = p * g->sh - g->ph + rr * g->dh;
+    if (h < 0 || h >= g->H) continue;
+    for (int64_t ss = 0; ss < g->S; ++ss) {
+      const int64_t w = q * g->sw - g->pw + ss * g->dw;
+      if (w < 0 || w >= g->W) continue;
+      for (int64_t c = 0; c < g->C; ++c) {
+        const double xv = load_float(g->X, g->dtype, ((n * g->H + h) * g->W + w) * g->C + c);
+        const double wv = load_float(g->Wt, g->dtype, ((k * g->R + rr) * g->S + ss) * g->C + c);
+        s += xv * wv;
+        a_abs += fabs(xv * wv);
+      }
+    }
+  }
+  double v = (double)g->alpha * s;
+  if (g->beta != 0.0f) v += (double)g->beta * load_float(g->Cm, g->dtype, m * g->ldc + k);
+  if (g->bias) v += (double)g->bias[k];
+  *r = oracle_act(g->act, v);
+  *sabs = a_abs;
+}
+
+static void* conv_run_slice(void* arg) {
+  const conv_slice* s = (const conv_slice*)arg;
+  const conv_job* g = s->job;
+  for (int64_t e = s->lo; e < s->hi; ++e) conv_one(g, g->mm[e], g->kk[e], &g->r[e], &g->sabs[e]);
+  return NULL;
+}
+
+/*
+ * r and S_abs for the n output elements (mm[e], kk[e]) of the convolution
+ * above (fp16 or bf16 only).  Returns the thread count used, or -1 when the
+ * output would be empty.
+ */
+int oracle_conv2d_elements(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                           int64_t ph, int64_t pw, int64_t sh, int64_t sw, int64_t dh, int64_t dw,
+                           const void* X, const void* Wt, const void* Cm, int64_t ldc,
+                           float alpha, float beta, const float* bias, int act, int dtype,
+                           int64_t n, const int64_t* mm, const int64_t* kk,
+                           double* r, double* sabs, int nthreads) {
+  conv_job g;
+  g.N = N; g.H = H; g.W = W; g.C = C; g.K = K; g.R = R; g.S = S;
+  g.P = oracle_conv_out_extent(H, ph, dh, R, sh);
+  g.Q = oracle_conv_out_extent(W, pw, dw, S, sw);
+  if (g.P <= 0 || g.Q <= 0) return -1;
+  g.ph = ph; g.pw = pw; g.sh = sh; g.sw = sw; g.dh = dh; g.dw = dw;
+  g.X = X; g.Wt = Wt; g.Cm = Cm; g.ldc = ldc;
+  g.alpha = alpha; g.beta = beta; g.bias = bias; g.act = act; g.dtype = dtype;
+  g.n = n; g.mm = mm; g.kk = kk; g.r = r; g.sabs = sabs;
+  if (nthreads <= 0) nthreads = oracle_num_cpus();
+  if (nthreads > 256) nthreads = 256;
+  if ((int64_t)nthreads > n) nthreads = n > 0 ? (int)n : 1;
+  pthread_t th[256];
+  conv_slice sl[256];
+  for (int t = 0; t < nthreads; ++t) {
+    sl[t].job = &g;
+    sl[t].lo = n * t / nthreads;
+    sl[t].hi = n * (t + 1) / nthreads;
+  }
+  for (int t = 1; t < nthreads; ++t) pthread_create(&th[t], NULL, conv_run_slice, &sl[t]);
+  conv_run_slice(&sl[0]);
+  for (int t = 1; t < nthreads; ++t) pthread_join(th[t], NULL);
+  return nthreads;
+}

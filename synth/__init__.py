@@ -342,3 +342,44 @@ def transpose_input(rows: int, cols: int, elem_bytes: int, seed: int, lds: int |
     n = rows * lds if rows else 0
     raw = Stream(seed).raw(n)
     return raw.astype(ELEM_DTYPE[elem_bytes]) if elem_bytes < 8 else raw
+
+
+# ---------------------------------------------------------------- convolution inputs
+
+def conv_out_extent(n, pad, dil, taps, stride):
+    """Output extent of one spatial mode (for sizing C only)."""
+    span = n + 2 * pad - dil * (taps - 1) - 1
+    return span // stride + 1 if span >= 0 else 0
+
+
+class ConvProblem:
+    """Inputs of one 2-D convolution: X (N, H, W, C) NHWC and Wt (K, R, S, C)
+    KRSC, tightly packed, stored as fp16/bf16 bit patterns; optional C
+    ((N P Q) x K row-major) and fp32 bias[K].  Draw order X, Wt, C, bias."""
+
+    def __init__(self, N, H, W, C, K, R, S, pad=(0, 0), stride=(1, 1), dil=(1, 1), dtype="bf16", seed=0,
+                 dist_x="uniform", dist_w="uniform", with_c=False, dist_bias=None):
+        self.N, self.H, self.W, self.C, self.K, self.R, self.S = N, H, W, C, K, R, S
+        self.pad, self.stride, self.dil = tuple(pad), tuple(stride), tuple(dil)
+        self.dtype = dtype
+        self.P = conv_out_extent(H, pad[0], dil[0], R, stride[0])
+        self.Q = conv_out_extent(W, pad[1], dil[1], S, stride[1])
+        self.M = N * self.P * self.Q
+        st = Stream(seed)
+        self.X = store(draw(st, N * H * W * C, dist_x), dtype)
+        self.Wt = store(draw(st, K * R * S * C, dist_w), dtype)
+        self.Cm = store(draw(st, self.M * K, "uniform"), dtype) if with_c else None
+        self.ldc = K
+        self.bias = draw(st, K, dist_bias).astype(np.float32) if dist_bias else None
+
+    def dims(self):
+        return (self.N, self.H, self.W, self.C, self.K, self.R, self.S) + self.pad + self.stride + self.dil
+
+
+# 3 x 3, stride 1, pad 1 over a 56 x 56 feature map with 256 channels in and
+# out, batch 32 (a mid-network layer of a residual image network; the pages
+# name implicit-GEMM convolution without a workload).
+CONV_WORKLOADS = {
+    "conv3x3_bf16_32x56x56x256": dict(N=32, H=56, W=56, C=256, K=256, R=3, S=3, pad=(1, 1), stride=(1, 1),
+                                      dil=(1, 1), dtype="bf16", seed=31),
+}
