@@ -44,10 +44,12 @@ def workload_spec(name):
     import synth
     if name in synth.TRANSPOSE_WORKLOADS:
         return dict(synth.TRANSPOSE_WORKLOADS[name], kind="transpose")
+    if name in synth.CONV_WORKLOADS:
+        return dict(synth.CONV_WORKLOADS[name], kind="conv")
     try:
         return synth.workload(name)
     except (KeyError, ValueError):
-        names = synth.all_workload_names() + sorted(synth.TRANSPOSE_WORKLOADS)
+        names = synth.all_workload_names() + sorted(synth.TRANSPOSE_WORKLOADS) + sorted(synth.CONV_WORKLOADS)
         raise SystemExit(f"unknown workload {name}; choose from {names}")
 
 
@@ -266,6 +268,8 @@ def main():
     if spec.get("kind") == "transpose":
         return run_transpose_reference(args, spec, name) if args.impl == "reference" else \
             run_transpose(args, spec, name)
+    if spec.get("kind") == "conv":
+        return run_conv_reference(args, spec, name) if args.impl == "reference" else run_conv(args, spec, name)
     if args.impl == "reference":
         return run_reference(args, spec, name)
 
@@ -712,6 +716,239 @@ def run_transpose(args, spec, name):
             "config": t_config(spec, name, world), "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": rows * cols * eb,
                     "d2h_bytes_per_step": rows * cols * eb},
+            "gpu_launches": launches, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+
+# ---------------------------------------------------------------- convolution workload
+
+C_METRIC = "implicit-GEMM convolution TFLOPS, 1 GPU"
+
+
+def conv_problem(spec):
+    import synth
+    kw = {k: v for k, v in spec.items() if k != "kind"}
+    return synth.ConvProblem(**kw)
+
+
+def conv_config(cp, name, world):
+    return {"workload": name, "N": cp.N, "H": cp.H, "W": cp.W, "C": cp.C, "K": cp.K, "R": cp.R, "S": cp.S,
+            "pad": list(cp.pad), "stride": list(cp.stride), "dil": list(cp.dil), "dtype": cp.dtype,
+            "gemm_view": {"M": cp.M, "N": cp.K, "K": cp.R * cp.S * cp.C},
+            "parallelism": f"replicas{world}" if world > 1 else "single",
+            "l2": "inputs larger than L2 (no flush)" if conv_bytes(cp) > 2 * 129e6 else "L2 flushed between steps"}
+
+
+def conv_bytes(cp):
+    """Bytes the convolution must move at least once: X, the filters and D."""
+    return 2 * (cp.N * cp.H * cp.W * cp.C + cp.K * cp.R * cp.S * cp.C + cp.M * cp.K)
+
+
+def conv_oracle_rate(cp, budget_s):
+    """Times oracle.conv_elements on whole output rows; returns (flop/s, description, threads)."""
+    import numpy as np
+
+    import oracle
+    kg = cp.R * cp.S * cp.C
+
+    def timed(n):
+        mm = (np.arange(n, dtype=np.int64) // cp.K) % cp.M
+        kk = np.arange(n, dtype=np.int64) % cp.K
+        t0 = time.perf_counter()
+        _, _, used = oracle.conv_elements(cp, mm, kk)
+        return time.perf_counter() - t0, used
+
+    n = min(256, cp.M * cp.K)
+    dt, used = timed(n)
+    while dt < budget_s / 4 and n < cp.M * cp.K:
+        n = min(cp.M * cp.K, n * 4)
+        dt, used = timed(n)
+    if dt < budget_s and n < cp.M * cp.K:
+        n = int(min(cp.M * cp.K, n * budget_s / max(dt, 1e-6)))
+        dt, used = timed(n)
+    return 2.0 * n * kg / dt, f"{n} output elements ({n / cp.K:.2f} pixels x {cp.K} channels, R S C = {kg}) in {dt:.2f} s", used
+
+
+def run_conv_reference(args, spec, name):
+    """The oracle's convolution, as it stands, on a fixed per-step sample (rank 0 only)."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    cp = conv_problem(spec)
+    kg = cp.R * cp.S * cp.C
+    rate, _, used = conv_oracle_rate(cp, 3.0)
+    per_step_s = min(10.0, max(0.01, 90.0 / max(1, args.steps + args.warmup)))
+    n = int(max(64, min(cp.M * cp.K, rate * per_step_s / (2.0 * kg))))
+    mm = (np.arange(n, dtype=np.int64) // cp.K) % cp.M
+    kk = np.arange(n, dtype=np.int64) % cp.K
+    rates, t_all = [], None
+    for i in range(args.warmup + args.steps):
+        if i == args.warmup:
+            t_all = time.perf_counter()
+        t0 = time.perf_counter()
+        _, _, used = oracle.conv_elements(cp, mm, kk)
+        if i >= args.warmup:
+            rates.append(2.0 * n * kg / (time.perf_counter() - t0))
+    wall = time.perf_counter() - t_all
+    value = statistics.median(rates) / 1e12
+    line = {
+        "impl": "reference", "metric": C_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wall / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": cp.dtype, "data": "synthetic",
+        "config": conv_config(cp, name, world),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": used, "kind": "oracle",
+                         "sample": f"{n} output elements per step ({n / cp.K:.2f} pixels x {cp.K} channels)"},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_conv(args, spec, name):
+    """One ttc_conv2d_fprop call per step."""
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_setup()
+    import tiled_tensor_core_02_gb300 as ttc
+    from tiled_tensor_core_02_gb300 import _build
+    if rank == 0 or not _build.up_to_date():
+        _build.build()
+    barrier(world)
+    ttc.load()
+    cp = conv_problem(spec)
+    kg = cp.R * cp.S * cp.C
+    flops = 2.0 * cp.M * cp.K * kg
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
+
+    X, Wt = dev(cp.X), dev(cp.Wt)
+    D = torch.empty(cp.M * cp.K, dtype=torch.int16, device="cuda")
+    need_flush = conv_bytes(cp) <= 2 * 129e6
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda") if need_flush else None
+    stream = torch.cuda.current_stream()
+    s = stream.cuda_stream
+
+    def step(Xp=X, Wp=Wt, Dp=D):
+        st = ttc.ttc_conv2d_fprop(*cp.dims(), Xp.data_ptr(), Wp.data_ptr(), None, cp.K, Dp.data_ptr(), cp.K,
+                                  1.0, 0.0, None, ttc.ACT["none"], ttc.DTYPE[cp.dtype], s)
+        if st != 0:
+            raise ttc.TTCError(st, "ttc_conv2d_fprop")
+
+    for _ in range(args.warmup):
+        if flush is not None:
+            flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if ttc.ttc_get_device_error(s) != 0:
+        raise SystemExit("device error during warm-up")
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = ttc.ttc_launch_count()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = ttc.ttc_launch_count() - launches0
+    barrier(world)
+    clocks = sampler.stop()
+    if ttc.ttc_get_device_error(s) != 0:
+        raise SystemExit("device error during the timed region")
+    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    total_ms = sum(kern_ms) if flush is not None else t0.elapsed_time(t1)
+    total_ms = max_over_ranks(total_ms, world)
+    value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak_key = "bf16_tflops_sustained" if total_ms >= 1000.0 else "bf16_tflops"
+    achieved = flops / (statistics.mean(kern_ms) * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peaks[peak_key], "unit": "TFLOP/s",
+                "frac": achieved / peaks[peak_key], "peak_source": f"{peak_src} {peak_key}",
+                "traffic": load_traffic(name), "alg_bytes": conv_bytes(cp), "alg_flops": flops,
+                "intensity_flop_per_byte": flops / conv_bytes(cp),
+                "kernel_ms_mean": statistics.mean(kern_ms), "kernel_ms_median": statistics.median(kern_ms),
+                "kernel_ms_min": min(kern_ms)}
+
+    # end to end: upload input and filters from pinned memory, convolve, read D back
+    hX = torch.empty(X.numel(), dtype=X.dtype, pin_memory=True).copy_(X)
+    hW = torch.empty(Wt.numel(), dtype=Wt.dtype, pin_memory=True).copy_(Wt)
+    hD = [torch.empty(D.numel(), dtype=D.dtype, pin_memory=True) for _ in range(2)]
+    dX, dW = [torch.empty_like(X) for _ in range(2)], [torch.empty_like(Wt) for _ in range(2)]
+    dD = [D, torch.empty_like(D)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_done, comp_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+    used_once = [False, False]
+
+    def e2e_step(i):
+        j = i & 1
+        with torch.cuda.stream(s_in):
+            if used_once[j]:
+                s_in.wait_event(comp_done[j])
+            dX[j].copy_(hX, non_blocking=True)
+            dW[j].copy_(hW, non_blocking=True)
+            in_done[j].record(s_in)
+        stream.wait_event(in_done[j])
+        if used_once[j]:
+            stream.wait_event(out_done[j])
+        step(dX[j], dW[j], dD[j])
+        comp_done[j].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[j])
+            hD[j].copy_(dD[j], non_blocking=True)
+            out_done[j].record(s_out)
+        used_once[j] = True
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    stream.wait_event(out_done[0])
+    stream.wait_event(out_done[1])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = flops * args.e2e_steps * world / (e2e_ms * 1e-3) / 1e12
+    if not torch.equal(hD[(args.e2e_steps - 1) & 1], D.cpu()):
+        raise SystemExit("end-to-end result differs from the device-timed result")
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, used = conv_oracle_rate(cp, args.cpu_budget)
+        cpu = {"value": rate / 1e12, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": C_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": cp.dtype, "data": "synthetic",
+            "config": conv_config(cp, name, world), "roofline": roofline, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": 2 * (X.numel() + Wt.numel()),
+                    "d2h_bytes_per_step": 2 * D.numel()},
             "gpu_launches": launches, "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -111,6 +111,36 @@ ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t
                                     ttc_act act, ttc_dtype dtype, void* stream);
 
 /*
+ * Implicit-GEMM 2-D convolution, forward: the convolution run as a GEMM whose
+ * rows are output pixels and whose reduction runs over filter tap x channel,
+ * the A operand gathered from the input on the fly and never stored (the
+ * implicit-GEMM view described in section 5.2 of the
+ * PitchLinearStripminedThreadMap walkthrough, lpnh.cn/news/2469163).  With
+ *   P = (H + 2 pad_h - dil_h (R - 1) - 1) / stride_h + 1   (Q likewise)
+ * and m = (n P + p) Q + q it computes, for every m < N P Q and k < K,
+ *   D[m ldd + k] = act(alpha acc + beta Cm[m ldc + k] + bias[k]),
+ *   acc = sum over r < R, s < S, c < C of
+ *         X[n, p stride_h - pad_h + r dil_h, q stride_w - pad_w + s dil_w, c] * Wt[k, r, s, c]
+ * (cross-correlation; taps outside the H x W input count as zero).
+ * Layouts: X is N x H x W x C (NHWC) and Wt is K x R x S x C (KRSC), both tightly
+ * packed; Cm and D are (N P Q) x K row-major with pitches ldc, ldd >= K (the
+ * NPQK output).  fp16 or bf16 in and out, fp32 accumulation; bias fp32[K] or
+ * NULL; Cm read only when beta != 0 (it may equal D with ldc == ldd).
+ * Asynchronous on `stream`; allocates nothing; the caller owns every buffer.
+ * TTC_ERR_INVALID_ARG for negative sizes, zero strides or dilations, a filter
+ * larger than the padded input, NULL or misaligned pointers, pitches below K,
+ * D overlapping X or Cm; TTC_ERR_UNSUPPORTED for int8 or extents beyond int
+ * range.  N == 0 or K == 0 is a no-op; C == 0 leaves the epilogue of a zero
+ * sum.
+ */
+ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K,
+                            int64_t R, int64_t S, int64_t pad_h, int64_t pad_w,
+                            int64_t stride_h, int64_t stride_w, int64_t dil_h, int64_t dil_w,
+                            const void* X, const void* Wt, const void* Cm, int64_t ldc,
+                            void* D, int64_t ldd, float alpha, float beta, const float* bias,
+                            ttc_act act, ttc_dtype dtype, void* stream);
+
+/*
  * Out-of-place transpose: dst (cols x rows, row-major, pitch ldd) = src
  * (rows x cols, row-major, pitch lds)^T, for elements of elem_bytes = 1, 2,
  * 4 or 8 bytes (bit copies).  The layout-only transpose kernel of "4.21 What

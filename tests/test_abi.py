@@ -141,3 +141,23 @@ def test_transpose_validation(lib):
     assert t(64, 64, P, 64, P + 1024, 64, 4, None) == 1     # overlapping ranges
     assert t(0, 64, None, 64, None, 0, 4, None) == 0        # empty is a no-op
     assert t(64, 0, None, 0, None, 64, 2, None) == 0
+
+
+def test_conv_validation(lib):
+    cv = ttc.ttc_conv2d_fprop
+    base = [2, 8, 8, 16, 32, 3, 3, 1, 1, 1, 1, 1, 1]
+    ok_args = lambda dims: dims + [P, P * 4, None, 32, P * 8, 32, 1.0, 0.0, None, 0, BF16, None]
+    a = list(base); a[7] = -1
+    assert cv(*ok_args(a)) == 1                   # negative padding
+    a = list(base); a[9] = 0
+    assert cv(*ok_args(a)) == 1                   # zero stride
+    a = list(base); a[5] = 11
+    assert cv(*ok_args(a)) == 1                   # filter larger than the padded input
+    assert cv(*(base + [P, P * 4, None, 32, P * 8, 31, 1.0, 0.0, None, 0, BF16, None])) == 1   # ldd < K
+    assert cv(*(base + [P, P * 4, None, 32, None, 32, 1.0, 0.0, None, 0, BF16, None])) == 1     # no output
+    assert cv(*(base + [P, P * 4, None, 32, P * 8, 32, 1.0, 1.0, None, 0, BF16, None])) == 1    # beta without C
+    assert cv(*(base + [P + 1, P * 4, None, 32, P * 8, 32, 1.0, 0.0, None, 0, BF16, None])) == 1  # misaligned X
+    assert cv(*(base + [P, P * 4, None, 32, P, 32, 1.0, 0.0, None, 0, BF16, None])) == 1        # D overlaps X
+    assert cv(*(base + [P, P * 4, None, 32, P * 8, 32, 1.0, 0.0, None, 0, 2, None])) == 2       # int8
+    a = list(base); a[0] = 0
+    assert cv(*ok_args(a)) == 0                   # N = 0: no-op

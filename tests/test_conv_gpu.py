@@ -1,0 +1,111 @@
+"""GPU parity of ttc_conv2d_fprop (implicit-GEMM convolution) against the
+oracle's per-element convolution, with the GEMM's float tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import tiled_tensor_core_02_gb300 as ttc
+from gpu_util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_conv(cp, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, x_offset=0, in_place=False, expect=0):
+    ldd = cp.K if ldd is None else ldd
+    X = to_dev(np.concatenate([np.zeros(x_offset, np.uint16), cp.X]))
+    Wt = to_dev(cp.Wt)
+    bias = to_dev(cp.bias) if (use_bias and cp.bias is not None) else None
+    if in_place:
+        D = to_dev(cp.Cm)
+        Cm = D
+    else:
+        D = torch.full((max(cp.M * ldd, 1),), -1, dtype=torch.int16, device="cuda")
+        Cm = to_dev(cp.Cm) if (beta != 0.0 and cp.Cm is not None) else None
+    st = ttc.ttc_conv2d_fprop(*cp.dims(), X.data_ptr() + 2 * x_offset, Wt.data_ptr(),
+                              Cm.data_ptr() if Cm is not None else None, cp.ldc if Cm is not None else cp.K,
+                              D.data_ptr(), ldd, alpha, beta, bias.data_ptr() if bias is not None else None,
+                              ttc.ACT[act], ttc.DTYPE[cp.dtype], torch.cuda.current_stream().cuda_stream)
+    assert st == expect, ttc.ttc_status_string(st)
+    torch.cuda.synchronize()
+    assert ttc.ttc_get_device_error(None) == 0
+    return D.cpu().numpy().view(np.uint16)
+
+
+def check_full(cp, out, ldd=None, **kw):
+    ldd = cp.K if ldd is None else ldd
+    r, sabs = oracle.conv_full(cp, **kw)
+    d = oracle.decode(out.reshape(-1)[:cp.M * ldd].reshape(cp.M, ldd)[:, :cp.K], cp.dtype)
+    ok, worst, w = oracle.check_float(d.ravel(), r.ravel(), sabs.ravel(), cp.dtype)
+    assert ok, f"worst error {worst:.3f} x tolerance at {np.unravel_index(w, d.shape)}"
+
+
+SHAPES = [
+    # N, H, W, C, K, R, S, pad, stride, dil
+    (2, 9, 9, 64, 96, 3, 3, (1, 1), (1, 1), (1, 1)),       # vector path, ragged K
+    (1, 14, 14, 128, 256, 3, 3, (1, 1), (2, 2), (1, 1)),   # strided
+    (2, 8, 8, 256, 64, 1, 1, (0, 0), (1, 1), (1, 1)),      # 1 x 1
+    (1, 32, 32, 3, 64, 7, 7, (3, 3), (2, 2), (1, 1)),      # first-layer shape, C = 3 (per-element path)
+    (1, 17, 13, 16, 40, 3, 3, (2, 2), (1, 1), (2, 2)),     # dilated
+    (3, 7, 11, 24, 70, 2, 3, (1, 0), (1, 2), (1, 1)),      # rectangular filter, asymmetric stride/pad
+    (1, 5, 5, 8, 8, 5, 5, (0, 0), (1, 1), (1, 1)),         # one output pixel per image
+    (4, 12, 12, 72, 136, 3, 3, (1, 1), (1, 1), (1, 1)),    # M, K and R S C all ragged vs the tiles
+]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("shape", SHAPES)
+def test_conv_matches_oracle(shape, dtype):
+    N, H, W, C, K, R, S, pad, stride, dil = shape
+    cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype=dtype, seed=sum(shape[:7]))
+    check_full(cp, run_conv(cp))
+
+
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_tanh"])
+def test_conv_epilogue(act):
+    cp = synth.ConvProblem(2, 10, 10, 32, 48, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=7, with_c=True,
+                           dist_bias="uniform")
+    check_full(cp, run_conv(cp, alpha=0.75, beta=0.5, act=act), alpha=0.75, beta=0.5, act=act)
+
+
+def test_conv_in_place_c_and_padded_output_pitch():
+    cp = synth.ConvProblem(1, 9, 9, 16, 24, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=8, with_c=True)
+    check_full(cp, run_conv(cp, beta=1.0, in_place=True, use_bias=False), beta=1.0, use_bias=False)
+    out = run_conv(cp, ldd=40).reshape(cp.M, 40)
+    check_full(cp, out.ravel(), ldd=40)
+    assert (out[:, cp.K:] == 0xFFFF).all()  # the pitch padding is not written
+
+
+def test_conv_unaligned_input_takes_the_per_element_path():
+    cp = synth.ConvProblem(2, 6, 6, 16, 32, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=9)
+    check_full(cp, run_conv(cp, x_offset=1))
+
+
+def test_conv_empty_and_degenerate():
+    cp = synth.ConvProblem(1, 4, 4, 8, 8, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=10, with_c=True,
+                           dist_bias="uniform")
+    # C = 0 channels: a zero sum, the epilogue alone
+    cp0 = synth.ConvProblem(1, 4, 4, 0, 8, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=10, with_c=True,
+                            dist_bias="uniform")
+    cp0.Cm, cp0.bias = cp.Cm, cp.bias
+    check_full(cp0, run_conv(cp0, beta=1.0), beta=1.0)
+    # N = 0 and K = 0 are no-ops
+    assert ttc.ttc_conv2d_fprop(0, 4, 4, 8, 8, 3, 3, 1, 1, 1, 1, 1, 1, None, None, None, 8, None, 8, 1.0, 0.0,
+                                None, 0, ttc.DTYPE["bf16"], None) == 0
+    assert ttc.ttc_conv2d_fprop(1, 4, 4, 8, 0, 3, 3, 1, 1, 1, 1, 1, 1, None, None, None, 1, None, 1, 1.0, 0.0,
+                                None, 0, ttc.DTYPE["bf16"], None) == 0
+
+
+@pytest.mark.parametrize("name", sorted(synth.CONV_WORKLOADS))
+def test_conv_full_size_sampled(name):
+    """The benchmark's convolution in its launch configuration: sampled rows,
+    columns and elements against the oracle."""
+    spec = dict(synth.CONV_WORKLOADS[name])
+    cp = synth.ConvProblem(**spec)
+    out = run_conv(cp).reshape(cp.M, cp.K)
+    mm, kk = oracle.sample_indices(cp.M, cp.K, seed=spec["seed"], n_lines=4, n_elems=16384)
+    r, sabs, _ = oracle.conv_elements(cp, mm, kk)
+    d = oracle.decode(out[mm, kk], cp.dtype)
+    ok, worst, w = oracle.check_float(d, r, sabs, cp.dtype)
+    assert ok, f"worst error {worst:.3f} x tolerance at (m={mm[w]}, k={kk[w]})"

@@ -33,7 +33,7 @@ KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_gene
 
 # Every symbol the C header declares (checked by the test suite).
 EXPORTS = ("ttc_gemm", "ttc_gemm_strided_batched", "ttc_gemm_ws", "ttc_gemm_workspace_size",
-           "ttc_gemm_static_scratch", "ttc_transpose",
+           "ttc_gemm_static_scratch", "ttc_transpose", "ttc_conv2d_fprop",
            "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
 
 _lib = None
@@ -63,6 +63,8 @@ def load():
     L.ttc_gemm_strided_batched.argtypes = [i64, i64, i64, i64, vp, i64, i64, i, vp, i64, i64, i, vp, i64, i64,
                                            vp, i64, i64, f, f, vp, i, i, vp]
     L.ttc_gemm_strided_batched.restype = i
+    L.ttc_conv2d_fprop.argtypes = [i64] * 13 + [vp, vp, vp, i64, vp, i64, f, f, vp, i, i, vp]
+    L.ttc_conv2d_fprop.restype = i
     L.ttc_transpose.argtypes = [i64, i64, vp, i64, vp, i64, i, vp]
     L.ttc_transpose.restype = i
     L.ttc_gemm_ws.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, vp, i64, f, f, vp, i, i, vp,
@@ -99,6 +101,12 @@ def ttc_gemm_strided_batched(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, s
     return load().ttc_gemm_strided_batched(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, strideB,
                                            layoutB, C, ldc, strideC, D, ldd, strideD, alpha, beta, bias,
                                            act, dtype, stream)
+
+
+def ttc_conv2d_fprop(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, X, Wt, Cm, ldc, D,
+                     ldd, alpha, beta, bias, act, dtype, stream) -> int:
+    return load().ttc_conv2d_fprop(N, H, W, C, K, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w, X, Wt, Cm,
+                                   ldc, D, ldd, alpha, beta, bias, act, dtype, stream)
 
 
 def ttc_transpose(rows, cols, src, lds, dst, ldd, elem_bytes, stream) -> int:

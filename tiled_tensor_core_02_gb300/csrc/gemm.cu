@@ -136,6 +136,8 @@ cudaError_t launch(int mode, int bn, const GemmParams& prm, int grid, cudaStream
     case kModeGenBF16: return launch_mode<kModeGenBF16>(bn, prm, grid, s);
     case kModeI8: return launch_mode<kModeI8>(bn, prm, grid, s);
     case kModeI8Tma: return launch_mode<kModeI8Tma>(bn, prm, grid, s);
+    case kModeConvF16: return launch_mode<kModeConvF16>(bn, prm, grid, s);
+    case kModeConvBF16: return launch_mode<kModeConvBF16>(bn, prm, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -588,7 +590,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       }
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
       prm.num_n_blocks = (int)((N + pbn - 1) / pbn);
- prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+      prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
       prm.num_tiles = (int)batch * prm.tiles_per_batch;
       const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
@@ -629,6 +631,121 @@ ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t
                                     const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
   return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, nullptr,
                    0, stream, batch, strideA, strideB, strideC, strideD);
+}
+
+ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
+                            int64_t pad_h, int64_t pad_w, int64_t stride_h, int64_t stride_w, int64_t dil_h,
+                            int64_t dil_w, const void* X, const void* Wt, const void* Cm, int64_t ldc, void* D,
+                            int64_t ldd, float alpha, float beta, const float* bias, ttc_act act, ttc_dtype dtype,
+                            void* stream) {
+  // ------------------------------------------------------------ validation
+  if (N < 0 || H < 1 || W < 1 || C < 0 || K < 0 || R < 1 || S < 1 || pad_h < 0 || pad_w < 0 || stride_h < 1 ||
+      stride_w < 1 || dil_h < 1 || dil_w < 1)
+    return TTC_ERR_INVALID_ARG;
+  if (act != TTC_ACT_NONE && act != TTC_ACT_RELU && act != TTC_ACT_GELU_TANH) return TTC_ERR_INVALID_ARG;
+  if (dtype == TTC_I8) return TTC_ERR_UNSUPPORTED;
+  if (dtype != TTC_F16 && dtype != TTC_BF16) return TTC_ERR_INVALID_ARG;
+  // every spatial quantity the kernel forms (p sh - ph + r dh, ...) must stay far inside int
+  const int64_t small = 1ll << 24;
+  if (H > small || W > small || pad_h > small || pad_w > small || stride_h > small || stride_w > small ||
+      dil_h > small || dil_w > small || R > small || S > small || dil_h * (R - 1) > small || dil_w * (S - 1) > small)
+    return TTC_ERR_UNSUPPORTED;
+  const int64_t span_h = H + 2 * pad_h - dil_h * (R - 1) - 1, span_w = W + 2 * pad_w - dil_w * (S - 1) - 1;
+  if (span_h < 0 || span_w < 0) return TTC_ERR_INVALID_ARG;  // the filter does not fit the padded input
+  const int64_t P = span_h / stride_h + 1, Q = span_w / stride_w + 1;
+  if (N == 0 || K == 0) return TTC_OK;
+  const int64_t lim = 0x7FFFFFFFll;
+  if (N > lim / (P * Q) || N > lim / (H * W) || C > lim / (R * S) || K > lim || ldd > lim || ldc > lim)
+    return TTC_ERR_UNSUPPORTED;
+  const int64_t M = N * P * Q, Kg = R * S * C;
+  if (D == nullptr || ldd < K) return TTC_ERR_INVALID_ARG;
+  if (beta != 0.0f && (Cm == nullptr || ldc < K)) return TTC_ERR_INVALID_ARG;
+  if (Kg > 0 && (X == nullptr || Wt == nullptr)) return TTC_ERR_INVALID_ARG;
+  if ((Kg > 0 && (reinterpret_cast<uintptr_t>(X) % 2 || reinterpret_cast<uintptr_t>(Wt) % 2)) ||
+      reinterpret_cast<uintptr_t>(D) % 2 || (beta != 0.0f && reinterpret_cast<uintptr_t>(Cm) % 2) ||
+      reinterpret_cast<uintptr_t>(bias) % 4)
+    return TTC_ERR_INVALID_ARG;
+  if (beta != 0.0f) {
+    const int64_t c_bytes = ((M - 1) * ldc + K) * 2, d_bytes = ((M - 1) * ldd + K) * 2;
+    const bool in_place = Cm == D && ldc == ldd;
+    if (!in_place && ranges_overlap(Cm, c_bytes, D, d_bytes)) return TTC_ERR_INVALID_ARG;
+  }
+  if (Kg > 0 && ranges_overlap(X, N * H * W * C * 2, D, ((M - 1) * ldd + K) * 2)) return TTC_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  ttc_status st = device_info(&dev);
+  if (st != TTC_OK) return st;
+
+  // ------------------------------------------------------------ plan: 128-pixel tiles, tile width by SM fill
+  const int forced_bn = g_force_tile_n.load();
+  int bn = 0;
+  double best = -1.0;
+  for (int cand = 256; cand >= 32; cand /= 2) {
+    if (forced_bn != 0 && cand != forced_bn) continue;
+    if (forced_bn == 0 && cand > 32 && cand / 2 >= K) continue;
+    const int64_t tiles = ((M + kBM - 1) / kBM) * ((K + cand - 1) / cand);
+    const double rate = cand == 256 ? 1.0 : cand == 128 ? 0.7 : cand == 64 ? 0.45 : 0.3;
+    const double score = (double)(tiles < dev->sm_count ? tiles : dev->sm_count) * rate;
+    if (score > best + 1e-9) {
+      best = score;
+      bn = cand;
+    }
+  }
+  if (bn == 0) return TTC_ERR_UNSUPPORTED;
+  const int mode = dtype == TTC_BF16 ? kModeConvBF16 : kModeConvF16;
+  const bool store_tma = tma_ok(D, ldd, 2) && !g_force_generic_store.load();
+
+  GemmParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (store_tma && !encode_3d(&prm.tmD, dt, 2, D, K, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+    return TTC_ERR_CUDA;
+  prm.A = X;
+  prm.lda = Kg;
+  prm.B = Wt;  // B(kk, k) = Wt[k Kg + kk]: the K-major ("column-major") B operand
+  prm.ldb = Kg > 0 ? Kg : 1;
+  prm.a_vec = C % 8 == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0;
+  prm.b_vec = reinterpret_cast<uintptr_t>(Wt) % 16 == 0 && (Kg * 2) % 16 == 0;
+  prm.M = (int)M;
+  prm.N = (int)K;
+  prm.K = (int)Kg;
+  prm.num_m_blocks = (int)((M + kBM - 1) / kBM);
+  prm.num_n_blocks = (int)((K + bn - 1) / bn);
+  prm.num_k_blocks = (int)((Kg + kBK - 1) / kBK);
+  prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+  prm.num_tiles = prm.tiles_per_batch;
+  prm.batch = 1;
+  const int gm = g_group_m.load() > 0 ? g_group_m.load() : 16;
+  prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
+  prm.ksplit = 1;
+  prm.kb_split = prm.num_k_blocks;
+  prm.alpha = alpha;
+  prm.beta = beta;
+  prm.C = beta != 0.0f ? Cm : nullptr;
+  prm.ldc = ldc;
+  prm.D = D;
+  prm.ldd = ldd;
+  prm.bias = bias;
+  prm.act = (int)act;
+  prm.d_tma = store_tma ? 1 : 0;
+  prm.err = dev->err;
+  prm.timeout_ns = (uint64_t)g_timeout_ns.load();
+  prm.inject_stall = g_inject_stall.load();
+  prm.cv_h = (int)H;
+  prm.cv_w = (int)W;
+  prm.cv_c = (int)(C > 0 ? C : 1);
+  prm.cv_p = (int)P;
+  prm.cv_q = (int)Q;
+  prm.cv_s = (int)S;
+  prm.cv_ph = (int)pad_h;
+  prm.cv_pw = (int)pad_w;
+  prm.cv_sh = (int)stride_h;
+  prm.cv_sw = (int)stride_w;
+  prm.cv_dh = (int)dil_h;
+  prm.cv_dw = (int)dil_w;
+  const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
+  if (launch(mode, bn, prm, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return TTC_OK;
 }
 
 ttc_status ttc_transpose(int64_t rows, int64_t cols, const void* src, int64_t lds, void* dst, int64_t ldd,

@@ -54,12 +54,16 @@ enum Mode : int {
   kModeGenBF16 = 3,  // plain loads, bf16
   kModeI8 = 4,       // plain loads of int8, converted to fp16; int32 out
   kModeI8Tma = 5,    // TMA loads of int8 into a staging ring, converter warps widen to fp16; int32 out
+  kModeConvF16 = 6,  // implicit-GEMM convolution: A gathered from the NHWC input (plain loads), fp16
+  kModeConvBF16 = 7, // the same, bf16
 };
 
 template <int MODE>
 struct ModeTraits {
   static constexpr bool kTmaLoad = MODE == kModeTmaF16 || MODE == kModeTmaBF16;
-  static constexpr bool kBF16 = MODE == kModeTmaBF16 || MODE == kModeGenBF16;  // tensor-core input type
+  static constexpr bool kBF16 =
+      MODE == kModeTmaBF16 || MODE == kModeGenBF16 || MODE == kModeConvBF16;  // tensor-core input type
+  static constexpr bool kConv = MODE == kModeConvF16 || MODE == kModeConvBF16;
   static constexpr bool kStaged = MODE == kModeI8Tma;  // TMA int8 staging + converter warps
   static constexpr bool kI8 = MODE == kModeI8 || MODE == kModeI8Tma;
   // producer warps: 1 TMA thread; 4 plain-load warps; or 1 TMA warp + 4 converter warps
@@ -107,6 +111,13 @@ struct GemmParams {
   uint32_t* err;
   uint64_t timeout_ns;
   int inject_stall;
+  // implicit-GEMM convolution (kModeConv*): A is not a matrix in memory but
+  // the im2col view of the NHWC input at A.  Row m is output pixel (n, p, q),
+  // m = (n P + p) Q + q; column kk is filter tap (r, s) and channel c,
+  // kk = (r S + s) C + c.  a_vec: C is a multiple of 8 and the input is 16-byte
+  // aligned, so each 8-column group is one 16-byte load.
+  int cv_h, cv_w, cv_c, cv_p, cv_q, cv_s;
+  int cv_ph, cv_pw, cv_sh, cv_sw, cv_dh, cv_dw;
 };
 
 template <int BN, int MODE>
@@ -253,6 +264,97 @@ __device__ __forceinline__ void generic_load_tile(uint8_t* sdst, const void* gsr
       const int r = map.row(tid, i0 + b);
       const uint32_t off = swz((uint32_t)((c / 64) * ROWS * 128 + r * 128 + (c % 64) * 2));
       *reinterpret_cast<uint4*>(sdst + off) = w[b];
+    }
+  }
+}
+
+// ------------------------------------------------------------------ implicit-GEMM convolution
+// One im2col row as the producer threads need it across a tile's k-blocks.
+struct ConvRow {
+  int pix;  // n H W: index of the first pixel of the row's image
+  int h0;   // p sh - ph; a large negative value for rows past M (always outside)
+  int w0;   // q sw - pw
+};
+
+__device__ __forceinline__ ConvRow conv_row(const GemmParams& p, int m) {
+  ConvRow cr;
+  if (m >= p.M) {
+    cr.pix = 0;
+    cr.h0 = -(1 << 29);
+    cr.w0 = 0;
+    return cr;
+  }
+  const int pq = p.cv_p * p.cv_q;
+  const int n = m / pq;
+  const int rem = m - n * pq;
+  const int pp = rem / p.cv_q;
+  const int qq = rem - pp * p.cv_q;
+  cr.pix = n * p.cv_h * p.cv_w;
+  cr.h0 = pp * p.cv_sh - p.cv_ph;
+  cr.w0 = qq * p.cv_sw - p.cv_pw;
+  return cr;
+}
+
+// The A tile of k-block k0 (kBM rows x kBK columns of the im2col matrix),
+// written with the placement generic_load_tile<kBM, kBK> uses.  Element
+// (m, kk) is x[n, h0 + r dh, w0 + s dw, c], zero where the tap is outside the
+// input or kk >= K.  rows[i] describes map row i of this thread.
+template <int ITERS>
+__device__ __forceinline__ void im2col_load_tile(uint8_t* sdst, const GemmParams& p, const ConvRow (&rows)[ITERS],
+                                                 int k0, int tid) {
+  constexpr layout::StripMined map{kBM, kBK, 128, 8};
+  static_assert(map.iterations() == ITERS, "one ConvRow per map row");
+  constexpr layout::SwizzleBytes128 swz{};
+  const uint16_t* X = static_cast<const uint16_t*>(p.A);
+  const int col = map.col(tid);
+  const int kk = k0 + col;
+  const unsigned H = (unsigned)p.cv_h, W = (unsigned)p.cv_w;
+  const int C = p.cv_c;
+  if (p.a_vec) {
+    // the group's 8 columns are channels c .. c + 7 of one tap
+    const bool k_ok = kk < p.K;
+    const int rs = kk / C;
+    const int c = kk - rs * C;
+    const int rr = rs / p.cv_s;
+    const int ss = rs - rr * p.cv_s;
+    const int dh = rr * p.cv_dh, dw = ss * p.cv_dw;
+#pragma unroll
+    for (int i = 0; i < ITERS; ++i) {
+      const int h = rows[i].h0 + dh, w = rows[i].w0 + dw;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (k_ok && (unsigned)h < H && (unsigned)w < W)
+        v = __ldg(reinterpret_cast<const uint4*>(X + ((int64_t)rows[i].pix + (int64_t)h * p.cv_w + w) * C + c));
+      const int r = map.row(tid, i);
+      *reinterpret_cast<uint4*>(sdst + swz((uint32_t)(r * 128 + col * 2))) = v;
+    }
+  } else {
+    // every column decomposed on its own (C not a multiple of 8, or unaligned input)
+    int dh[8], dw[8], cc[8];
+    bool ok[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int k = kk + j;
+      ok[j] = k < p.K;
+      const int rs = k / C;
+      cc[j] = k - rs * C;
+      const int rr = rs / p.cv_s;
+      dh[j] = rr * p.cv_dh;
+      dw[j] = (rs - rr * p.cv_s) * p.cv_dw;
+    }
+#pragma unroll
+    for (int i = 0; i < ITERS; ++i) {
+      uint16_t e[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int h = rows[i].h0 + dh[j], w = rows[i].w0 + dw[j];
+        e[j] = (ok[j] && (unsigned)h < H && (unsigned)w < W)
+                   ? __ldg(X + ((int64_t)rows[i].pix + (int64_t)h * p.cv_w + w) * C + cc[j])
+                   : (uint16_t)0;
+      }
+      const int r = map.row(tid, i);
+      *reinterpret_cast<uint4*>(sdst + swz((uint32_t)(r * 128 + col * 2))) =
+          make_uint4(e[0] | ((uint32_t)e[1] << 16), e[2] | ((uint32_t)e[3] << 16), e[4] | ((uint32_t)e[5] << 16),
+                     e[6] | ((uint32_t)e[7] << 16));
     }
   }
 }
@@ -754,6 +856,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         constexpr int kInBytes = kI8 ? 1 : 2;
         const void* Ab = static_cast<const char*>(p.A) + (int64_t)bz * p.a_bs * kInBytes;
         const void* Bb = static_cast<const char*>(p.B) + (int64_t)bz * p.b_bs * kInBytes;
+        constexpr int kConvIters = layout::StripMined{kBM, kBK, 128, 8}.iterations();
+        ConvRow crow[Tr::kConv ? kConvIters : 1];
+        if constexpr (Tr::kConv) {
+          constexpr layout::StripMined cmap{kBM, kBK, 128, 8};
+#pragma unroll
+          for (int i = 0; i < kConvIters; ++i) crow[i] = conv_row(p, m0 + cmap.row(tid, i));
+        }
         bool ok = true;
         for (int kb = k_lo; kb < k_hi; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
@@ -763,7 +872,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           uint8_t* a = sA + stage * kABytes;
           uint8_t* b = sB + stage * Cfg::kBBytes;
           const int k0 = kb * kBK;
-          if (!p.a_mn)
+          if constexpr (Tr::kConv)
+            im2col_load_tile<kConvIters>(a, p, crow, k0, tid);
+          else if (!p.a_mn)
             generic_load_tile<kBM, kBK, kI8>(a, Ab, p.lda, m0, k0, p.M, p.K, p.a_vec, tid);
           else
             generic_load_tile<kBK, kBM, kI8>(a, Ab, p.lda, k0, m0, p.K, p.M, p.a_vec, tid);
