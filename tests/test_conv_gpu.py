@@ -109,3 +109,36 @@ def test_conv_full_size_sampled(name):
     d = oracle.decode(out[mm, kk], cp.dtype)
     ok, worst, w = oracle.check_float(d, r, sabs, cp.dtype)
     assert ok, f"worst error {worst:.3f} x tolerance at (m={mm[w]}, k={kk[w]})"
+
+
+# Shapes the im2col-TMA CTA-pair path takes (C a multiple of 64): forced onto
+# it (pair = 1) and onto the plain-load kernel (pair = 2), both against the oracle.
+PAIR_SHAPES = [
+    (2, 20, 20, 64, 128, 3, 3, (1, 1), (1, 1), (1, 1)),    # 800 pixels: ragged against 256-pixel tiles
+    (3, 30, 28, 128, 256, 3, 3, (1, 1), (2, 2), (1, 1)),   # strided; tiles cross image boundaries
+    (2, 17, 19, 64, 192, 5, 5, (2, 2), (1, 1), (2, 2)),    # dilated 5 x 5
+    (3, 9, 31, 128, 320, 1, 3, (0, 1), (1, 2), (1, 1)),    # rectangular filter, ragged K
+    (2, 7, 7, 256, 256, 3, 3, (0, 0), (1, 1), (1, 1)),     # no padding, 50 pixels: the odd CTA's rows all past M
+    (4, 16, 16, 64, 128, 1, 1, (0, 0), (2, 2), (1, 1)),    # 1 x 1, stride 2
+]
+
+
+@pytest.fixture
+def pair_knob():
+    yield lambda v: ttc.ttc_set_knob("pair", v)
+    ttc.ttc_set_knob("pair", 0)
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("shape", PAIR_SHAPES)
+def test_conv_im2col_pair_path_matches_oracle(shape, pair, pair_knob):
+    N, H, W, C, K, R, S, pad, stride, dil = shape
+    cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype="bf16", seed=sum(shape[:7]) + 100,
+                           with_c=True, dist_bias="uniform")
+    pair_knob(pair)
+    check_full(cp, run_conv(cp, alpha=1.25, beta=0.5, act="relu"), alpha=1.25, beta=0.5, act="relu")
+
+
+def test_conv_im2col_pair_path_f16():
+    cp = synth.ConvProblem(2, 12, 12, 128, 256, 3, 3, (1, 1), (1, 1), (1, 1), dtype="f16", seed=77)
+    check_full(cp, run_conv(cp))

@@ -115,6 +115,82 @@ bool tma_batch_ok(int64_t batch, int64_t stride, int esize) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// CTA-pair tile width for an M x N problem (times batch): the width whose
+// tiles fill the resident pairs best, weighted by the width's measured
+// relative rate (a narrower tile stages more A per column: 1, 0.87, 0.64 for
+// 256, 192, 128 on bf16 8192^3) and by the share of its last column of tiles
+// that lies inside N.  192 needs a K-major B (its half, 96 columns, is not a
+// whole number of 64-column MN-major slabs).  bn == 0: no width fits.
+struct PairChoice {
+  int bn = 0;
+  int clusters = 0;
+};
+PairChoice choose_pair(DeviceInfo* dev, bool bf16, int64_t M, int64_t N, int64_t batch, bool b_mn) {
+  const int forced_pbn = g_pair_tile_n.load();
+  PairChoice pc;
+  double best = -1.0;
+  const int widths[3] = {256, 192, 128};
+  for (int wi = 0; wi < 3; ++wi) {
+    const int w = widths[wi];
+    if ((forced_pbn != 0 && w != forced_pbn) || (b_mn && w == 192)) continue;
+    int& cl = dev->pair_clusters[bf16 ? 1 : 0][wi];
+    if (cl < 0) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      if (cl < 0) cl = pair_max_clusters(bf16, w);
+    }
+    if (cl <= 0) continue;
+    const int64_t nb = (N + w - 1) / w;
+    const int64_t tiles = batch * ((M + kPairBM - 1) / kPairBM) * nb;
+    const int64_t waves = (tiles + cl - 1) / cl;
+    const double fill = (double)tiles / (double)(waves * cl);
+    const double inside = (double)N / (double)(nb * w);
+    const double rate = w == 256 ? 1.0 : w == 192 ? 0.87 : 0.64;
+    const double score = fill * inside * rate;
+    if (score > best + 1e-9) {
+      best = score;
+      pc.bn = w;
+      pc.clusters = cl;
+    }
+  }
+  return pc;
+}
+
+using EncodeIm2colFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeIm2colFn g_encode_im2col = nullptr;
+
+// im2col map over an N x H x W x C tensor (16-bit elements, tightly packed):
+// boxes of 128 output pixels x 64 channels, 128-byte swizzle.  The bounding
+// box of window corners runs from -pad to pad - (taps - 1) dil past the last
+// input row/column in each spatial mode, so it holds exactly P x Q corners,
+// visited with the convolution's stride.
+bool encode_im2col(CUtensorMap* m, CUtensorMapDataType dt, const void* X, int64_t N, int64_t H, int64_t W,
+                   int64_t C, int64_t R, int64_t S, int64_t ph, int64_t pw, int64_t sh, int64_t sw, int64_t dh,
+                   int64_t dw) {
+  if (g_encode_im2col == nullptr) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_encode_im2col == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      g_encode_im2col = reinterpret_cast<EncodeIm2colFn>(fn);
+    }
+  }
+  cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2), (cuuint64_t)(H * W * C * 2)};
+  int lower[2] = {(int)-pw, (int)-ph};
+  int upper[2] = {(int)(pw - (S - 1) * dw), (int)(ph - (R - 1) * dh)};
+  cuuint32_t estr[4] = {1, (cuuint32_t)sw, (cuuint32_t)sh, 1};
+  return g_encode_im2col(m, dt, 4, const_cast<void*>(X), dims, strides, lower, upper, kBK, 128, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
@@ -548,37 +624,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   const bool pair_ok = (mode == kModeTmaF16 || mode == kModeTmaBF16) && forced_bn == 0 && !swap && ksplit == 1;
   if (pair_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && N >= 256))) {
     const bool bf16 = dtype == TTC_BF16;
-    // Pair tile width: the one whose tiles fill the resident pairs best,
-    // weighted by the width's measured relative rate (a narrower tile stages
-    // more A per column: 1, 0.87, 0.64 for 256, 192, 128 on bf16 8192^3) and by the share of its last
-    // column of tiles that lies inside N.  192 needs a K-major B (its half,
-    // 96 columns, is not a whole number of 64-column MN-major slabs).
-    const int forced_pbn = g_pair_tile_n.load();
-    int pbn = 0, clusters = 0;
-    double best = -1.0;
-    const int widths[3] = {256, 192, 128};
-    for (int wi = 0; wi < 3; ++wi) {
-      const int w = widths[wi];
-      if ((forced_pbn != 0 && w != forced_pbn) || (b_mn && w == 192)) continue;
-      int& cl = dev->pair_clusters[bf16 ? 1 : 0][wi];
-      if (cl < 0) {
-        std::lock_guard<std::mutex> lk(g_mu);
-        if (cl < 0) cl = pair_max_clusters(bf16, w);
-      }
-      if (cl <= 0) continue;
-      const int64_t nb = (N + w - 1) / w;
-      const int64_t tiles = batch * ((M + kPairBM - 1) / kPairBM) * nb;
-      const int64_t waves = (tiles + cl - 1) / cl;
-      const double fill = (double)tiles / (double)(waves * cl);
-      const double inside = (double)N / (double)(nb * w);
-      const double rate = w == 256 ? 1.0 : w == 192 ? 0.87 : 0.64;
-      const double score = fill * inside * rate;
-      if (score > best + 1e-9) {
-        best = score;
-        pbn = w;
-        clusters = cl;
-      }
-    }
+    const PairChoice pc = choose_pair(dev, bf16, M, N, batch, b_mn);
+    const int pbn = pc.bn, clusters = pc.clusters;
     const int64_t pair_tiles = pbn ? batch * ((M + kPairBM - 1) / kPairBM) * ((N + pbn - 1) / pbn) : 0;
     if (pbn != 0 && (pair_mode == 1 || pair_tiles * 4 >= dev->sm_count)) {
       if (K > 0) {
@@ -742,6 +789,39 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
   prm.cv_sw = (int)stride_w;
   prm.cv_dh = (int)dil_h;
   prm.cv_dw = (int)dil_w;
+
+  // CTA-pair kernel with im2col TMA loads: whole 64-channel blocks per filter
+  // tap, window corners and tap offsets inside the ranges an im2col map of two
+  // spatial modes accepts ([-128, 127] and [0, 255]), strides up to 8, and at
+  // least one 256-pixel pair tile
+  const int pair_mode = g_pair_mode.load();
+  const bool im2col_ok = C > 0 && C % kBK == 0 && reinterpret_cast<uintptr_t>(X) % 16 == 0 && tma_ok(Wt, Kg, 2) &&
+                         pad_h <= 127 && pad_w <= 127 && pad_h - (R - 1) * dil_h >= -128 &&
+                         pad_w - (S - 1) * dil_w >= -128 && (R - 1) * dil_h <= 255 && (S - 1) * dil_w <= 255 &&
+                         stride_h <= 8 && stride_w <= 8 && !g_force_generic_load.load() && forced_bn == 0;
+  if (im2col_ok && pair_mode != 2 && (pair_mode == 1 || (M >= kPairBM && K >= 128))) {
+    const bool bf16 = dtype == TTC_BF16;
+    const PairChoice pc = choose_pair(dev, bf16, M, K, 1, false);
+    if (pc.bn != 0) {
+      if (!encode_im2col(&prm.tmA, dt, X, N, H, W, C, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w) ||
+          !encode_3d(&prm.tmB, dt, 2, Wt, Kg, K, Kg, kBK, pc.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+        return TTC_ERR_CUDA;
+      prm.cv_tma = 1;
+      prm.cv_cblk = (int)(C / kBK);
+      prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
+      prm.num_n_blocks = (int)((K + pc.bn - 1) / pc.bn);
+      prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+      prm.num_tiles = prm.tiles_per_batch;
+      const int gmp = g_group_m.load() > 0 ? g_group_m.load() : 8;
+      prm.group_m = prm.num_m_blocks < gmp ? prm.num_m_blocks : gmp;
+      const int nclus = prm.num_tiles < pc.clusters ? prm.num_tiles : pc.clusters;
+      if (launch_pair(bf16, pc.bn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTC_ERR_CUDA;
+      g_launches.fetch_add(1);
+      return TTC_OK;
+    }
+  }
+
   const int grid = prm.num_tiles < dev->sm_count ? prm.num_tiles : dev->sm_count;
   if (launch(mode, bn, prm, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
   g_launches.fetch_add(1);

@@ -122,6 +122,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int za = bz * p.a_bc, zb = bz * p.b_bc;
         const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
         const int n0 = nb * kPairBN + (int)rank * PairCfg::kBHalf;  // this CTA's B columns
+        // convolution: window corner of output pixel m0 (rows past the end start
+        // beyond the last image, where the im2col box reads zeros)
+        int cv_n = 0, cv_h0 = 0, cv_w0 = 0;
+        if (p.cv_tma) {
+          const int pq = p.cv_p * p.cv_q;
+          cv_n = m0 / pq;
+          const int rem = m0 - cv_n * pq;
+          const int pp = rem / p.cv_q;
+          cv_h0 = pp * p.cv_sh - p.cv_ph;
+          cv_w0 = (rem - pp * p.cv_q) * p.cv_sw - p.cv_pw;
+        }
         for (int kb = 0; kb < p.num_k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
@@ -136,7 +147,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           uint8_t* a = sA + stage * PairCfg::kAHalfBytes;
           uint8_t* b = sB + stage * PairCfg::kBHalfBytes;
           const int k0 = kb * kBK;
-          if (!p.a_mn) {
+          if (p.cv_tma) {
+            const int tap = kb / p.cv_cblk;
+            const int c0 = (kb - tap * p.cv_cblk) * kBK;
+            const int rr = tap / p.cv_s;
+            const int ss = tap - rr * p.cv_s;
+            tma_load_im2col_4d_pair(a, &p.tmA, c0, cv_w0, cv_h0, cv_n, (uint16_t)(ss * p.cv_dw),
+                                    (uint16_t)(rr * p.cv_dh), full_leader, pol);
+          } else if (!p.a_mn) {
             tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol);
           } else {
             tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol);

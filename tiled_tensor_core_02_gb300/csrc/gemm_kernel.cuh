@@ -118,6 +118,11 @@ struct GemmParams {
   // aligned, so each 8-column group is one 16-byte load.
   int cv_h, cv_w, cv_c, cv_p, cv_q, cv_s;
   int cv_ph, cv_pw, cv_sh, cv_sw, cv_dh, cv_dw;
+  // CTA-pair kernel, convolution by im2col TMA (tmA is an im2col map over the
+  // NHWC input, 128 pixels x 64 channels per box): k-block kb is filter tap
+  // kb / cv_cblk, channels 64 (kb mod cv_cblk) onwards (C = 64 cv_cblk)
+  int cv_tma;
+  int cv_cblk;
 };
 
 template <int BN, int MODE>

@@ -321,6 +321,23 @@ __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// im2col TMA load for a CTA pair (completion on the leader's barrier): the
+// map fixes the box, `pixels` consecutive output pixels x `channels`
+// channels of an NHWC tensor.  (c, w, h, n) is the first pixel's window
+// corner, (off_w, off_h) the filter tap's offset inside the window; pixels
+// advance along W, then H, then N inside the map's bounding box, and taps
+// outside the tensor read zeros.
+__device__ __forceinline__ void tma_load_im2col_4d_pair(void* dst, const CUtensorMap* m, int32_t c, int32_t w,
+                                                        int32_t h, int32_t n, uint16_t off_w, uint16_t off_h,
+                                                        uint32_t bar_cluster, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar_cluster), "h"(off_w),
+      "h"(off_h), "l"(cache_hint)
+      : "memory");
+}
+
 // TMEM allocation shared by a CTA pair: one warp of each CTA executes these.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
