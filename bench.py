@@ -69,6 +69,26 @@ def single_problem_bytes(spec):
     return b
 
 
+L2_BYTES = 129e6
+
+
+def rotation_copies(nbytes):
+    """Input copies the timed loop cycles through: 1 when one step's data is
+    already beyond twice the L2, else enough copies to cycle ~3x the L2, so
+    every step starts with its inputs evicted and no foreign kernel (an L2
+    flush) runs between the timed launches."""
+    if nbytes > 2 * L2_BYTES:
+        return 1
+    return int(-(-3 * L2_BYTES // nbytes))
+
+
+def l2_note(nbytes):
+    n = rotation_copies(nbytes)
+    if n == 1:
+        return "inputs larger than L2 (no flush)"
+    return f"inputs rotated over {n} copies ({n * nbytes / 1e6:.0f} MB, > 2x L2), no flush"
+
+
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
 
@@ -242,8 +262,7 @@ def config_of(spec, name, world):
             "layoutA": spec["layoutA"], "layoutB": spec["layoutB"], "alpha": spec["alpha"],
             "beta": spec["beta"], "act": spec["act"], "bias": bool(spec.get("dist_bias")),
             "seed": spec["seed"], "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": "inputs larger than L2 (no flush)" if algorithmic_bytes(spec) > 2 * 129e6
-            else "L2 flushed between steps"}
+            "l2": l2_note(algorithmic_bytes(spec))}
 
 
 def main():
@@ -301,16 +320,19 @@ def main():
     if nbatch > 1:
         # batches packed back to back (strides = one matrix each)
         probs = synth.make_batch(spec)
-        A = dev(np.concatenate([q.A for q in probs]))
-        B = dev(np.concatenate([q.B for q in probs]))
-        C = dev(np.concatenate([q.C for q in probs])) if p.C is not None else None
+        hA = np.concatenate([q.A for q in probs])
+        hB = np.concatenate([q.B for q in probs])
+        hC = np.concatenate([q.C for q in probs]) if p.C is not None else None
     else:
-        A, B = dev(p.A), dev(p.B)
-        C = dev(p.C) if p.C is not None else None
+        hA, hB, hC = p.A, p.B, p.C
+    ncopy = rotation_copies(algorithmic_bytes(spec))
+    copies = []
+    for _ in range(ncopy):
+        copies.append((dev(hA), dev(hB), dev(hC) if hC is not None else None,
+                       torch.empty(nbatch * M * N, dtype=torch.int32 if p.dtype == "i8" else torch.int16,
+                                   device="cuda")))
+    A, B, C, D = copies[0]
     bias = dev(p.bias) if p.bias is not None else None
-    D = torch.empty(nbatch * M * N, dtype=torch.int32 if p.dtype == "i8" else torch.int16, device="cuda")
-    need_flush = algorithmic_bytes(spec) <= 2 * 129e6
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda") if need_flush else None
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
     lay = {"row": ttc.ROW_MAJOR, "col": ttc.COL_MAJOR}
@@ -340,10 +362,8 @@ def main():
         if st != 0:
             raise ttc.TTCError(st)
 
-    for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
-        step()
+    for i in range(args.warmup):
+        step(*copies[i % ncopy])
     torch.cuda.synchronize()
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during warm-up")
@@ -360,10 +380,8 @@ def main():
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
         starts[i].record(stream)
-        step()
+        step(*copies[(args.warmup + i) % ncopy])
         ends[i].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
@@ -373,10 +391,7 @@ def main():
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during the timed region")
     kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = t_start.elapsed_time(t_end)
-    if flush is not None:
-        total_ms = sum(kern_ms)  # the L2 flush between steps is not part of a step
-    total_ms = max_over_ranks(total_ms, world)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     avg_kernel_s = statistics.mean(kern_ms) * 1e-3
 
@@ -482,6 +497,7 @@ def main():
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches,
             "workspace_bytes": ws_bytes,
+            "input_copies": ncopy,
             "clocks": clocks,
             "frac_of_peak": value / peak,
         }
@@ -742,7 +758,7 @@ def conv_config(cp, name, world):
             "pad": list(cp.pad), "stride": list(cp.stride), "dil": list(cp.dil), "dtype": cp.dtype,
             "gemm_view": {"M": cp.M, "N": cp.K, "K": cp.R * cp.S * cp.C},
             "parallelism": f"replicas{world}" if world > 1 else "single",
-            "l2": "inputs larger than L2 (no flush)" if conv_bytes(cp) > 2 * 129e6 else "L2 flushed between steps"}
+            "l2": l2_note(conv_bytes(cp))}
 
 
 def conv_bytes(cp):
@@ -833,10 +849,10 @@ def run_conv(args, spec, name):
     def dev(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda()
 
-    X, Wt = dev(cp.X), dev(cp.Wt)
-    D = torch.empty(cp.M * cp.K, dtype=torch.int16, device="cuda")
-    need_flush = conv_bytes(cp) <= 2 * 129e6
-    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.int32, device="cuda") if need_flush else None
+    ncopy = rotation_copies(conv_bytes(cp))
+    copies = [(dev(cp.X), dev(cp.Wt), torch.empty(cp.M * cp.K, dtype=torch.int16, device="cuda"))
+              for _ in range(ncopy)]
+    X, Wt, D = copies[0]
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
 
@@ -846,10 +862,8 @@ def run_conv(args, spec, name):
         if st != 0:
             raise ttc.TTCError(st, "ttc_conv2d_fprop")
 
-    for _ in range(args.warmup):
-        if flush is not None:
-            flush.zero_()
-        step()
+    for i in range(args.warmup):
+        step(*copies[i % ncopy])
     torch.cuda.synchronize()
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during warm-up")
@@ -864,10 +878,8 @@ def run_conv(args, spec, name):
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record(stream)
     for i in range(args.steps):
-        if flush is not None:
-            flush.zero_()
         starts[i].record(stream)
-        step()
+        step(*copies[(args.warmup + i) % ncopy])
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -877,8 +889,7 @@ def run_conv(args, spec, name):
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during the timed region")
     kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = sum(kern_ms) if flush is not None else t0.elapsed_time(t1)
-    total_ms = max_over_ranks(total_ms, world)
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak_key = "bf16_tflops_sustained" if total_ms >= 1000.0 else "bf16_tflops"
@@ -949,7 +960,7 @@ def run_conv(args, spec, name):
             "config": conv_config(cp, name, world), "roofline": roofline, "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": 2 * (X.numel() + Wt.numel()),
                     "d2h_bytes_per_step": 2 * D.numel()},
-            "gpu_launches": launches, "clocks": clocks,
+            "gpu_launches": launches, "clocks": clocks, "input_copies": ncopy,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
