@@ -642,12 +642,16 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
       const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
+      prm.a_stream = prm.num_n_blocks == 1;
+      prm.b_stream = prm.num_m_blocks == 1;
       if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       return TTC_OK;
     }
   }
 
+  prm.a_stream = prm.num_n_blocks == 1;
+  prm.b_stream = prm.num_m_blocks == 1;
   const int max_clusters = dev->sm_count / ksplit > 0 ? dev->sm_count / ksplit : 1;
   const int clusters = prm.num_tiles < max_clusters ? prm.num_tiles : max_clusters;
   if (launch(mode, bn, prm, clusters * ksplit, static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -111,7 +111,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)
     if (lane == 0) {
-      const uint64_t pol = policy_evict_last();
+      // operands re-read by other tiles stay in L2; one read once goes first
+      const uint64_t pol_a = p.a_stream ? policy_evict_first() : policy_evict_last();
+      const uint64_t pol_b = p.b_stream ? policy_evict_first() : policy_evict_last();
       int stage = 0;
       uint32_t phase = 0;
       uint32_t armed_mask = 0, armed_parity = 0;
@@ -153,19 +155,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const int rr = tap / p.cv_s;
             const int ss = tap - rr * p.cv_s;
             tma_load_im2col_4d_pair(a, &p.tmA, c0, cv_w0, cv_h0, cv_n, (uint16_t)(ss * p.cv_dw),
-                                    (uint16_t)(rr * p.cv_dh), full_leader, pol);
+                                    (uint16_t)(rr * p.cv_dh), full_leader, pol_a);
           } else if (!p.a_mn) {
-            tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol);
+            tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol_a);
           } else {
-            tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol);
-            tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol);
+            tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol_a);
+            tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol_a);
           }
           if (!p.b_mn) {
-            tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol);
+            tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol_b);
           } else {
 #pragma unroll
             for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
-              tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol);
+              tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol_b);
           }
           if (++stage == S) {
             stage = 0;

@@ -123,6 +123,10 @@ struct GemmParams {
   // kb / cv_cblk, channels 64 (kb mod cv_cblk) onwards (C = 64 cv_cblk)
   int cv_tma;
   int cv_cblk;
+  // 1: the operand is read by one tile only (one tile column for A, one tile
+  // row for B), so its TMA loads carry an evict-first L2 hint; otherwise
+  // evict-last keeps it for the other tiles that read it
+  int a_stream, b_stream;
 };
 
 template <int BN, int MODE>
@@ -719,7 +723,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     // ---------------------------------------------------------------- producer
     if constexpr (Tr::kTmaLoad) {
       if (lane == 0) {
-        const uint64_t pol = policy_evict_last();
+        // operands re-read by other tiles stay in L2; one read once goes first
+        const uint64_t pol_a = p.a_stream ? policy_evict_first() : policy_evict_last();
+        const uint64_t pol_b = p.b_stream ? policy_evict_first() : policy_evict_last();
         int stage = 0;
         uint32_t phase = 0;
         uint32_t issued_mask = 0, issued_parity = 0;
@@ -739,17 +745,17 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* b = sB + stage * Cfg::kBBytes;
             const int k0 = kb * kBK;
             if (!p.a_mn) {
-              tma_load_3d(a, &p.tmA, k0, m0, za, &full[stage], pol);
+              tma_load_3d(a, &p.tmA, k0, m0, za, &full[stage], pol_a);
             } else {
-              tma_load_3d(a, &p.tmA, m0, k0, za, &full[stage], pol);
-              if (p.a_boxes > 1) tma_load_3d(a + kABytes / 2, &p.tmA, m0 + 64, k0, za, &full[stage], pol);
+              tma_load_3d(a, &p.tmA, m0, k0, za, &full[stage], pol_a);
+              if (p.a_boxes > 1) tma_load_3d(a + kABytes / 2, &p.tmA, m0 + 64, k0, za, &full[stage], pol_a);
             }
             if (!p.b_mn) {
-              tma_load_3d(b, &p.tmB, k0, n0, zb, &full[stage], pol);
+              tma_load_3d(b, &p.tmB, k0, n0, zb, &full[stage], pol_b);
             } else {
 #pragma unroll
               for (int h = 0; h < BN / 64; ++h)
-                tma_load_3d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, &full[stage], pol);
+                tma_load_3d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, &full[stage], pol_b);
             }
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -769,7 +775,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       if (warp == 0) {
         // TMA thread: raw int8 tiles into the staging ring
         if (lane == 0) {
-          const uint64_t pol = policy_evict_last();
+          // operands re-read by other tiles stay in L2; one read once goes first
+          const uint64_t pol_a = p.a_stream ? policy_evict_first() : policy_evict_last();
+          const uint64_t pol_b = p.b_stream ? policy_evict_first() : policy_evict_last();
           int st8 = 0;
           uint32_t ph8 = 0;
           uint32_t issued_mask = 0, issued_parity = 0;
@@ -789,13 +797,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               uint8_t* b = a + kBM * kBK;
               const int k0 = kb * kBK;
               if (!p.a_mn)
-                tma_load_3d(a, &p.tmA, k0, m0, za, &full8[st8], pol);
+                tma_load_3d(a, &p.tmA, k0, m0, za, &full8[st8], pol_a);
               else
-                tma_load_3d(a, &p.tmA, m0, k0, za, &full8[st8], pol);
+                tma_load_3d(a, &p.tmA, m0, k0, za, &full8[st8], pol_a);
               if (!p.b_mn)
-                tma_load_3d(b, &p.tmB, k0, n0, zb, &full8[st8], pol);
+                tma_load_3d(b, &p.tmB, k0, n0, zb, &full8[st8], pol_b);
               else
-                tma_load_3d(b, &p.tmB, n0, k0, zb, &full8[st8], pol);
+                tma_load_3d(b, &p.tmB, n0, k0, zb, &full8[st8], pol_b);
               issued_mask |= 1u << st8;
               issued_parity = (issued_parity & ~(1u << st8)) | (ph8 << st8);
               if (++st8 == S8) {
