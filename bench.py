@@ -145,6 +145,33 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def timed_loops(steps, launch, stream):
+    """The timed region: `steps` launches back to back with one event pair
+    around the loop (the throughput `value` comes from this pass), then the
+    same loop with an event pair around every launch (the per-launch kernel
+    durations the roofline uses; the events' own cost stays out of `value`).
+    launch(i) enqueues step i.  Returns (total_ms, kern_ms, launches of the
+    first pass)."""
+    import torch
+    import tiled_tensor_core_02_gb300 as ttc
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n0 = ttc.ttc_launch_count()
+    t0.record(stream)
+    for i in range(steps):
+        launch(i)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = ttc.ttc_launch_count() - n0
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        starts[i].record(stream)
+        launch(i)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in zip(starts, ends)], launches
+
+
 def dist_setup():
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -373,25 +400,13 @@ def main():
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    launches0 = ttc.ttc_launch_count()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(*copies[(args.warmup + i) % ncopy])
-        ends[i].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    launches = ttc.ttc_launch_count() - launches0
+    total_ms, kern_ms, launches = timed_loops(args.steps, lambda i: step(*copies[(args.warmup + i) % ncopy]),
+                                              stream)
     barrier(world)
     clocks = sampler.stop()
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during the timed region")
-    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world)
+    total_ms = max_over_ranks(total_ms, world)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     avg_kernel_s = statistics.mean(kern_ms) * 1e-3
 
@@ -646,22 +661,10 @@ def run_transpose(args, spec, name):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    launches0 = ttc.ttc_launch_count()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    launches = ttc.ttc_launch_count() - launches0
+    total_ms, kern_ms, launches = timed_loops(args.steps, lambda i: step(), stream)
     barrier(world)
     clocks = sampler.stop()
-    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    total_ms = max_over_ranks(total_ms, world)
     value = nbytes * args.steps * world / (total_ms * 1e-3) / 1e9
     peaks, peak_src = load_peaks()
     achieved = nbytes / (statistics.mean(kern_ms) * 1e-3) / 1e9
@@ -872,24 +875,13 @@ def run_conv(args, spec, name):
     time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    launches0 = ttc.ttc_launch_count()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(args.steps):
-        starts[i].record(stream)
-        step(*copies[(args.warmup + i) % ncopy])
-        ends[i].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    launches = ttc.ttc_launch_count() - launches0
+    total_ms, kern_ms, launches = timed_loops(args.steps, lambda i: step(*copies[(args.warmup + i) % ncopy]),
+                                              stream)
     barrier(world)
     clocks = sampler.stop()
     if ttc.ttc_get_device_error(s) != 0:
         raise SystemExit("device error during the timed region")
-    kern_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    total_ms = max_over_ranks(t0.elapsed_time(t1), world)
+    total_ms = max_over_ranks(total_ms, world)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
     peaks, peak_src = load_peaks()
     peak_key = "bf16_tflops_sustained" if total_ms >= 1000.0 else "bf16_tflops"

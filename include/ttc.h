@@ -266,6 +266,11 @@ const char* ttc_status_string(ttc_status status);
  *     tile rows per column of tiles (0: 16 for single CTAs, 8 for pairs).
  *   TTC_KNOB_PAIR_TILE_N: 0 lets the planner choose the CTA-pair tile width;
  *     256, 192 or 128 forces it (192 only with a column-major B).
+ *   TTC_KNOB_GEMV: 0 (default) runs matrix-vector problems whose reduction
+ *     is contiguous (M == 1 with a column-major B, or N == 1 with a
+ *     row-major A; fp16/bf16, K > 0, not batched) on the CUDA-core
+ *     matrix-vector kernel; 1 sends them to the tensor-core kernels like any
+ *     other shape.
  *   TTC_KNOB_SPLIT_K: 0 lets the planner choose; 1..8 splits every tile's K
  *     range across that many CTAs of a cluster (fp16/bf16 only), whose
  *     partial sums are added through distributed shared memory.
@@ -281,7 +286,8 @@ typedef enum {
   TTC_KNOB_SWAP_AB = 6,
   TTC_KNOB_SPLIT_K = 7,
   TTC_KNOB_PAIR_TILE_N = 8,
-  TTC_KNOB_GROUP_M = 9
+  TTC_KNOB_GROUP_M = 9,
+  TTC_KNOB_GEMV = 10
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -46,6 +46,8 @@ def test_knobs_validate(lib):
     assert ttc.ttc_set_knob("tile_n", 0) == 0
     assert ttc.ttc_set_knob("inject_stall", 2) == 1
     assert ttc.ttc_set_knob(99, 0) == 1
+    assert ttc.ttc_set_knob("gemv", 1) == 0 and ttc.ttc_set_knob("gemv", 2) == 1
+    assert ttc.ttc_set_knob("gemv", 0) == 0
 
 
 BF16 = ttc.DTYPE["bf16"]

@@ -14,6 +14,7 @@
 
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
+#include "gemv.cuh"
 #include "repack.cuh"
 #include "transpose.cuh"
 #include "ttc.h"
@@ -35,6 +36,7 @@ std::atomic<int> g_swap_mode{0};
 std::atomic<int> g_split_k{0};
 std::atomic<int> g_pair_tile_n{0};
 std::atomic<int> g_group_m{0};
+std::atomic<int> g_gemv_off{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -332,6 +334,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value < 0 || value > 64) return TTC_ERR_INVALID_ARG;
       g_group_m.store((int)value);
       return TTC_OK;
+    case TTC_KNOB_GEMV:
+      if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
+      g_gemv_off.store((int)value);
+      return TTC_OK;
     case TTC_KNOB_PAIR_TILE_N:
       if (value != 0 && value != 256 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
       g_pair_tile_n.store((int)value);
@@ -405,6 +411,50 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // ------------------------------------------------------------ canonicalisation
   canonicalise(M, N, K, layoutA, lda, layoutB, ldb);
   if (M == 1 && !tma_ok(D, ldd, out_esize) && reinterpret_cast<uintptr_t>(D) % 16 == 0) ldd = round_up(N, 16);
+
+  // ------------------------------------------------------------ matrix-vector problems
+  // One output row (M == 1) or column (N == 1) whose reduction runs along the
+  // matrix operand's contiguous dimension streams that operand with two FLOPs
+  // per element: CUDA-core kernel, one warp per output, no tiles.
+  const bool gemv_rows = (M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR);
+  if (gemv_rows && K > 0 && dtype != TTC_I8 && batch == 1 && !g_gemv_off.load()) {
+    GemvParams gp;
+    std::memset(&gp, 0, sizeof gp);
+    if (M == 1) {
+      // D[0, n] = sum_k A[0, k] B[k, n]; column n of B is K-contiguous
+      gp.x = static_cast<const uint16_t*>(A);
+      gp.incx = layoutA == TTC_ROW_MAJOR ? 1 : lda;
+      gp.mat = static_cast<const uint16_t*>(B);
+      gp.ldm = ldb;
+      gp.rows = (int)N;
+      gp.incy = 1;
+      gp.incc = 1;
+      gp.incb = 1;
+    } else {
+      // D[m, 0] = sum_k A[m, k] B[k, 0]; row m of A is K-contiguous
+      gp.x = static_cast<const uint16_t*>(B);
+      gp.incx = layoutB == TTC_COL_MAJOR ? 1 : ldb;
+      gp.mat = static_cast<const uint16_t*>(A);
+      gp.ldm = lda;
+      gp.rows = (int)M;
+      gp.incy = ldd;
+      gp.incc = ldc;
+      gp.incb = 0;  // the bias is per output column: one value for the single column
+    }
+    gp.K = (int)K;
+    gp.y = static_cast<uint16_t*>(D);
+    gp.c = beta != 0.0f ? static_cast<const uint16_t*>(C) : nullptr;
+    gp.bias = bias;
+    gp.alpha = alpha;
+    gp.beta = beta;
+    gp.act = (int)act;
+    gp.bf16 = dtype == TTC_BF16;
+    gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0 && gp.incx == 1 &&
+             reinterpret_cast<uintptr_t>(gp.x) % 16 == 0;
+    if (launch_gemv_rows(gp, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+    g_launches.fetch_add(1);
+    return TTC_OK;
+  }
 
   // ------------------------------------------------------------ workspace: repack what TMA cannot read
   if (batch == 1 && workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
