@@ -43,6 +43,7 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiCols = 32;  // columns per epilogue chunk
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kI8ChunkKBlocks = 16;     // int8: drain the accumulator every 1024 k
+constexpr int kConvWarps = 8;           // int8 TMA staging: warps widening int8 tiles to fp16
 
 enum ActKind : int { kActNone = 0, kActRelu = 1, kActGelu = 2 };
 
@@ -66,8 +67,8 @@ struct ModeTraits {
   static constexpr bool kConv = MODE == kModeConvF16 || MODE == kModeConvBF16;
   static constexpr bool kStaged = MODE == kModeI8Tma;  // TMA int8 staging + converter warps
   static constexpr bool kI8 = MODE == kModeI8 || MODE == kModeI8Tma;
-  // producer warps: 1 TMA thread; 4 plain-load warps; or 1 TMA warp + 4 converter warps
-  static constexpr int kProdWarps = kTmaLoad ? 1 : (kStaged ? 5 : 4);
+  // producer warps: 1 TMA thread; 4 plain-load warps; or 1 TMA warp + kConvWarps converter warps
+  static constexpr int kProdWarps = kTmaLoad ? 1 : (kStaged ? 1 + kConvWarps : 4);
   static constexpr int kMmaWarp = kProdWarps;
   static constexpr int kEpiWarp0 = kProdWarps + 1;
   static constexpr int kThreads = 32 * (kProdWarps + 1 + kEpiWarps);
@@ -148,7 +149,12 @@ struct TileCfg {
   static constexpr int kStagesRaw = kStageBudget / (kStageBytes + kStage8Bytes);
   static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
   static constexpr int kStages8 = T::kStaged ? kStages : 0;
-  static constexpr int kTmemCols = 2 * BN < 32 ? 32 : 2 * BN;
+  // two accumulators of BN columns; int8 adds BN columns of exact int32 running
+  // sums after them; allocations are powers of two of at least 32 columns
+  static constexpr int kTmemUsed = (T::kI8 ? 3 : 2) * BN;
+  static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
+                                   : kTmemUsed <= 256 ? 256 : 512;
+  static_assert(kTmemUsed <= 512, "TMEM columns");
   static constexpr int kSmemBytes =
       1024 /*align slack*/ + kStages * kStageBytes + kStages8 * kStage8Bytes + kEpiBytes + kRedBytes + kBarBytes;
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole epilogue chunks");
@@ -373,16 +379,17 @@ __device__ __forceinline__ void im2col_load_tile(uint8_t* sdst, const GemmParams
 // swizzle) into the fp16 128-byte-swizzled layout the tensor core reads (the
 // same placement as generic_load_tile).  Exact: with u = x + 128 (a byte),
 // the fp16 bit pattern 0x6400 | u is 1024 + u, and subtracting 1152 leaves x.
-template <int ROWS, int COLS>
+template <int ROWS, int COLS, int NT>
 __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16, int tid) {
   constexpr int kChunksPerRow = COLS / 16;
   constexpr int kChunks = ROWS * kChunksPerRow;
-  static_assert(kChunks % 128 == 0, "128 converter threads");
+  constexpr int kIters = (kChunks + NT - 1) / NT;
   constexpr layout::SwizzleBytes128 swz{};
   const __half2 bias2 = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
 #pragma unroll
-  for (int i = 0; i < kChunks / 128; ++i) {
-    const int q = tid + 128 * i;
+  for (int i = 0; i < kIters; ++i) {
+    const int q = tid + NT * i;
+    if (kChunks % NT != 0 && q >= kChunks) break;
     const int r = q / kChunksPerRow;
     const int c = (q % kChunksPerRow) * 16;
     const uint4 w = *reinterpret_cast<const uint4*>(s8 + r * COLS + c);
@@ -679,12 +686,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     // the lanes of warp 0 initialise the barriers between them
     for (int s = lane; s < S; s += 32) {
       // generic: one arrive per plain-load warp; staged: one per converter warp
-      mbar_init(&full[s], Tr::kTmaLoad ? 1 : 4);
+      mbar_init(&full[s], Tr::kTmaLoad ? 1 : (Tr::kStaged ? kConvWarps : 4));
       mbar_init(&empty[s], 1);
     }
     for (int s = lane; s < S8; s += 32) {
       mbar_init(&full8[s], 1);
-      mbar_init(&empty8[s], 4);
+      mbar_init(&empty8[s], kConvWarps);
     }
     if (lane < 2 * kEpiWarps) {
       mbar_init(&red_full[lane], 32 * (p.ksplit > 1 ? p.ksplit - 1 : 1));
@@ -819,7 +826,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         }
       } else {
         // converter warps: int8 staging slot -> fp16 MMA slot
-        const int ctid = threadIdx.x - 32;  // 0..127
+        const int ctid = threadIdx.x - 32;  // 0 .. 32 kConvWarps - 1
         int st8 = 0, stage = 0;
         uint32_t ph8 = 0, phase = 0;
         bool ok = true;
@@ -834,13 +841,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* a = sA + stage * kABytes;
             uint8_t* b = sB + stage * Cfg::kBBytes;
             if (!p.a_mn)
-              convert_i8_tile<kBM, kBK>(a8, a, ctid);
+              convert_i8_tile<kBM, kBK, 32 * kConvWarps>(a8, a, ctid);
             else
-              convert_i8_tile<kBK, kBM>(a8, a, ctid);
+              convert_i8_tile<kBK, kBM, 32 * kConvWarps>(a8, a, ctid);
             if (!p.b_mn)
-              convert_i8_tile<BN, kBK>(b8, b, ctid);
+              convert_i8_tile<BN, kBK, 32 * kConvWarps>(b8, b, ctid);
             else
-              convert_i8_tile<kBK, BN>(b8, b, ctid);
+              convert_i8_tile<kBK, BN, 32 * kConvWarps>(b8, b, ctid);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -986,13 +993,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       const bool row_ok = grow < p.M;
       const EpiPtrs ep = epi_ptrs(p, bz, Tr::kOutBytes);
 
-      // int8: exact int32 sums of the per-chunk partials, held in registers
-      int32_t isum[kI8 ? BN / kEpiCols : 1][32];
+      // int8: exact int32 sums of the per-chunk partials, kept in TMEM columns
+      // [2 BN, 3 BN) of this warp's lanes (each partial is an integer below
+      // 2^24 in magnitude, exact in fp32)
+      const uint32_t sum_cols = tmem_base + lane_base + 2 * BN;
       if constexpr (kI8) {
-#pragma unroll
-        for (int c = 0; c < BN / kEpiCols; ++c)
-#pragma unroll
-          for (int j = 0; j < 32; ++j) isum[c][j] = 0;
         for (int u = 0; u < units_per_tile; ++u, ++unit) {
           const int acc = unit & 1;
           if (!mbar_wait(&tmem_full[acc], (unit >> 1) & 1, wc)) {
@@ -1001,14 +1006,18 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           }
           tc_fence_after();
           if (has_k) {
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < BN / kEpiCols; ++c) {
-              uint32_t r[32];
+              uint32_t r[32], sm[32];
               tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * kEpiCols, r);
+              if (u > 0) tmem_ld_32x32b_x32(sum_cols + c * kEpiCols, sm);
               tmem_ld_wait();
 #pragma unroll
-              for (int j = 0; j < 32; ++j) isum[c][j] += __float2int_rn(__uint_as_float(r[j]));
+              for (int j = 0; j < 32; ++j)
+                sm[j] = (uint32_t)((u > 0 ? (int32_t)sm[j] : 0) + __float2int_rn(__uint_as_float(r[j])));
+              tmem_st_32x32b_x32(sum_cols + c * kEpiCols, sm);
             }
+            tmem_st_wait();
           }
           tc_fence_before();
           __syncwarp();
@@ -1027,17 +1036,23 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       }
       const int acc = unit & 1;  // fp16/bf16: the unit being drained below
 
-      // int8 indexes the register sums by chunk, so it unrolls; fp16/bf16 keeps one chunk's code
-      constexpr int kEpiUnroll = kI8 ? BN / kEpiCols : 1;
-#pragma unroll kEpiUnroll
+#pragma unroll 1
       for (int c = 0; c < BN / kEpiCols; ++c) {
         const int gcol0 = n0 + c * kEpiCols;
         uint32_t packed[Tr::kOutBytes == 4 ? 32 : 16];
         if constexpr (kI8) {
           // D = sum (+ C when beta == 1); alpha == 1 (checked on the host)
           int32_t v[32];
+          if (has_k) {
+            uint32_t sm[32];
+            tmem_ld_32x32b_x32(sum_cols + c * kEpiCols, sm);
+            tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = isum[c][j];
+            for (int j = 0; j < 32; ++j) v[j] = (int32_t)sm[j];
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0;
+          }
           if (p.beta != 0.0f && row_ok && p.d_trans) {
             const int32_t* ccol = reinterpret_cast<const int32_t*>(ep.C) + grow;
 #pragma unroll
