@@ -267,3 +267,17 @@ def test_transpose_matches_numpy_and_is_an_involution(rows, cols, eb):
     assert not dst.reshape(cols, rows + 1)[:, rows:].any()
     back = oracle.transpose(dst, cols, rows, lds=rows + 1, ldd=cols)
     assert np.array_equal(back.reshape(rows, cols), logical)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16", "i8"])
+@pytest.mark.parametrize("layout", ["row", "col"])
+def test_matvec_matches_numpy(dtype, layout):
+    rows, cols = 37, 53
+    st = synth.Stream(17)
+    vals = synth.draw(st, rows * cols, "int8" if dtype == "i8" else "uniform")
+    X = synth.store(vals, dtype).reshape(rows, cols)
+    buf, ld = synth.to_layout(X, layout, (cols if layout == "row" else rows) + 3)
+    x = synth.Stream(18).uniform(cols)
+    logical = X.astype(np.float64) if dtype == "i8" else oracle.decode(X, dtype)
+    y = oracle.matvec(rows, cols, buf, ld, layout, dtype, x)
+    assert np.allclose(y, logical @ x, rtol=1e-13, atol=1e-12)
