@@ -44,6 +44,8 @@ constexpr int kEpiCols = 32;  // columns per epilogue chunk
 constexpr int kABytes = kBM * kBK * 2;  // 16 KiB
 constexpr int kI8ChunkKBlocks = 16;     // int8: drain the accumulator every 1024 k
 constexpr int kConvWarps = 8;           // int8 TMA staging: warps widening int8 tiles to fp16
+constexpr int kConvGroups = 2;          // ... in groups that take alternate k-blocks
+constexpr int kConvGroupWarps = kConvWarps / kConvGroups;
 
 enum ActKind : int { kActNone = 0, kActRelu = 1, kActGelu = 2 };
 
@@ -686,12 +688,12 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     // the lanes of warp 0 initialise the barriers between them
     for (int s = lane; s < S; s += 32) {
       // generic: one arrive per plain-load warp; staged: one per converter warp
-      mbar_init(&full[s], Tr::kTmaLoad ? 1 : (Tr::kStaged ? kConvWarps : 4));
+      mbar_init(&full[s], Tr::kTmaLoad ? 1 : (Tr::kStaged ? kConvGroupWarps : 4));
       mbar_init(&empty[s], 1);
     }
     for (int s = lane; s < S8; s += 32) {
       mbar_init(&full8[s], 1);
-      mbar_init(&empty8[s], kConvWarps);
+      mbar_init(&empty8[s], kConvGroupWarps);
     }
     if (lane < 2 * kEpiWarps) {
       mbar_init(&red_full[lane], 32 * (p.ksplit > 1 ? p.ksplit - 1 : 1));
@@ -825,13 +827,19 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           }
         }
       } else {
-        // converter warps: int8 staging slot -> fp16 MMA slot
+        // converter warps: int8 staging slot -> fp16 MMA slot.  Group g widens
+        // the k-blocks at positions j = g (mod kConvGroups) of the CTA's
+        // k-block sequence, so the groups' conversions overlap.
         const int ctid = threadIdx.x - 32;  // 0 .. 32 kConvWarps - 1
-        int st8 = 0, stage = 0;
-        uint32_t ph8 = 0, phase = 0;
+        const int grp = ctid / (32 * kConvGroupWarps);
+        const int gtid = ctid % (32 * kConvGroupWarps);
         bool ok = true;
+        int j = 0;  // position in the k-block sequence
         for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
-          for (int kb = k_lo; kb < k_hi; ++kb) {
+          for (int kb = k_lo; kb < k_hi; ++kb, ++j) {
+            if (j % kConvGroups != grp) continue;
+            const int st8 = j % S8, stage = j % S;
+            const uint32_t ph8 = (uint32_t)(j / S8) & 1u, phase = (uint32_t)(j / S) & 1u;
             if (!mbar_wait(&full8[st8], ph8, wc) || !mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
@@ -841,26 +849,18 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* a = sA + stage * kABytes;
             uint8_t* b = sB + stage * Cfg::kBBytes;
             if (!p.a_mn)
-              convert_i8_tile<kBM, kBK, 32 * kConvWarps>(a8, a, ctid);
+              convert_i8_tile<kBM, kBK, 32 * kConvGroupWarps>(a8, a, gtid);
             else
-              convert_i8_tile<kBK, kBM, 32 * kConvWarps>(a8, a, ctid);
+              convert_i8_tile<kBK, kBM, 32 * kConvGroupWarps>(a8, a, gtid);
             if (!p.b_mn)
-              convert_i8_tile<BN, kBK, 32 * kConvWarps>(b8, b, ctid);
+              convert_i8_tile<BN, kBK, 32 * kConvGroupWarps>(b8, b, gtid);
             else
-              convert_i8_tile<kBK, BN, 32 * kConvWarps>(b8, b, ctid);
+              convert_i8_tile<kBK, BN, 32 * kConvGroupWarps>(b8, b, gtid);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(&full[stage]);
               mbar_arrive(&empty8[st8]);
-            }
-            if (++st8 == S8) {
-              st8 = 0;
-              ph8 ^= 1u;
-            }
-            if (++stage == S) {
-              stage = 0;
-              phase ^= 1u;
             }
           }
         }
