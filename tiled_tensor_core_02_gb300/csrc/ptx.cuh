@@ -106,18 +106,9 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// 2-D tiled load, completion counted in bytes on `bar`.  c0 is the innermost
-// (contiguous) coordinate; the caller keeps c0 * element size a multiple of 16.
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1,
-                                            uint64_t* bar, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(cache_hint)
-      : "memory");
-}
-
-// 3-D tiled load: (c0, c1) as above, c2 the batch index.
+// 3-D tiled load, completion counted in bytes on `bar`.  c0 is the innermost
+// (contiguous) coordinate, which the caller keeps at a multiple of 16 bytes;
+// c1 the row; c2 the batch index.
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1, int32_t c2,
                                             uint64_t* bar, uint64_t cache_hint) {
   asm volatile(
@@ -132,13 +123,6 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, int32_t c0, i
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
                    reinterpret_cast<uint64_t>(m)),
                "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, int32_t c0, int32_t c1, const void* src) {
-  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
-                   reinterpret_cast<uint64_t>(m)),
-               "r"(c0), "r"(c1), "r"(smem_u32(src))
                : "memory");
 }
 
@@ -256,7 +240,6 @@ __host__ __device__ constexpr uint32_t idesc_f16(bool bf16, bool a_mn_major, boo
          ((b_mn_major ? 1u : 0u) << 16) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
-
 // ------------------------------------------------------------------ clusters / CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -316,16 +299,8 @@ __device__ __forceinline__ void cluster_sync() {
 }
 
 // TMA load by one CTA of a pair whose completion is counted on an mbarrier
-// that may live in the peer CTA (bar_cluster: shared::cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1,
-                                                 uint32_t bar_cluster, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
-      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar_cluster), "l"(cache_hint)
-      : "memory");
-}
-
+// that may live in the peer CTA (bar_cluster: shared::cluster address);
+// coordinates as for tma_load_3d.
 __device__ __forceinline__ void tma_load_3d_pair(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1,
                                                  int32_t c2, uint32_t bar_cluster, uint64_t cache_hint) {
   asm volatile(
@@ -388,7 +363,6 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
       : "memory");
 }
 
-
 // 16 bytes from shared::cluster address `addr` (any CTA of the cluster).
 __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
   uint4 v;
@@ -400,7 +374,6 @@ __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
 }
 
 // ------------------------------------------------------------------ misc
-__device__ __forceinline__ uint32_t elect_lane0() { return (threadIdx.x & 31u) == 0u; }
 
 __device__ __forceinline__ float tanh_approx(float x) {
   float y;
