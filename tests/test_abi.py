@@ -48,6 +48,8 @@ def test_knobs_validate(lib):
     assert ttc.ttc_set_knob(99, 0) == 1
     assert ttc.ttc_set_knob("gemv", 1) == 0 and ttc.ttc_set_knob("gemv", 2) == 1
     assert ttc.ttc_set_knob("gemv", 0) == 0
+    assert ttc.ttc_set_knob("conv_halo", 2) == 0 and ttc.ttc_set_knob("conv_halo", 3) == 1
+    assert ttc.ttc_set_knob("conv_halo", 0) == 0
 
 
 BF16 = ttc.DTYPE["bf16"]

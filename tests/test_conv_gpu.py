@@ -97,13 +97,19 @@ def test_conv_empty_and_degenerate():
                                 None, 0, ttc.DTYPE["bf16"], None) == 0
 
 
+@pytest.mark.parametrize("halo", [0, 2])
 @pytest.mark.parametrize("name", sorted(synth.CONV_WORKLOADS))
-def test_conv_full_size_sampled(name):
-    """The benchmark's convolution in its launch configuration: sampled rows,
-    columns and elements against the oracle."""
+def test_conv_full_size_sampled(name, halo):
+    """The benchmark's convolution in its launch configuration (halo = 0: the
+    planner's choice, the halo kernel; 2: im2col loads): sampled rows, columns
+    and elements against the oracle."""
     spec = dict(synth.CONV_WORKLOADS[name])
     cp = synth.ConvProblem(**spec)
-    out = run_conv(cp).reshape(cp.M, cp.K)
+    ttc.ttc_set_knob("conv_halo", halo)
+    try:
+        out = run_conv(cp).reshape(cp.M, cp.K)
+    finally:
+        ttc.ttc_set_knob("conv_halo", 0)
     mm, kk = oracle.sample_indices(cp.M, cp.K, seed=spec["seed"], n_lines=4, n_elems=16384)
     r, sabs, _ = oracle.conv_elements(cp, mm, kk)
     d = oracle.decode(out[mm, kk], cp.dtype)
@@ -129,16 +135,77 @@ def pair_knob():
     ttc.ttc_set_knob("pair", 0)
 
 
+@pytest.fixture
+def halo_knob():
+    yield lambda v: ttc.ttc_set_knob("conv_halo", v)
+    ttc.ttc_set_knob("conv_halo", 0)
+
+
 @pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("shape", PAIR_SHAPES)
-def test_conv_im2col_pair_path_matches_oracle(shape, pair, pair_knob):
+def test_conv_im2col_pair_path_matches_oracle(shape, pair, pair_knob, halo_knob):
     N, H, W, C, K, R, S, pad, stride, dil = shape
     cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype="bf16", seed=sum(shape[:7]) + 100,
                            with_c=True, dist_bias="uniform")
     pair_knob(pair)
+    halo_knob(2)
     check_full(cp, run_conv(cp, alpha=1.25, beta=0.5, act="relu"), alpha=1.25, beta=0.5, act="relu")
 
 
-def test_conv_im2col_pair_path_f16():
+def test_conv_im2col_pair_path_f16(halo_knob):
+    halo_knob(2)
     cp = synth.ConvProblem(2, 12, 12, 128, 256, 3, 3, (1, 1), (1, 1), (1, 1), dtype="f16", seed=77)
     check_full(cp, run_conv(cp))
+
+
+# Unit-stride shapes the halo kernel takes (C a multiple of 64, K of 32): one
+# box of padded input rows per 64-channel block feeds every filter tap.
+HALO_SHAPES = [
+    (2, 20, 20, 64, 128, 3, 3, (1, 1), (1, 1), (1, 1)),    # 4 position tiles per image, the last ragged
+    (3, 9, 11, 64, 96, 3, 3, (1, 1), (1, 1), (1, 1)),      # odd N: the last pair's second image is absent
+    (2, 17, 19, 128, 192, 5, 5, (2, 2), (1, 1), (2, 2)),   # dilated 5 x 5, a partial 256-wide channel block
+    (1, 9, 31, 64, 320, 1, 3, (0, 1), (1, 1), (1, 1)),     # rectangular filter, one image, 3 channel blocks of 128
+    (2, 7, 7, 256, 256, 3, 3, (0, 0), (1, 1), (1, 1)),     # no padding: 5 x 5 outputs
+    (4, 16, 16, 64, 128, 1, 1, (0, 0), (1, 1), (1, 1)),    # 1 x 1: no dropped positions
+    (2, 14, 14, 128, 384, 7, 7, (3, 3), (1, 1), (1, 1)),   # 7 x 7, 3 blocks of 128 output channels
+    (5, 6, 40, 64, 64, 3, 1, (2, 0), (1, 1), (3, 1)),      # tall dilation, pad > 1, tiles spanning 4 rows
+]
+
+
+@pytest.mark.parametrize("shape", HALO_SHAPES)
+def test_conv_halo_path_matches_oracle(shape, halo_knob):
+    N, H, W, C, K, R, S, pad, stride, dil = shape
+    cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype="bf16", seed=sum(shape[:7]) + 200,
+                           with_c=True, dist_bias="uniform")
+    halo_knob(1)
+    check_full(cp, run_conv(cp, alpha=1.25, beta=0.5, act="relu"), alpha=1.25, beta=0.5, act="relu")
+
+
+@pytest.mark.parametrize("act", ["none", "gelu_tanh"])
+def test_conv_halo_path_f16_and_epilogue(act, halo_knob):
+    halo_knob(1)
+    cp = synth.ConvProblem(3, 12, 12, 128, 256, 3, 3, (1, 1), (1, 1), (1, 1), dtype="f16", seed=78)
+    check_full(cp, run_conv(cp, act=act), act=act)
+
+
+def test_conv_halo_path_in_place_c_and_padded_pitch(halo_knob):
+    halo_knob(1)
+    cp = synth.ConvProblem(3, 10, 10, 64, 96, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=79, with_c=True)
+    check_full(cp, run_conv(cp, beta=1.0, in_place=True, use_bias=False), beta=1.0, use_bias=False)
+    out = run_conv(cp, ldd=136).reshape(cp.M, 136)
+    check_full(cp, out.ravel(), ldd=136)
+    assert (out[:, cp.K:] == 0xFFFF).all()  # the pitch padding is not written
+
+
+def test_conv_halo_declines_what_it_cannot_run(halo_knob):
+    """Forced, the halo kernel still leaves strided, unaligned and too-wide
+    problems to the other paths; the results stay right."""
+    halo_knob(1)
+    for shape, kw in [((1, 14, 14, 128, 256, 3, 3, (1, 1), (2, 2), (1, 1)), {}),     # stride 2
+                      ((2, 6, 6, 64, 96, 3, 3, (1, 1), (1, 1), (1, 1)), dict(ldd=100)),  # ldd not a multiple of 8
+                      ((1, 3, 300, 64, 64, 3, 3, (1, 1), (1, 1), (1, 1)), {}),       # padded row over 256 pixels
+                      ((1, 8, 8, 64, 80, 3, 3, (1, 1), (1, 1), (1, 1)), {})]:        # K not a multiple of 32
+        N, H, W, C, K, R, S, pad, stride, dil = shape
+        cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype="bf16", seed=sum(shape[:7]))
+        ldd = kw.get("ldd", K)
+        check_full(cp, run_conv(cp, ldd=ldd), ldd=ldd)

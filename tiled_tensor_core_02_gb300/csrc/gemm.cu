@@ -12,6 +12,7 @@
 #include <mutex>
 #include <utility>
 
+#include "conv_halo.cuh"
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
 #include "gemv.cuh"
@@ -36,6 +37,7 @@ std::atomic<int> g_swap_mode{0};
 std::atomic<int> g_split_k{0};
 std::atomic<int> g_pair_tile_n{0};
 std::atomic<int> g_group_m{0};
+std::atomic<int> g_conv_halo{0};
 std::atomic<int> g_gemv_off{0};
 std::atomic<int64_t> g_launches{0};
 
@@ -45,6 +47,7 @@ struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
   int pair_clusters[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // resident CTA pairs [bf16][width 256/192/128]
+  int halo_clusters[2][2] = {{-1, -1}, {-1, -1}};          // halo convolution pairs [bf16][width 256/128]
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -193,6 +196,60 @@ bool encode_im2col(CUtensorMap* m, CUtensorMapDataType dt, const void* X, int64_
                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tiled map over an N x H x W x C tensor (16-bit elements, tightly packed)
+// for the halo convolution: boxes of 64 channels x `wp` pixels x `rows` rows of
+// one image, 128-byte swizzle.  The kernel starts each box at pixel -pad_w of
+// a row, so a box row is one zero-padded input row.
+bool encode_halo(CUtensorMap* m, CUtensorMapDataType dt, const void* X, int64_t N, int64_t H, int64_t W, int64_t C,
+                 int64_t wp, int64_t rows) {
+  cuuint64_t dims[4] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)N};
+  cuuint64_t strides[3] = {(cuuint64_t)(C * 2), (cuuint64_t)(W * C * 2), (cuuint64_t)(H * W * C * 2)};
+  cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)wp, (cuuint32_t)rows, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return g_encode(m, dt, 4, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Plan of the halo convolution for a unit-stride problem, or ok == false when
+// its shape does not fit the kernel: a padded output row of at most 256
+// positions, a halo box of at most 256 rows, and two halo buffers plus at
+// least three filter stages in shared memory.
+struct HaloPlan {
+  bool ok = false;
+  int bn = 0, wp = 0, rows = 0, tiles_per_img = 0, stages = 0, smem = 0;
+  uint32_t tx = 0, bytes = 0;
+};
+HaloPlan plan_halo(int64_t P, int64_t Q, int64_t K, int64_t R, int64_t S, int64_t dh, int64_t dw) {
+  HaloPlan h;
+  const int64_t wp = Q + (S - 1) * dw;
+  if (wp > 256) return h;
+  // rows a tile's taps reach: from its first position's row to its last
+  // position shifted by the last tap; 128 j mod wp repeats with period <= wp
+  const int64_t tiles_per_img = (P * wp + kBM - 1) / kBM;
+  const int64_t reach = (kBM - 1) + (R - 1) * dh * wp + (S - 1) * dw;
+  int64_t rows = 0;
+  for (int64_t j = 0; j < tiles_per_img && j < 256; ++j) {
+    const int64_t r = ((kBM * j) % wp + reach) / wp + 1;
+    if (r > rows) rows = r;
+  }
+  if (rows > 256) return h;
+  h.bn = (K % 256 == 0 || K % 256 > 128) ? 256 : 128;
+  const int b_half = h.bn / 2 * kBK * 2;
+  h.tx = (uint32_t)(rows * wp * kBK * 2);
+  h.bytes = (h.tx + 1023u) / 1024u * 1024u;
+  const int64_t room = 227 * 1024 - conv_halo_smem_bytes((int)h.bytes, 0, b_half);
+  const int64_t stages = room / b_half;
+  if (stages < 3) return h;
+  h.stages = (int)(stages < kHaloMaxStages ? stages : kHaloMaxStages);
+  h.smem = conv_halo_smem_bytes((int)h.bytes, h.stages, b_half);
+  h.wp = (int)wp;
+  h.rows = (int)rows;
+  h.tiles_per_img = (int)tiles_per_img;
+  h.ok = true;
+  return h;
+}
+
 template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
@@ -337,6 +394,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
     case TTC_KNOB_GEMV:
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_gemv_off.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_CONV_HALO:
+      if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
+      g_conv_halo.store((int)value);
       return TTC_OK;
     case TTC_KNOB_PAIR_TILE_N:
       if (value != 0 && value != 256 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
@@ -843,6 +904,60 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
   prm.cv_sw = (int)stride_w;
   prm.cv_dh = (int)dil_h;
   prm.cv_dw = (int)dil_w;
+
+  // Unit stride: the halo kernel, when whole 64-channel blocks, output
+  // channels in 32-column chunks and 16-byte aligned rows of X, D and C let it
+  // run, and its plan fits
+  const int halo_mode = g_conv_halo.load();
+  const bool c_rows16 = beta == 0.0f || (reinterpret_cast<uintptr_t>(Cm) % 16 == 0 && ldc % 8 == 0);
+  if (halo_mode != 2 && stride_h == 1 && stride_w == 1 && C > 0 && C % kBK == 0 && K % 32 == 0 &&
+      reinterpret_cast<uintptr_t>(X) % 16 == 0 && tma_ok(Wt, Kg, 2) && reinterpret_cast<uintptr_t>(D) % 16 == 0 &&
+      ldd % 8 == 0 && c_rows16 && !g_force_generic_load.load() && forced_bn == 0 &&
+      (halo_mode == 1 || (M >= kPairBM && K >= 128))) {
+    const HaloPlan hpn = plan_halo(P, Q, K, R, S, dil_h, dil_w);
+    const int64_t img_pairs = (N + 1) / 2, n_blocks = (K + hpn.bn - 1) / (hpn.bn > 0 ? hpn.bn : 1);
+    if (hpn.ok && img_pairs * hpn.tiles_per_img * n_blocks <= lim) {
+      const bool bf16 = dtype == TTC_BF16;
+      int& cl = dev->halo_clusters[bf16 ? 1 : 0][hpn.bn == 256 ? 0 : 1];
+      if (cl < 0) {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (cl < 0) cl = conv_halo_max_clusters(bf16, hpn.bn);
+      }
+      if (cl > 0) {
+        ConvHaloParams hp;
+        std::memset(&hp, 0, sizeof hp);
+        if (!encode_halo(&prm.tmA, dt, X, N, H, W, C, hpn.wp, hpn.rows) ||
+            !encode_3d(&prm.tmB, dt, 2, Wt, Kg, K, Kg, kBK, hpn.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+          return TTC_ERR_CUDA;
+        hp.g = prm;
+        hp.n_img = (int)N;
+        hp.img_pairs = (int)img_pairs;
+        hp.tiles_per_img = hpn.tiles_per_img;
+        hp.n_blocks = (int)n_blocks;
+        hp.num_tiles = (int)(img_pairs * hpn.tiles_per_img * n_blocks);
+        hp.wp = hpn.wp;
+        hp.p = (int)P;
+        hp.q = (int)Q;
+        hp.c = (int)C;
+        hp.cblk = (int)(C / kBK);
+        hp.taps = (int)(R * S);
+        hp.s = (int)S;
+        hp.row_step = (int)(dil_h * hpn.wp);
+        hp.dw = (int)dil_w;
+        hp.ph = (int)pad_h;
+        hp.pw = (int)pad_w;
+        hp.halo_rows = hpn.rows;
+        hp.halo_tx = hpn.tx;
+        hp.halo_bytes = hpn.bytes;
+        hp.stages = hpn.stages;
+        const int nclus = hp.num_tiles < cl ? hp.num_tiles : cl;
+        if (launch_conv_halo(bf16, hpn.bn, hp, hpn.smem, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+          return TTC_ERR_CUDA;
+        g_launches.fetch_add(1);
+        return TTC_OK;
+      }
+    }
+  }
 
   // CTA-pair kernel with im2col TMA loads: whole 64-channel blocks per filter
   // tap, window corners and tap offsets inside the ranges an im2col map of two

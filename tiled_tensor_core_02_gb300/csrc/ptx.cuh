@@ -219,7 +219,11 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 //   [16,30) leading-dimension byte offset >> 4
 //   [32,46) stride-dimension byte offset >> 4
 //   [46,48) descriptor version (1 on sm_100 family)
-//   [49,52) base offset (0: swizzle atoms are 1024-byte aligned)
+//   [49,52) base offset, left 0: the MMA takes the 128-byte swizzle's XOR
+//           phase from the absolute address bits [7,10) of each row, as the
+//           TMA does when it writes, so an operand may start at any 128-byte
+//           row of a TMA-written region (measured: setting the field to the
+//           start row's phase gives wrong products)
 //   [61,64) swizzle mode (2 = 128-byte swizzle)
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   uint64_t d = 0;
@@ -324,6 +328,18 @@ __device__ __forceinline__ void tma_load_im2col_4d_pair(void* dst, const CUtenso
       ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], {%7, %8}, %9;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar_cluster), "h"(off_w),
       "h"(off_h), "l"(cache_hint)
+      : "memory");
+}
+
+// 4-D tiled TMA load for a CTA pair (completion on the leader's barrier); the
+// map fixes the box and the element order, (c0, c1, c2, c3) is the box's first
+// element, coordinates outside the tensor read zeros.
+__device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m, int32_t c0, int32_t c1, int32_t c2,
+                                                 int32_t c3, uint32_t bar_cluster, uint64_t cache_hint) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar_cluster), "l"(cache_hint)
       : "memory");
 }
 
