@@ -55,9 +55,11 @@ __device__ __forceinline__ int halo_out_row(const ConvHaloParams& hp, int img, i
 // Writes one 32-column chunk of the warp's 32 positions: each thread stages
 // its row's 64 bytes (16-byte words XOR-swizzled by row pair, so the writes
 // and the reads are free of bank conflicts), then each store instruction
-// writes 8 rows x 64 bytes, dropping positions that are not outputs.
+// writes 8 rows x 64 bytes.  out_row[it] is the output row (or -1: dropped)
+// of the position this thread stores in step it, row it * 8 + lane / 4 of the
+// warp's 32.
 __device__ __forceinline__ void halo_store_chunk(const ConvHaloParams& hp, const uint32_t (&packed)[16],
-                                                 uint8_t* sbuf, int lane, int img, int pos0, int gcol0) {
+                                                 uint8_t* sbuf, int lane, const int (&out_row)[4], int gcol0) {
 #pragma unroll
   for (int ch = 0; ch < 4; ++ch)
     *reinterpret_cast<uint4*>(sbuf + lane * 64 + ((ch ^ ((lane >> 1) & 3)) * 16)) =
@@ -67,7 +69,7 @@ __device__ __forceinline__ void halo_store_chunk(const ConvHaloParams& hp, const
 #pragma unroll
   for (int it = 0; it < 4; ++it) {
     const int r = it * 8 + (lane >> 2);
-    const int m = halo_out_row(hp, img, pos0 + r);
+    const int m = out_row[it];
     if (m >= 0 && gcol0 + ch * 8 < hp.g.N) {
       const uint4 v = *reinterpret_cast<const uint4*>(sbuf + r * 64 + ((ch ^ ((r >> 1) & 3)) * 16));
       *reinterpret_cast<uint4*>(static_cast<uint16_t*>(hp.g.D) + (int64_t)m * hp.g.ldd + gcol0 + ch * 8) = v;
@@ -200,6 +202,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (leader && lane == 0) {
       const uint32_t idesc = idesc_f16(kBF16, false, false, 2 * kBM, BN);
+      // descriptors are built once and stepped: the start address is a 14-bit
+      // field at bit 0 (address >> 4) that no shared-memory offset overflows,
+      // so +2 is one 16-deep k-step (32 bytes), +8 one 128-byte row
+      const uint64_t desc0 = smem_desc_sw128(0u, 16, 1024);
+      const uint64_t b_desc0 = desc0 + (smem_u32(sB) >> 4);
+      const uint64_t a_tap_step = (uint64_t)hp.dw * 8u;
+      const uint64_t a_row_step = (uint64_t)(hp.row_step - hp.s * hp.dw) * 8u;
       bool ok = true;
       bool any_mma = false;
       if (p.inject_stall) ok = mbar_wait(stall_bar, 0, wc);  // nothing arrives here
@@ -224,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           tc_fence_after();
           // tap (r, s) starts r row_step + s dw rows past the tile's first position
-          uint32_t a_addr = smem_u32(sH + hb * hp.halo_bytes) + (uint32_t)off * 128u;
+          uint64_t ad = desc0 + ((smem_u32(sH + hb * hp.halo_bytes) + (uint32_t)off * 128u) >> 4);
           int fs = 0;
           for (int tap = 0; tap < hp.taps; ++tap) {
             if (!mbar_wait(&full[stage], phase, wc)) {
@@ -232,23 +241,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t b_addr = smem_u32(sB + stage * kBHalfBytes);
+            const uint64_t bd = b_desc0 + (uint32_t)stage * (kBHalfBytes >> 4);
+            mma_f16_pair(d_tmem, ad, bd, idesc, (cb | tap) != 0);
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k) {
-              const uint64_t ad = smem_desc_sw128(a_addr + k * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(b_addr + k * 32, 16, 1024);
-              mma_f16_pair(d_tmem, ad, bd, idesc, (cb | tap | k) != 0);
-            }
+            for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
             any_mma = true;
             mma_commit_pair(&empty[stage], 0x3);
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
             }
-            a_addr += (uint32_t)hp.dw * 128u;
+            ad += a_tap_step;
             if (++fs == hp.s) {
               fs = 0;
-              a_addr += (uint32_t)(hp.row_step - hp.s * hp.dw) * 128u;
+              ad += a_row_step;
             }
           }
           if (!ok) break;
@@ -278,6 +284,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const int pos0 = ht.j * kBM + q * 32;  // the warp's first position
       const int m = halo_out_row(hp, ht.img, pos0 + lane);
       const bool row_ok = m >= 0;
+      int out_row[4];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) out_row[s4] = halo_out_row(hp, ht.img, pos0 + s4 * 8 + (lane >> 2));
       const int grow = row_ok ? m : p.M;  // past the end: C reads nothing for it
       const int n0 = ht.nb * BN;
       const int chunks = min(BN, p.N - n0) / kEpiCols;
@@ -301,7 +310,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         uint32_t packed[16];
         epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, nullptr, lane, ep);
         if (c + 1 < chunks) c_fetch16(p, ep, cpath, grow, gcol0 + kEpiCols, lane, cc);
-        halo_store_chunk(hp, packed, sbuf, lane, ht.img, pos0, gcol0);
+        halo_store_chunk(hp, packed, sbuf, lane, out_row, gcol0);
       }
     }
   }

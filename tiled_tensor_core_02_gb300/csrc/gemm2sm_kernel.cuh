@@ -192,8 +192,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
-      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      // descriptors are built once and stepped: the start address is a 14-bit
+      // field at bit 0 (address >> 4) that no shared-memory offset overflows
+      const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), p.a_mn ? 8192u : 16u, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), p.b_mn ? 8192u : 16u, 1024);
+      const uint64_t a_kstep = p.a_mn ? 2048u >> 4 : 32u >> 4, b_kstep = p.b_mn ? 2048u >> 4 : 32u >> 4;
       for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
@@ -209,14 +212,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_addr = smem_u32(sA + stage * PairCfg::kAHalfBytes);
-          const uint32_t b_addr = smem_u32(sB + stage * PairCfg::kBHalfBytes);
+          const uint64_t ad = a_desc0 + (uint32_t)stage * (PairCfg::kAHalfBytes >> 4);
+          const uint64_t bd = b_desc0 + (uint32_t)stage * (PairCfg::kBHalfBytes >> 4);
+          mma_f16_pair(d_tmem, ad, bd, idesc, kb != 0);
 #pragma unroll
-          for (int k = 0; k < kBK / kUmmaK; ++k) {
-            const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024);
-            const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024);
-            mma_f16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0);
-          }
+          for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
           if (++stage == S) {

@@ -925,8 +925,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       int stage = 0;
       uint32_t phase = 0;
       int unit = 0;
-      const uint32_t a_lbo = p.a_mn ? 8192u : 16u, b_lbo = p.b_mn ? 8192u : 16u;
-      const uint32_t a_kstep = p.a_mn ? 2048u : 32u, b_kstep = p.b_mn ? 2048u : 32u;
+      // descriptors are built once and stepped: the start address is a 14-bit
+      // field at bit 0 (address >> 4) that no shared-memory offset overflows
+      const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), p.a_mn ? 8192u : 16u, 1024);
+      const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), p.b_mn ? 8192u : 16u, 1024);
+      const uint64_t a_kstep = p.a_mn ? 2048u >> 4 : 32u >> 4, b_kstep = p.b_mn ? 2048u >> 4 : 32u >> 4;
       for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
         for (int u = 0; ok && u < units_per_tile; ++u, ++unit) {
           const int acc = unit & 1;
@@ -945,14 +948,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               break;
             }
             tc_fence_after();
-            const uint32_t a_addr = smem_u32(sA + stage * kABytes);
-            const uint32_t b_addr = smem_u32(sB + stage * Cfg::kBBytes);
+            const uint64_t ad = a_desc0 + (uint32_t)stage * (kABytes >> 4);
+            const uint64_t bd = b_desc0 + (uint32_t)stage * (Cfg::kBBytes >> 4);
+            mma_f16(d_tmem, ad, bd, idesc, kb != kb0);
 #pragma unroll
-            for (int k = 0; k < kBK / kUmmaK; ++k) {
-              const uint64_t ad = smem_desc_sw128(a_addr + k * a_kstep, a_lbo, 1024);
-              const uint64_t bd = smem_desc_sw128(b_addr + k * b_kstep, b_lbo, 1024);
-              mma_f16(d_tmem, ad, bd, idesc, (kb != kb0) || (k != 0));
-            }
+            for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
             any_mma = true;
             mma_commit(&empty[stage]);
             if (++stage == S) {
