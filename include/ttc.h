@@ -271,6 +271,9 @@ const char* ttc_status_string(ttc_status status);
  *     row-major A; fp16/bf16, K > 0, not batched) on the CUDA-core
  *     matrix-vector kernel; 1 sends them to the tensor-core kernels like any
  *     other shape.
+ *   TTC_KNOB_PAIR_TAIL: 0 (default) lets the CTA-pair kernels run a last,
+ *     partial wave of tiles (or a problem of at most half a wave) as half
+ *     tiles on twice as many pairs; 1 keeps whole tiles.
  *   TTC_KNOB_CONV_HALO: 0 (default) runs a unit-stride convolution that
  *     qualifies (see ttc_conv2d_fprop) on the halo-tile kernel; 1 does the
  *     same whatever the problem's size; 2 never uses it (im2col loads or
@@ -292,7 +295,8 @@ typedef enum {
   TTC_KNOB_PAIR_TILE_N = 8,
   TTC_KNOB_GROUP_M = 9,
   TTC_KNOB_GEMV = 10,
-  TTC_KNOB_CONV_HALO = 11
+  TTC_KNOB_CONV_HALO = 11,
+  TTC_KNOB_PAIR_TAIL = 12
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -181,6 +181,22 @@ def test_conv_halo_path_matches_oracle(shape, halo_knob):
     check_full(cp, run_conv(cp, alpha=1.25, beta=0.5, act="relu"), alpha=1.25, beta=0.5, act="relu")
 
 
+@pytest.mark.parametrize("tail", [0, 1], ids=["halves", "whole"])
+@pytest.mark.parametrize("K", [256, 192])
+def test_conv_halo_path_half_and_whole_tiles(K, tail, halo_knob):
+    """Few tiles on many pairs: the default walk splits every tile into two
+    halves of 128 output channels (K = 192: the second half only 64 wide);
+    tail = 1 keeps whole tiles."""
+    halo_knob(1)
+    ttc.ttc_set_knob("pair_tail", tail)
+    try:
+        cp = synth.ConvProblem(3, 14, 15, 64, K, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=80 + K,
+                               with_c=True, dist_bias="uniform")
+        check_full(cp, run_conv(cp, alpha=0.5, beta=1.0, act="relu"), alpha=0.5, beta=1.0, act="relu")
+    finally:
+        ttc.ttc_set_knob("pair_tail", 0)
+
+
 @pytest.mark.parametrize("act", ["none", "gelu_tanh"])
 def test_conv_halo_path_f16_and_epilogue(act, halo_knob):
     halo_knob(1)

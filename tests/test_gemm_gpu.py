@@ -24,7 +24,7 @@ def _built():
     _build.build()
     ttc.load()
     for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab",
-              "split_k", "pair_tile_n"):
+              "split_k", "pair_tile_n", "pair_tail", "conv_halo"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -288,16 +288,38 @@ def test_int8_8192_sampled_and_freivalds():
 
 # ------------------------------------------------------------------ single-CTA vs CTA-pair kernels
 
-@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+@pytest.mark.parametrize("pair", [1, 2, 3], ids=["pair", "single", "pair-whole-tiles"])
 @pytest.mark.parametrize("la,lb", synth.MAJORNESS)
 def test_pair_and_single_kernels(pair, la, lb):
-    ttc.ttc_set_knob("pair", pair)
+    """9 pair tiles: on the pair kernel as 18 half tiles (the default for a
+    problem of at most half a wave) or as whole tiles."""
+    ttc.ttc_set_knob("pair", 1 if pair == 3 else pair)
+    ttc.ttc_set_knob("pair_tail", 1 if pair == 3 else 0)
     try:
         p = synth.Problem(520, 600, 264, dtype="bf16", layoutA=la, layoutB=lb, seed=24, distC="uniform",
                           dist_bias="normal:0.5")
         d = run(p, 0.75, 1.5, "gelu_tanh")
         check_full(p, d, 0.75, 1.5, "gelu_tanh")
     finally:
+        ttc.ttc_set_knob("pair_tail", 0)
+        ttc.ttc_set_knob("pair", 0)
+
+
+@pytest.mark.parametrize("tail", [0, 1], ids=["halves", "whole"])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_pair_kernel_last_wave_halves(tail, la, lb):
+    """80 pair tiles (10 x 8, ragged in M and N): on 76 resident pairs the
+    last 4 run as 8 half tiles (tail = 0) or whole (tail = 1); the second half
+    of the last tile column lies partly past N."""
+    ttc.ttc_set_knob("pair", 1)
+    ttc.ttc_set_knob("pair_tail", tail)
+    try:
+        p = synth.Problem(2500, 2000, 192, dtype="bf16", layoutA=la, layoutB=lb, seed=26, distC="uniform",
+                          dist_bias="normal:0.5")
+        d = run(p, 1.25, 0.5, "gelu_tanh")
+        check_full(p, d, 1.25, 0.5, "gelu_tanh")
+    finally:
+        ttc.ttc_set_knob("pair_tail", 0)
         ttc.ttc_set_knob("pair", 0)
 
 

@@ -34,6 +34,11 @@ struct ConvHaloParams {
   uint32_t halo_tx;   // bytes of one halo box
   uint32_t halo_bytes;  // its shared-memory footprint, a multiple of 1024
   int stages;         // filter ring depth (<= kHaloMaxStages)
+  // work units [0, num_units) walk the tiles; units from tail_from on are
+  // half tiles (the left or right half of the output channels of tile
+  // tail_from + (u - tail_from) / 2): a last partial wave keeps twice as many
+  // pairs busy for half as long.  tail_from == num_units: whole tiles.
+  int tail_from, num_units;
 };
 
 // Bytes of dynamic shared memory the kernel needs (plus 1024 for alignment).

@@ -18,6 +18,10 @@
 // last image pairs with an image past the end, whose box reads zeros and whose
 // rows are not stored.
 //
+// The pairs walk work units: whole tiles, then, for a last partial wave, half
+// tiles of BN / 2 output channels (MMAs with N = BN / 2; each CTA uses the
+// first rows of its usual filter box).
+//
 // Synchronisation, in addition to the pair kernel's (full/empty ring for the
 // filter operand, tmem_full/tmem_empty for the two accumulators):
 //   hfull[h]   even CTA only; its producer arms it with both CTAs' halo bytes.
@@ -35,7 +39,17 @@ struct HaloTile {
   int img;  // this CTA's image
 };
 
-__device__ __forceinline__ HaloTile halo_tile(const ConvHaloParams& hp, int t, uint32_t rank) {
+// Tile of work unit u (see ConvHaloParams::tail_from); n_off and half give the
+// unit's first output channel inside the tile and whether it is a half.
+__device__ __forceinline__ HaloTile halo_tile(const ConvHaloParams& hp, int u, uint32_t rank, int half_cols,
+                                              int& n_off, bool& half) {
+  half = u >= hp.tail_from;
+  int t = u;
+  n_off = 0;
+  if (half) {
+    t = hp.tail_from + ((u - hp.tail_from) >> 1);
+    n_off = ((u - hp.tail_from) & 1) * half_cols;
+  }
   HaloTile h;
   h.nb = t % hp.n_blocks;
   const int rest = t / hp.n_blocks;
@@ -150,11 +164,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0, hphase = 0;
       uint32_t armed_mask = 0, armed_parity = 0, harmed_mask = 0, harmed_parity = 0;
       bool ok = true;
-      for (int t = pair; ok && t < hp.num_tiles; t += num_pairs) {
-        const HaloTile ht = halo_tile(hp, t, rank);
+      for (int u = pair; ok && u < hp.num_units; u += num_pairs) {
+        int n_off;
+        bool half;
+        const HaloTile ht = halo_tile(hp, u, rank, BN / 2, n_off, half);
         const int l0 = ht.j * kBM;
         const int hrow = l0 / hp.wp;  // first output row of the tile
-        const int n0 = ht.nb * BN + (int)rank * kBHalf;
+        // this CTA's filters: a half unit uses the first kBHalf / 2 rows of the usual box
+        const int n0 = ht.nb * BN + n_off + (int)rank * (half ? kBHalf / 2 : kBHalf);
         for (int cb = 0; ok && cb < hp.cblk; ++cb) {
           if (!mbar_wait(&hempty[hb], hphase ^ 1u, wc)) {
             ok = false;
@@ -201,7 +218,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (leader && lane == 0) {
-      const uint32_t idesc = idesc_f16(kBF16, false, false, 2 * kBM, BN);
+      const uint32_t idesc_full = idesc_f16(kBF16, false, false, 2 * kBM, BN);
+      const uint32_t idesc_half = idesc_f16(kBF16, false, false, 2 * kBM, BN / 2);
       // descriptors are built once and stepped: the start address is a 14-bit
       // field at bit 0 (address >> 4) that no shared-memory offset overflows,
       // so +2 is one 16-deep k-step (32 bytes), +8 one 128-byte row
@@ -215,14 +233,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       int stage = 0, hb = 0;
       uint32_t phase = 0, hphase = 0;
       int it = 0;
-      for (int t = pair; ok && t < hp.num_tiles; t += num_pairs, ++it) {
+      for (int u = pair; ok && u < hp.num_units; u += num_pairs, ++it) {
         const int acc = it & 1;
         if (!mbar_wait_cluster(&tmem_empty[acc], ((it >> 1) & 1) ^ 1u, wc)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const HaloTile ht = halo_tile(hp, t, rank);
+        int n_off;
+        bool half;
+        const HaloTile ht = halo_tile(hp, u, rank, BN / 2, n_off, half);
+        const uint32_t idesc = half ? idesc_half : idesc_full;
         const int l0 = ht.j * kBM;
         const int off = l0 - (l0 / hp.wp) * hp.wp;  // the tile's first position inside its halo row
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -278,9 +299,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint8_t* sbuf = sEpi + (warp - 2) * kHaloEpiBufBytes;
     int it = 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    for (int t = pair; t < hp.num_tiles; t += num_pairs, ++it) {
+    for (int u = pair; u < hp.num_units; u += num_pairs, ++it) {
       const int acc = it & 1;
-      const HaloTile ht = halo_tile(hp, t, rank);
+      int n_off;
+      bool half;
+      const HaloTile ht = halo_tile(hp, u, rank, BN / 2, n_off, half);
       const int pos0 = ht.j * kBM + q * 32;  // the warp's first position
       const int m = halo_out_row(hp, ht.img, pos0 + lane);
       const bool row_ok = m >= 0;
@@ -288,14 +311,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll
       for (int s4 = 0; s4 < 4; ++s4) out_row[s4] = halo_out_row(hp, ht.img, pos0 + s4 * 8 + (lane >> 2));
       const int grow = row_ok ? m : p.M;  // past the end: C reads nothing for it
-      const int n0 = ht.nb * BN;
-      const int chunks = min(BN, p.N - n0) / kEpiCols;
+      const int n0 = ht.nb * BN + n_off;
+      const int chunks = max(0, min(half ? BN / 2 : BN, p.N - n0)) / kEpiCols;
       const EpiPtrs ep = epi_ptrs(p, 0, 2);
       const int cpath = p.beta != 0.0f ? kCVec : kCNone;
       CChunk16 cc;
       c_fetch16(p, ep, cpath, grow, n0, lane, cc);
       if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
       tc_fence_after();
+      if (chunks == 0) {
+        // nothing of this unit is stored: release the accumulator at once
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < chunks; ++c) {
         const int gcol0 = n0 + c * kEpiCols;

@@ -38,6 +38,7 @@ std::atomic<int> g_split_k{0};
 std::atomic<int> g_pair_tile_n{0};
 std::atomic<int> g_group_m{0};
 std::atomic<int> g_conv_halo{0};
+std::atomic<int> g_pair_tail{0};
 std::atomic<int> g_gemv_off{0};
 std::atomic<int64_t> g_launches{0};
 
@@ -250,6 +251,36 @@ HaloPlan plan_halo(int64_t P, int64_t Q, int64_t K, int64_t R, int64_t S, int64_
   return h;
 }
 
+// CTA pairs to launch for `tiles` tiles with `clusters` pairs resident, and
+// the work units they walk: a last partial wave of R tiles whose halves fit
+// in one wave (2 R <= pairs) runs as 2 R half tiles, as does a problem of at
+// most half a wave.  Units from tail_from on are halves.
+int split_last_wave(int tiles, int clusters, bool split, int& tail_from, int& num_units) {
+  tail_from = tiles;
+  num_units = tiles;
+  split = split && g_pair_tail.load() == 0;
+  if (tiles < clusters) {
+    if (split && 2 * tiles <= clusters) {
+      tail_from = 0;
+      num_units = 2 * tiles;
+      return 2 * tiles;
+    }
+    return tiles;
+  }
+  const int rest = tiles % clusters;
+  if (split && rest > 0 && 2 * rest <= clusters) {
+    tail_from = tiles - rest;
+    num_units = tiles + rest;
+  }
+  return clusters;
+}
+
+// The GEMM pair kernel's walk.  Only 256-wide pair tiles are halved, so a
+// CTA's half of B is one whole 64-column slab when B is MN-major.
+int plan_pair_units(GemmParams& prm, int pbn, int clusters) {
+  return split_last_wave(prm.num_tiles, clusters, pbn == 256, prm.tail_from, prm.num_units);
+}
+
 template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
@@ -394,6 +425,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
     case TTC_KNOB_GEMV:
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_gemv_off.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_PAIR_TAIL:
+      if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
+      g_pair_tail.store((int)value);
       return TTC_OK;
     case TTC_KNOB_CONV_HALO:
       if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
@@ -752,7 +787,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       prm.num_tiles = (int)batch * prm.tiles_per_batch;
       const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
-      const int nclus = prm.num_tiles < clusters ? prm.num_tiles : clusters;
+      const int nclus = plan_pair_units(prm, pbn, clusters);
       prm.a_stream = prm.num_n_blocks == 1;
       prm.b_stream = prm.num_m_blocks == 1;
       if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
@@ -950,7 +985,7 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
         hp.halo_tx = hpn.tx;
         hp.halo_bytes = hpn.bytes;
         hp.stages = hpn.stages;
-        const int nclus = hp.num_tiles < cl ? hp.num_tiles : cl;
+        const int nclus = split_last_wave(hp.num_tiles, cl, hpn.bn == 256, hp.tail_from, hp.num_units);
         if (launch_conv_halo(bf16, hpn.bn, hp, hpn.smem, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
           return TTC_ERR_CUDA;
         g_launches.fetch_add(1);
@@ -983,7 +1018,7 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
       prm.num_tiles = prm.tiles_per_batch;
       const int gmp = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gmp ? prm.num_m_blocks : gmp;
-      const int nclus = prm.num_tiles < pc.clusters ? prm.num_tiles : pc.clusters;
+      const int nclus = plan_pair_units(prm, pc.bn, pc.clusters);
       if (launch_pair(bf16, pc.bn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TTC_ERR_CUDA;
       g_launches.fetch_add(1);

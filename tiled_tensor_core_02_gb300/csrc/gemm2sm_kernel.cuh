@@ -20,6 +20,11 @@
 //                odd CTA's remotely); the MMA waits before reusing accumulator a.
 // The layout of a CTA's half tiles, the epilogue and the error handling are
 // those of gemm_kernel (one CTA); every wait is bounded.
+//
+// The pairs walk work units (GemmParams::num_units): whole tiles, then, for
+// a last partial wave, half tiles of N = BN / 2 columns.  A half unit issues
+// MMAs with N = BN / 2, and each CTA uses the first BN / 4 columns of its
+// usual B box, which it loads starting at its own columns.
 #pragma once
 #include "gemm_kernel.cuh"
 
@@ -118,12 +123,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       uint32_t phase = 0;
       uint32_t armed_mask = 0, armed_parity = 0;
       bool ok = true;
-      for (int t = pair; ok && t < p.num_tiles; t += num_pairs) {
+      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
+        int t, n_off;
+        bool half;
+        pair_unit(p, u, kPairBN / 2, t, n_off, half);
         int bz, mb, nb;
         tile_coords(t, p, bz, mb, nb);
         const int za = bz * p.a_bc, zb = bz * p.b_bc;
         const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
-        const int n0 = nb * kPairBN + (int)rank * PairCfg::kBHalf;  // this CTA's B columns
+        // this CTA's B columns: a half unit uses the first kBHalf / 2 of the
+        // usual box (the rest is loaded and not read)
+        const int n0 = nb * kPairBN + n_off + (int)rank * (half ? PairCfg::kBHalf / 2 : PairCfg::kBHalf);
         // convolution: window corner of output pixel m0 (rows past the end start
         // beyond the last image, where the im2col box reads zeros)
         int cv_n = 0, cv_h0 = 0, cv_w0 = 0;
@@ -185,7 +195,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
     if (leader && lane == 0) {
-      const uint32_t idesc = idesc_f16(kBF16, p.a_mn != 0, p.b_mn != 0, kPairBM, kPairBN);
+      const uint32_t idesc_full = idesc_f16(kBF16, p.a_mn != 0, p.b_mn != 0, kPairBM, kPairBN);
+      const uint32_t idesc_half = idesc_f16(kBF16, p.a_mn != 0, p.b_mn != 0, kPairBM, kPairBN / 2);
       bool ok = true;
       bool any_mma = false;
       if (p.inject_stall) ok = mbar_wait(stall_bar, 0, wc);  // nothing arrives here
@@ -197,7 +208,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), p.a_mn ? 8192u : 16u, 1024);
       const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), p.b_mn ? 8192u : 16u, 1024);
       const uint64_t a_kstep = p.a_mn ? 2048u >> 4 : 32u >> 4, b_kstep = p.b_mn ? 2048u >> 4 : 32u >> 4;
-      for (int t = pair; ok && t < p.num_tiles; t += num_pairs, ++it) {
+      for (int u = pair; ok && u < p.num_units; u += num_pairs, ++it) {
+        const uint32_t idesc = u >= p.tail_from ? idesc_half : idesc_full;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
@@ -247,22 +259,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int it = 0;
     const bool has_k = p.num_k_blocks > 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    for (int t = pair; t < p.num_tiles; t += num_pairs, ++it) {
+    // this thread's row of a tile's C, toward L2 one tile ahead of its epilogue
+    // (the first tile's during the first mainloop)
+    auto prefetch_c = [&](int unit) {
+      if (unit >= p.num_units || p.beta == 0.0f) return;
+      int pt, pn_off;
+      bool phalf;
+      pair_unit(p, unit, kPairBN / 2, pt, pn_off, phalf);
+      int pbz, pmb, pnb;
+      tile_coords(pt, p, pbz, pmb, pnb);
+      c_prefetch_row(p, epi_ptrs(p, pbz, 2), pmb * kPairBM + (int)rank * 128 + q * 32 + lane,
+                     pnb * kPairBN + pn_off, phalf ? kPairBN / 2 : kPairBN);
+    };
+    prefetch_c(pair);
+    for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
+      int t, n_off;
+      bool half;
+      pair_unit(p, u, kPairBN / 2, t, n_off, half);
+      const int chunks = (half ? kPairBN / 2 : kPairBN) / kEpiCols;
       const int acc = it & 1;
       int bz, mb, nb;
       tile_coords(t, p, bz, mb, nb);
       const int m0 = mb * kPairBM + (int)rank * 128;
-      const int n0 = nb * kPairBN;
+      const int n0 = nb * kPairBN + n_off;
       const int grow = m0 + q * 32 + lane;
       const bool row_ok = grow < p.M;
       const EpiPtrs ep = epi_ptrs(p, bz, 2);
+      prefetch_c(u + num_pairs);
       // the first chunk's C is fetched before waiting for the accumulator
       CChunk16 cc;
       c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
       if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
       tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < kPairBN / kEpiCols; ++c) {
+      for (int c = 0; c < chunks; ++c) {
         const int gcol0 = n0 + c * kEpiCols;
         uint32_t r[32];
         if (has_k) {
@@ -272,7 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        if (c == kPairBN / kEpiCols - 1) {
+        if (c == chunks - 1) {
           // this warp's accumulator rows are read: tell the even CTA's issuer
           tc_fence_before();
           __syncwarp();
@@ -282,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int cpath = c_path(p, ep, gcol0);
         uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, PairCfg::kEpiBufBytes, lane);
         epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
-        if (c + 1 < kPairBN / kEpiCols)
+        if (c + 1 < chunks)
           c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
         epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane,
                            ep);

@@ -130,7 +130,25 @@ struct GemmParams {
   // row for B), so its TMA loads carry an evict-first L2 hint; otherwise
   // evict-last keeps it for the other tiles that read it
   int a_stream, b_stream;
+  // CTA-pair kernel: work units [0, num_units) walk the tiles; units from
+  // tail_from on are half tiles (the left or right half of the columns of tile
+  // tail_from + (u - tail_from) / 2), so that a last, partial wave keeps twice
+  // as many pairs busy for half as long.  tail_from == num_units: whole tiles.
+  int tail_from, num_units;
 };
+
+// Tile and column offset of work unit u of the CTA-pair walk (see tail_from).
+__device__ __forceinline__ void pair_unit(const GemmParams& p, int u, int half_cols, int& t, int& n_off, bool& half) {
+  half = u >= p.tail_from;
+  if (!half) {
+    t = u;
+    n_off = 0;
+  } else {
+    const int h = u - p.tail_from;
+    t = p.tail_from + (h >> 1);
+    n_off = (h & 1) * half_cols;
+  }
+}
 
 template <int BN, int MODE>
 struct TileCfg {
@@ -445,6 +463,19 @@ __device__ __forceinline__ int c_path(const GemmParams& p, const EpiPtrs& e, int
   const bool vec =
       ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(e.C) & 15) == 0) && (gcol0 + 32 <= p.N);
   return vec ? kCVec : kCCoop;
+}
+
+// Pulls row `grow` of a tile's C, columns [n0, n0 + ncols), toward L2 ahead of
+// the tile's epilogue (16-bit C in the row-major orientation).  The range is
+// trimmed inward to 16-byte boundaries, so it never leaves the row.
+__device__ __forceinline__ void c_prefetch_row(const GemmParams& p, const EpiPtrs& e, int grow, int n0, int ncols) {
+  if (p.beta == 0.0f || p.d_trans || grow >= p.M) return;
+  const int n1 = min(n0 + ncols, p.N);
+  if (n1 <= n0) return;
+  const uint16_t* row = static_cast<const uint16_t*>(e.C) + (int64_t)grow * p.ldc;
+  const uintptr_t a0 = (reinterpret_cast<uintptr_t>(row + n0) + 15) & ~uintptr_t(15);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(row + n1) & ~uintptr_t(15);
+  if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
 }
 
 // C values of one chunk, fetched one chunk ahead of their use so that the
