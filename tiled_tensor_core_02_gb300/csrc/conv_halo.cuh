@@ -8,6 +8,10 @@
 namespace ttc {
 
 constexpr int kHaloMaxStages = 8;
+// k-blocks (one filter tap of one 64-channel block each) per filter stage:
+// one full/empty round trip per 8 MMAs keeps the tensor pipe fed, one per 4
+// does not (measured on GB300)
+constexpr int kHaloKPS = 2;
 constexpr int kHaloEpiBufBytes = 32 * kEpiCols * 2;  // one warp's 32 x 32 staging block
 constexpr int kHaloEpiBytes = kEpiWarps * kHaloEpiBufBytes;
 constexpr int kHaloBarBytes = 256;
@@ -33,7 +37,7 @@ struct ConvHaloParams {
   int halo_rows;      // input rows per halo box
   uint32_t halo_tx;   // bytes of one halo box
   uint32_t halo_bytes;  // its shared-memory footprint, a multiple of 1024
-  int stages;         // filter ring depth (<= kHaloMaxStages)
+  int stages;         // filter ring depth in stages of kHaloKPS k-blocks (<= kHaloMaxStages)
   // work units [0, num_units) walk the tiles; units from tail_from on are
   // half tiles (the left or right half of the output channels of tile
   // tail_from + (u - tail_from) / 2): a last partial wave keeps twice as many
@@ -43,7 +47,7 @@ struct ConvHaloParams {
 
 // Bytes of dynamic shared memory the kernel needs (plus 1024 for alignment).
 __host__ __device__ constexpr int conv_halo_smem_bytes(int halo_bytes, int stages, int b_half_bytes) {
-  return 1024 + 2 * halo_bytes + stages * b_half_bytes + kHaloEpiBytes + kHaloBarBytes;
+  return 1024 + 2 * halo_bytes + stages * kHaloKPS * b_half_bytes + kHaloEpiBytes + kHaloBarBytes;
 }
 
 // Largest number of CTA pairs resident at once for tile width `bn` (0 on error).

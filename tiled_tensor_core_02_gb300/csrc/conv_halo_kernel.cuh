@@ -104,7 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sH = smem;  // two halo buffers of hp.halo_bytes
   uint8_t* sB = sH + 2 * hp.halo_bytes;
-  uint8_t* sEpi = sB + S * kBHalfBytes;
+  uint8_t* sEpi = sB + S * kHaloKPS * kBHalfBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + kHaloEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kHaloMaxStages;
@@ -188,18 +188,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             hb = 0;
             hphase ^= 1u;
           }
-          for (int tap = 0; tap < hp.taps; ++tap) {
+          // the block's taps, kHaloKPS per stage (the last stage may hold fewer)
+          for (int t0 = 0; t0 < hp.taps; t0 += kHaloKPS) {
+            const int nkb = min(kHaloKPS, hp.taps - t0);
             if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
               break;
             }
             if (leader) {
-              mbar_arrive_expect_tx(&full[stage], 2 * kBHalfBytes);
+              mbar_arrive_expect_tx(&full[stage], 2 * nkb * kBHalfBytes);
               armed_mask |= 1u << stage;
               armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
             }
-            tma_load_3d_pair(sB + stage * kBHalfBytes, &p.tmB, tap * hp.c + cb * kBK, n0, 0,
-                             mapa_shared(smem_u32(&full[stage]), 0), pol_w);
+            for (int j = 0; j < nkb; ++j)
+              tma_load_3d_pair(sB + (stage * kHaloKPS + j) * kBHalfBytes, &p.tmB, (t0 + j) * hp.c + cb * kBK, n0, 0,
+                               mapa_shared(smem_u32(&full[stage]), 0), pol_w);
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
@@ -256,26 +259,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           // tap (r, s) starts r row_step + s dw rows past the tile's first position
           uint64_t ad = desc0 + ((smem_u32(sH + hb * hp.halo_bytes) + (uint32_t)off * 128u) >> 4);
           int fs = 0;
-          for (int tap = 0; tap < hp.taps; ++tap) {
+          for (int t0 = 0; t0 < hp.taps; t0 += kHaloKPS) {
+            const int nkb = min(kHaloKPS, hp.taps - t0);
             if (!mbar_wait(&full[stage], phase, wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t bd = b_desc0 + (uint32_t)stage * (kBHalfBytes >> 4);
-            mma_f16_pair(d_tmem, ad, bd, idesc, (cb | tap) != 0);
 #pragma unroll
-            for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
+            for (int j = 0; j < kHaloKPS; ++j) {
+              if (j < nkb) {
+                const uint64_t bd = b_desc0 + (uint32_t)(stage * kHaloKPS + j) * (kBHalfBytes >> 4);
+                mma_f16_pair(d_tmem, ad, bd, idesc, (cb | t0 | j) != 0);
+#pragma unroll
+                for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_pair(d_tmem, ad + 2 * k, bd + 2 * k, idesc, 1u);
+                ad += a_tap_step;
+                if (++fs == hp.s) {
+                  fs = 0;
+                  ad += a_row_step;
+                }
+              }
+            }
             any_mma = true;
             mma_commit_pair(&empty[stage], 0x3);
             if (++stage == S) {
               stage = 0;
               phase ^= 1u;
-            }
-            ad += a_tap_step;
-            if (++fs == hp.s) {
-              fs = 0;
-              ad += a_row_step;
             }
           }
           if (!ok) break;

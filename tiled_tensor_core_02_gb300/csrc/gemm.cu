@@ -215,7 +215,7 @@ bool encode_halo(CUtensorMap* m, CUtensorMapDataType dt, const void* X, int64_t 
 // Plan of the halo convolution for a unit-stride problem, or ok == false when
 // its shape does not fit the kernel: a padded output row of at most 256
 // positions, a halo box of at most 256 rows, and two halo buffers plus at
-// least three filter stages in shared memory.
+// least two filter stages in shared memory.
 struct HaloPlan {
   bool ok = false;
   int bn = 0, wp = 0, rows = 0, tiles_per_img = 0, stages = 0, smem = 0;
@@ -240,8 +240,8 @@ HaloPlan plan_halo(int64_t P, int64_t Q, int64_t K, int64_t R, int64_t S, int64_
   h.tx = (uint32_t)(rows * wp * kBK * 2);
   h.bytes = (h.tx + 1023u) / 1024u * 1024u;
   const int64_t room = 227 * 1024 - conv_halo_smem_bytes((int)h.bytes, 0, b_half);
-  const int64_t stages = room / b_half;
-  if (stages < 3) return h;
+  const int64_t stages = room / (kHaloKPS * b_half);
+  if (stages < 2) return h;
   h.stages = (int)(stages < kHaloMaxStages ? stages : kHaloMaxStages);
   h.smem = conv_halo_smem_bytes((int)h.bytes, h.stages, b_half);
   h.wp = (int)wp;

@@ -34,13 +34,18 @@ constexpr int kPairBM = 256;
 constexpr int kPairThreads = 192;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..5 epilogue
 
 // Pair tile 256 x BN (BN = 256, 192 or 128): each CTA stages 128 A rows and
-// BN / 2 B columns per k-block.
+// BN / 2 B columns per k-block.  A pipeline stage holds kKPS = 2 k-blocks
+// (128 of K, 8 MMAs per barrier round trip): measured on GB300, one full/empty
+// round trip per 4 MMAs holds the pair to ~85 ns per N = 256 MMA, one per 8
+// MMAs to the tensor pipe's own ~67 ns, with as few as 2 stages.
 template <int BN>
 struct PairCfg {
   static constexpr int kBHalf = BN / 2;
-  static constexpr int kAHalfBytes = 128 * kBK * 2;     // 16 KiB
-  static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // 16 / 12 / 8 KiB
-  static constexpr int kStageBytes = kAHalfBytes + kBHalfBytes;
+  static constexpr int kKPS = 2;                        // k-blocks per stage
+  static constexpr int kAHalfBytes = 128 * kBK * 2;     // one k-block of A rows: 16 KiB
+  static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // one k-block of B columns: 16 / 12 / 8 KiB
+  static constexpr int kKBlockBytes = kAHalfBytes + kBHalfBytes;
+  static constexpr int kStageBytes = kKPS * kKBlockBytes;
   static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
   static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kBarBytes = 256;
@@ -50,7 +55,7 @@ struct PairCfg {
   static constexpr int kTmemCols = 2 * BN > 256 ? 512 : 256;  // two accumulators, a power of two
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
   static_assert(BN == 256 || BN == 192 || BN == 128, "pair tile width");
-  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
@@ -62,9 +67,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   constexpr int S = PairCfg::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + S * PairCfg::kAHalfBytes;
-  uint8_t* sEpi = sB + S * PairCfg::kBHalfBytes;
+  constexpr int KPS = PairCfg::kKPS;
+  uint8_t* sA = smem;  // [stage][k-block of the stage][128 rows x 64]
+  uint8_t* sB = sA + S * KPS * PairCfg::kAHalfBytes;
+  uint8_t* sEpi = sB + S * KPS * PairCfg::kBHalfBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(sEpi + PairCfg::kEpiBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
@@ -145,39 +151,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           cv_h0 = pp * p.cv_sh - p.cv_ph;
           cv_w0 = (rem - pp * p.cv_q) * p.cv_sw - p.cv_pw;
         }
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += KPS) {
+          const int nkb = min(KPS, p.num_k_blocks - kb0);
           if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) {
-            mbar_arrive_expect_tx(&full[stage], 2 * PairCfg::kStageBytes);
+            mbar_arrive_expect_tx(&full[stage], 2 * nkb * PairCfg::kKBlockBytes);
             armed_mask |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
-          uint8_t* a = sA + stage * PairCfg::kAHalfBytes;
-          uint8_t* b = sB + stage * PairCfg::kBHalfBytes;
-          const int k0 = kb * kBK;
-          if (p.cv_tma) {
-            const int tap = kb / p.cv_cblk;
-            const int c0 = (kb - tap * p.cv_cblk) * kBK;
-            const int rr = tap / p.cv_s;
-            const int ss = tap - rr * p.cv_s;
-            tma_load_im2col_4d_pair(a, &p.tmA, c0, cv_w0, cv_h0, cv_n, (uint16_t)(ss * p.cv_dw),
-                                    (uint16_t)(rr * p.cv_dh), full_leader, pol_a);
-          } else if (!p.a_mn) {
-            tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol_a);
-          } else {
-            tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol_a);
-            tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol_a);
-          }
-          if (!p.b_mn) {
-            tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol_b);
-          } else {
+          for (int j = 0; j < nkb; ++j) {
+            const int kb = kb0 + j;
+            uint8_t* a = sA + (stage * KPS + j) * PairCfg::kAHalfBytes;
+            uint8_t* b = sB + (stage * KPS + j) * PairCfg::kBHalfBytes;
+            const int k0 = kb * kBK;
+            if (p.cv_tma) {
+              const int tap = kb / p.cv_cblk;
+              const int c0 = (kb - tap * p.cv_cblk) * kBK;
+              const int rr = tap / p.cv_s;
+              const int ss = tap - rr * p.cv_s;
+              tma_load_im2col_4d_pair(a, &p.tmA, c0, cv_w0, cv_h0, cv_n, (uint16_t)(ss * p.cv_dw),
+                                      (uint16_t)(rr * p.cv_dh), full_leader, pol_a);
+            } else if (!p.a_mn) {
+              tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol_a);
+            } else {
+              tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol_a);
+              tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol_a);
+            }
+            if (!p.b_mn) {
+              tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol_b);
+            } else {
 #pragma unroll
-            for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
-              tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol_b);
+              for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
+                tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol_b);
+            }
           }
           if (++stage == S) {
             stage = 0;
@@ -218,17 +228,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * kPairBN;
-        for (int kb = 0; kb < p.num_k_blocks; ++kb) {
+        for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += KPS) {
+          const int nkb = min(KPS, p.num_k_blocks - kb0);
           if (!mbar_wait(&full[stage], phase, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t ad = a_desc0 + (uint32_t)stage * (PairCfg::kAHalfBytes >> 4);
-          const uint64_t bd = b_desc0 + (uint32_t)stage * (PairCfg::kBHalfBytes >> 4);
-          mma_f16_pair(d_tmem, ad, bd, idesc, kb != 0);
 #pragma unroll
-          for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+          for (int j = 0; j < KPS; ++j) {
+            if (j < nkb) {
+              const uint64_t ad = a_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kAHalfBytes >> 4);
+              const uint64_t bd = b_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kBHalfBytes >> 4);
+              mma_f16_pair(d_tmem, ad, bd, idesc, (kb0 | j) != 0);
+#pragma unroll
+              for (int k = 1; k < kBK / kUmmaK; ++k)
+                mma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+            }
+          }
           any_mma = true;
           mma_commit_pair(&empty[stage], 0x3);
           if (++stage == S) {
