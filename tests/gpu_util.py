@@ -38,9 +38,15 @@ def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_d
     if workspace is None:
         st = ttc.ttc_gemm(*args, s)
     else:
-        # workspace: bytes to allocate (-1: exactly what the library asks for)
-        need = ttc.ttc_gemm_workspace_size(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
-                                           B.data_ptr(), p.ldb, LAY[p.layoutB], ttc.DTYPE[p.dtype])
+        # workspace: bytes to allocate (-1: what the library asks for the
+        # operand repack; -2: for the repack and an aligned copy of D)
+        if workspace == -2:
+            need = ttc.ttc_gemm_workspace_size_staged(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
+                                                      B.data_ptr(), p.ldb, LAY[p.layoutB], D.data_ptr(), ldd,
+                                                      ttc.DTYPE[p.dtype])
+        else:
+            need = ttc.ttc_gemm_workspace_size(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
+                                               B.data_ptr(), p.ldb, LAY[p.layoutB], ttc.DTYPE[p.dtype])
         nbytes = need if workspace < 0 else workspace
         ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device="cuda")
         st = ttc.ttc_gemm_ws(*args, ws.data_ptr() if nbytes else None, nbytes, s)

@@ -416,19 +416,37 @@ def test_split_k_generic_producer_and_swap():
 
 # ------------------------------------------------------------------ ttc_gemm_ws: repacked operands
 
+@pytest.mark.parametrize("ws", [-1, -2], ids=["repack", "repack+D"])
 @pytest.mark.parametrize("shape", synth.RAGGED_SHAPES, ids=lambda s: "x".join(map(str, s)))
 @pytest.mark.parametrize("la,lb", synth.MAJORNESS)
-def test_ragged_sweep_with_workspace(shape, la, lb):
+def test_ragged_sweep_with_workspace(shape, la, lb, ws):
     p, a, b, act = synth.make(synth.ragged_workload(*shape, la, lb))
-    d = run(p, a, b, act, workspace=-1)
+    d = run(p, a, b, act, workspace=ws)
     check_full(p, d, a, b, act)
 
 
-def test_workspace_int8_odd_pitch():
+@pytest.mark.parametrize("ws", [-1, -2], ids=["repack", "repack+D"])
+def test_workspace_int8_odd_pitch(ws):
+    """Odd operand pitches; with the staged size the int32 D (pitch 203, rows
+    not 16-byte aligned) and C are staged through an aligned copy too."""
     p = synth.Problem(300, 200, 72, dtype="i8", layoutA="row", layoutB="col", seed=31, distA="int8",
-                      distB="int8", lda=73, ldb=75)
-    d = run(p, 1.0, 0.0, workspace=-1)
-    check_full(p, d, 1.0, 0.0)
+                      distB="int8", lda=73, ldb=75, distC="int8")
+    d = run(p, 1.0, 1.0, workspace=ws, ldd=203)
+    check_full(p, d, 1.0, 1.0)
+
+
+@pytest.mark.parametrize("beta", [0.0, 1.0])
+def test_workspace_staged_d_in_place_and_padding(beta):
+    """D staged through the workspace: C == D in place at an odd pitch, and
+    the pitch padding of D left untouched."""
+    p = synth.Problem(260, 301, 96, dtype="bf16", layoutA="col", layoutB="row", seed=34, distC="uniform",
+                      lda=261, ldb=303, ldc=305)
+    D = to_dev(p.C.copy())  # C and D share storage, pitch 305
+    d = run(p, 1.5, beta, "relu", D=D, C_dev=D, ldd=305, workspace=-2)
+    check_full(p, d, 1.5, beta, "relu")
+    full = D.cpu().numpy().view(np.uint16).reshape(-1)
+    rows = full[: p.M * 305].reshape(p.M, 305)
+    assert np.array_equal(rows[:, p.N:], p.C.reshape(-1)[: p.M * 305].reshape(p.M, 305)[:, p.N:])
 
 
 def test_workspace_too_small_falls_back():

@@ -33,6 +33,7 @@ KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_gene
 
 # Every symbol the C header declares (checked by the test suite).
 EXPORTS = ("ttc_gemm", "ttc_gemm_strided_batched", "ttc_gemm_ws", "ttc_gemm_workspace_size",
+           "ttc_gemm_workspace_size_staged",
            "ttc_gemm_static_scratch", "ttc_transpose", "ttc_conv2d_fprop",
            "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
 
@@ -75,6 +76,8 @@ def load():
     L.ttc_gemm_static_scratch.restype = i
     L.ttc_gemm_workspace_size.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, i]
     L.ttc_gemm_workspace_size.restype = ctypes.c_size_t
+    L.ttc_gemm_workspace_size_staged.argtypes = [i64, i64, i64, vp, i64, i, vp, i64, i, vp, i64, i]
+    L.ttc_gemm_workspace_size_staged.restype = ctypes.c_size_t
     L.ttc_get_device_error.argtypes = [vp]
     L.ttc_get_device_error.restype = i
     L.ttc_status_string.argtypes = [i]
@@ -129,6 +132,10 @@ def ttc_gemm_static_scratch(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D
 
 def ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype) -> int:
     return load().ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype)
+
+
+def ttc_gemm_workspace_size_staged(M, N, K, A, lda, layoutA, B, ldb, layoutB, D, ldd, dtype) -> int:
+    return load().ttc_gemm_workspace_size_staged(M, N, K, A, lda, layoutA, B, ldb, layoutB, D, ldd, dtype)
 
 
 def ttc_get_device_error(stream=None) -> int:

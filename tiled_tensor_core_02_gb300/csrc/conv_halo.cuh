@@ -7,6 +7,7 @@
 
 namespace ttc {
 
+constexpr int kHaloThreads = 192;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..5 epilogue
 constexpr int kHaloMaxStages = 8;
 // k-blocks (one filter tap of one 64-channel block each) per filter stage:
 // one full/empty round trip per 8 MMAs keeps the tensor pipe fed, one per 4

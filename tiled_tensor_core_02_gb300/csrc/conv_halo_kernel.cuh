@@ -93,7 +93,7 @@ __device__ __forceinline__ void halo_store_chunk(const ConvHaloParams& hp, const
 }
 
 template <int BN, bool kBF16>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHaloThreads, 1)
     conv_halo_kernel(const __grid_constant__ ConvHaloParams hp) {
   const GemmParams& p = hp.g;
   constexpr int kBHalf = BN / 2;

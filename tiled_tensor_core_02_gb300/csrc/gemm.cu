@@ -367,6 +367,26 @@ RepackPlan plan_repack(int64_t M, int64_t N, int64_t K, const void* A, int64_t l
   return r;
 }
 
+// Aligned copy of D in the workspace, after the operand repack (`after`
+// bytes): used when D's rows cannot take TMA stores (pitch or base not
+// 16-byte aligned).  C is copied into it too, so the GEMM runs in place on
+// aligned rows with TMA stores and vector C loads, and the result is copied
+// back.  off/ld/bytes: its place, pitch (elements) and size.
+struct DStage {
+  bool on = false;
+  int64_t ld = 0;
+  size_t off = 0, bytes = 0;
+};
+DStage plan_dstage(int64_t M, int64_t N, const void* D, int64_t ldd, int esize, size_t after) {
+  DStage d;
+  if (M <= 0 || N <= 0 || tma_ok(D, ldd, esize)) return d;
+  d.on = true;
+  d.ld = round_up(N, 16 / esize);
+  d.off = after;
+  d.bytes = (size_t)round_up(M * d.ld * esize, 256);
+  return d;
+}
+
 }  // namespace
 }  // namespace ttc
 
@@ -556,7 +576,9 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (batch == 1 && workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
       !g_force_generic_load.load()) {
     const RepackPlan rp = plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, in_esize);
-    if (rp.bytes > 0 && rp.bytes <= workspace_bytes) {
+    const bool use_rp = rp.bytes > 0 && rp.bytes <= workspace_bytes;
+    const DStage ds = plan_dstage(M, N, D, ldd, out_esize, use_rp ? rp.bytes : 0);
+    if (use_rp) {
       uint8_t* ws = static_cast<uint8_t*>(workspace);
       cudaStream_t s = static_cast<cudaStream_t>(stream);
       if (rp.a) {
@@ -575,6 +597,22 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
         B = ws + rp.b_off;
         ldb = rp.b_ld;
       }
+    }
+    if (ds.on && ds.off + ds.bytes <= workspace_bytes && !g_force_generic_store.load()) {
+      // D staged: C copied in, the GEMM run in place on aligned rows (the
+      // operands already repacked, so no workspace), the result copied out
+      uint8_t* dst = static_cast<uint8_t*>(workspace) + ds.off;
+      cudaStream_t s = static_cast<cudaStream_t>(stream);
+      if (beta != 0.0f) {
+        if (launch_repack(C, ldc, M, N, dst, ds.ld, out_esize, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+        g_launches.fetch_add(1);
+      }
+      st = gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, beta != 0.0f ? dst : nullptr, ds.ld, dst, ds.ld,
+                     alpha, beta, bias, act, dtype, nullptr, 0, stream);
+      if (st != TTC_OK) return st;
+      if (launch_unpack(dst, ds.ld, M, N, D, ldd, out_esize, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+      g_launches.fetch_add(1);
+      return TTC_OK;
     }
   }
 
@@ -1060,6 +1098,21 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, i
   if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return 0;
   canonicalise(M, N, K, layoutA, lda, layoutB, ldb);
   return plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype == TTC_I8 ? 1 : 2).bytes;
+}
+
+size_t ttc_gemm_workspace_size_staged(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                                      ttc_layout layoutA, const void* B, int64_t ldb, ttc_layout layoutB,
+                                      const void* D, int64_t ldd, ttc_dtype dtype) {
+  if (M <= 0 || N <= 0 || K < 0 || ldd < N) return 0;
+  if ((layoutA != TTC_ROW_MAJOR && layoutA != TTC_COL_MAJOR) || (layoutB != TTC_ROW_MAJOR && layoutB != TTC_COL_MAJOR))
+    return 0;
+  if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return 0;
+  // matrix-vector problems take their own kernel and no workspace
+  const bool gemv = dtype != TTC_I8 && K > 0 &&
+                    ((M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR));
+  if (gemv) return 0;
+  const size_t ab = ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype);
+  return ab + plan_dstage(M, N, D, ldd, dtype == TTC_I8 ? 4 : 2, ab).bytes;
 }
 
 }  // extern "C"

@@ -31,7 +31,7 @@ int max_clusters() {
   if (set_smem_attr<BN, kBF16>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.blockDim = dim3(kHaloThreads, 1, 1);
   cfg.dynamicSmemBytes = kHaloSmemLimit;
   int n = 0;
   return cudaOccupancyMaxActiveClusters(&n, conv_halo_kernel<BN, kBF16>, &cfg) == cudaSuccess ? n : 0;
@@ -42,7 +42,7 @@ cudaError_t launch(const ConvHaloParams& hp, int smem_bytes, int clusters, cudaS
   if (smem_bytes > kHaloSmemLimit) return cudaErrorInvalidValue;
   const cudaError_t e = set_smem_attr<BN, kBF16>();
   if (e != cudaSuccess) return e;
-  conv_halo_kernel<BN, kBF16><<<2 * clusters, kPairThreads, smem_bytes, stream>>>(hp);
+  conv_halo_kernel<BN, kBF16><<<2 * clusters, kHaloThreads, smem_bytes, stream>>>(hp);
   return cudaGetLastError();
 }
 }  // namespace

@@ -6,10 +6,15 @@
 
 namespace ttc {
 
-// Copies `rows` rows of `cols` elements (elem_bytes = 1 or 2), `src_ld`
+// Copies `rows` rows of `cols` elements (elem_bytes = 1, 2 or 4), `src_ld`
 // elements apart, to `dst` with pitch `dst_ld` (a multiple of 16 bytes;
 // `dst` 16-byte aligned).
 cudaError_t launch_repack(const void* src, int64_t src_ld, int64_t rows, int64_t cols, void* dst, int64_t dst_ld,
+                          int elem_bytes, int sm_count, cudaStream_t stream);
+
+// Copies `rows` rows of `cols` elements (elem_bytes = 1, 2 or 4) from `src`
+// (pitch `src_ld`) to `dst` (pitch `dst_ld`), element-aligned at both ends.
+cudaError_t launch_unpack(const void* src, int64_t src_ld, int64_t rows, int64_t cols, void* dst, int64_t dst_ld,
                           int elem_bytes, int sm_count, cudaStream_t stream);
 
 }  // namespace ttc
