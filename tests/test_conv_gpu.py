@@ -225,3 +225,27 @@ def test_conv_halo_declines_what_it_cannot_run(halo_knob):
         cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype="bf16", seed=sum(shape[:7]))
         ldd = kw.get("ldd", K)
         check_full(cp, run_conv(cp, ldd=ldd), ldd=ldd)
+
+
+def test_conv_halo_stalled_pipeline_times_out_and_context_survives(halo_knob):
+    """The halo kernel's tensor-core issuer waits on a barrier nothing arrives
+    at: the launch ends with TTC_ERR_TIMEOUT within the wait budget (the
+    producers drain their halo and filter loads), and the context stays
+    usable."""
+    cp = synth.ConvProblem(2, 10, 10, 64, 128, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=81)
+    halo_knob(1)
+    ttc.ttc_set_knob("timeout_ns", 200_000_000)
+    ttc.ttc_set_knob("inject_stall", 1)
+    try:
+        X, Wt = to_dev(cp.X), to_dev(cp.Wt)
+        D = torch.zeros(cp.M * cp.K, dtype=torch.int16, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        st = ttc.ttc_conv2d_fprop(*cp.dims(), X.data_ptr(), Wt.data_ptr(), None, cp.K, D.data_ptr(), cp.K, 1.0,
+                                  0.0, None, 0, ttc.DTYPE["bf16"], s)
+        assert st == 0
+        assert ttc.ttc_get_device_error(s) == 4
+    finally:
+        ttc.ttc_set_knob("inject_stall", 0)
+        ttc.ttc_set_knob("timeout_ns", 0)
+    assert ttc.ttc_get_device_error(None) == 0
+    check_full(cp, run_conv(cp))

@@ -18,9 +18,11 @@
 // last image pairs with an image past the end, whose box reads zeros and whose
 // rows are not stored.
 //
-// The pairs walk work units: whole tiles, then, for a last partial wave, half
-// tiles of BN / 2 output channels (MMAs with N = BN / 2; each CTA uses the
-// first rows of its usual filter box).
+// Filter stages hold kHaloKPS taps (a block's 9 taps as 2, 2, 2, 2, 1 for a
+// 3 x 3 filter, never spanning two halos), so one barrier round trip covers 8
+// MMAs.  The pairs walk work units: whole tiles, then, for a last partial
+// wave, half tiles of BN / 2 output channels (MMAs with N = BN / 2; each CTA
+// uses the first rows of its usual filter box).
 //
 // Synchronisation, in addition to the pair kernel's (full/empty ring for the
 // filter operand, tmem_full/tmem_empty for the two accumulators):
