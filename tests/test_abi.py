@@ -116,6 +116,31 @@ def test_workspace_size_query(lib):
     assert ttc.ttc_gemm_workspace_size(64, 64, 64, P, 63, 9, P, 64, C, BF16) == 0
 
 
+def test_staged_workspace_size_query(lib):
+    """The staged size adds an aligned copy of D (pitch rounded to 16 bytes,
+    size to 256) after the operand repack, only when D's rows cannot take TMA
+    stores; matrix-vector shapes and invalid arguments need nothing."""
+    r256 = lambda b: (b + 255) // 256 * 256
+    ab = ttc.ttc_gemm_workspace_size(4099, 3001, 1023, P, 1023, R, P, 1023, C, BF16)
+    staged = ttc.ttc_gemm_workspace_size_staged
+    # D pitch 3001 elements (6002 bytes): a copy of 4099 rows of 3008
+    assert staged(4099, 3001, 1023, P, 1023, R, P, 1023, C, P, 3001, BF16) == ab + r256(4099 * 3008 * 2)
+    # aligned D: just the operand repack
+    assert staged(4099, 3001, 1023, P, 1023, R, P, 1023, C, P, 3008, BF16) == ab
+    # D's base not 16-byte aligned
+    assert staged(64, 64, 64, P, 64, R, P, 64, C, P + 2, 64, BF16) == r256(64 * 64 * 2)
+    # int8: int32 D with a pitch of 203 elements (812 bytes); the copy's pitch
+    # is N rounded to 16 bytes (200)
+    assert staged(300, 200, 64, P, 64, R, P, 64, C, P, 203, I8) == r256(300 * 200 * 4)
+    # matrix-vector shapes run without a workspace
+    assert staged(1, 4096, 4096, P, 4096, R, P, 4096, C, P, 4096, BF16) == 0
+    assert staged(4096, 1, 4096, P, 4096, R, P, 4096, C, P, 1, BF16) == 0
+    # empty or invalid problems
+    assert staged(0, 64, 64, P, 64, R, P, 64, C, P, 64, BF16) == 0
+    assert staged(64, 64, 64, P, 64, R, P, 64, C, P, 63, BF16) == 0
+    assert staged(64, 64, 64, P, 64, 9, P, 64, C, P, 64, BF16) == 0
+
+
 def test_static_scratch_rejects_oversized_problems(lib):
     # 4099 x 8192 bf16 with an odd pitch needs ~64 MiB of repacked A: beyond the
     # fixed 16 MiB, refused before any device work
