@@ -133,6 +133,38 @@ def test_epilogue_terms_with_k_zero():
     assert np.array_equal(r, want) and np.all(sabs == 0)
 
 
+@pytest.mark.parametrize("act", ["none", "relu", "gelu_tanh"])
+def test_epilogue_order_all_terms(act):
+    """All epilogue terms at once, K > 0, all-ones A and B: D = act(alpha K +
+    beta C + bias), the order of the epilogue box in the CUTLASS tutorial's
+    section 1 (alpha/beta, then bias, then the activation).  A bias scaled by
+    alpha, an activation applied before the bias, or beta applied to the bias
+    each give a different value here."""
+    M, N, K = 6, 9, 40
+    one = synth.store(np.ones(1), "bf16")[0]
+    st = synth.Stream(5)
+    c = synth.store(st.uniform(M * N), "bf16").reshape(M, N)
+    bias = np.linspace(-50.0, 30.0, N).astype(np.float32)
+    p = synth.Problem.from_logical(np.full((M, K), one, np.uint16), np.full((K, N), one, np.uint16), c,
+                                   bias=bias, dtype="bf16")
+    r, sabs = oracle.gemm_full(p, alpha=0.75, beta=-2.0, act=act)
+    pre = 0.75 * K - 2.0 * oracle.decode(c, "bf16") + bias.astype(np.float64)
+    tol = 1e-12
+    if act == "relu":
+        want = np.maximum(pre, 0.0)
+    elif act == "gelu_tanh":
+        # x Phi(x) (the erf form), which the tanh form stays within 5e-4 of
+        want = np.array([0.5 * x * (1.0 + math.erf(x / math.sqrt(2.0))) for x in pre.ravel()]).reshape(pre.shape)
+        tol = 5e-4
+    else:
+        want = pre
+    assert np.allclose(r, want, rtol=0.0, atol=tol) and np.all(sabs == K)
+    # the alternatives differ from it (so the test can tell them apart)
+    assert not np.allclose(want, 0.75 * (K + bias.astype(np.float64)) - 2.0 * oracle.decode(c, "bf16"))
+    if act == "relu":
+        assert not np.allclose(want, np.maximum(pre - bias, 0.0) + bias)
+
+
 def test_beta_zero_does_not_read_c():
     M, N, K = 3, 3, 2
     one = synth.store(np.ones(1), "bf16")[0]
