@@ -297,6 +297,11 @@ const char* ttc_status_string(ttc_status status);
  *   TTC_KNOB_SPLIT_K: 0 lets the planner choose; 1..8 splits every tile's K
  *     range across that many CTAs of a cluster (fp16/bf16 only), whose
  *     partial sums are added through distributed shared memory.
+ *   TTC_KNOB_PDL: 0 (default) launches the GEMM, convolution and
+ *     matrix-vector kernels with programmatic dependent launch: a kernel may
+ *     start its prologue (barrier set-up, tensor-memory allocation) while the
+ *     previous kernel on the stream finishes, and touches global memory only
+ *     once that kernel has completed; 1 launches them in plain stream order.
  * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
  */
 typedef enum {
@@ -312,7 +317,8 @@ typedef enum {
   TTC_KNOB_GROUP_M = 9,
   TTC_KNOB_GEMV = 10,
   TTC_KNOB_CONV_HALO = 11,
-  TTC_KNOB_PAIR_TAIL = 12
+  TTC_KNOB_PAIR_TAIL = 12,
+  TTC_KNOB_PDL = 13
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -52,6 +52,8 @@ def test_knobs_validate(lib):
     assert ttc.ttc_set_knob("conv_halo", 0) == 0
     assert ttc.ttc_set_knob("pair_tail", 1) == 0 and ttc.ttc_set_knob("pair_tail", 2) == 1
     assert ttc.ttc_set_knob("pair_tail", 0) == 0
+    assert ttc.ttc_set_knob("pdl", 1) == 0 and ttc.ttc_set_knob("pdl", 2) == 1
+    assert ttc.ttc_set_knob("pdl", 0) == 0
 
 
 BF16 = ttc.DTYPE["bf16"]

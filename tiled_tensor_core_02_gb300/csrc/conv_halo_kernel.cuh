@@ -156,6 +156,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHaloThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // global memory only after the previous grid on the stream (see ptx.cuh)
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)

@@ -40,6 +40,7 @@ std::atomic<int> g_group_m{0};
 std::atomic<int> g_conv_halo{0};
 std::atomic<int> g_pair_tail{0};
 std::atomic<int> g_gemv_off{0};
+std::atomic<int> g_pdl_off{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -388,6 +389,9 @@ DStage plan_dstage(int64_t M, int64_t N, const void* D, int64_t ldd, int esize, 
 }
 
 }  // namespace
+
+bool pdl_enabled() { return g_pdl_off.load() == 0; }
+
 }  // namespace ttc
 
 using namespace ttc;
@@ -449,6 +453,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
     case TTC_KNOB_PAIR_TAIL:
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_pair_tail.store((int)value);
+      return TTC_OK;
+    case TTC_KNOB_PDL:
+      if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
+      g_pdl_off.store((int)value);
       return TTC_OK;
     case TTC_KNOB_CONV_HALO:
       if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
@@ -633,10 +641,13 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   bool swap = swap_mode == 1;
   int bn = forced_bn;
   int ksplit = 1;
+  // A split must keep at least 16 k-blocks per CTA: with fewer, the exchange
+  // of partial sums costs more than the shorter main loop saves (measured on
+  // 512^3 and 1024^3 under graph replay: 11.5 vs 7.1 us and 13.2 vs 9.3 us).
   auto split_for = [&](int64_t tiles, int cand) {
     int sp = 1;
     if (dtype == TTC_I8 || cand > 128) return sp;  // split-K exchange buffers exist up to width 128
-    while (sp < 8 && tiles * sp * 2 <= dev->sm_count && nkb_total / (sp * 2) >= 2) sp *= 2;
+    while (sp < 8 && tiles * sp * 2 <= dev->sm_count && nkb_total / (sp * 2) >= 16) sp *= 2;
     return sp;
   };
   {

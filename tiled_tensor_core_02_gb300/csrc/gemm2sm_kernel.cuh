@@ -118,6 +118,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   cluster_sync();  // barrier initialisation and the TMEM address visible to both CTAs
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above touched only shared and tensor memory and the kernel
+  // parameters; global memory comes after the previous grid on the stream
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp == 0) {
     // ---------------------------------------------------------------- producer (both CTAs)

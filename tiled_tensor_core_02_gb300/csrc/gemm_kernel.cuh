@@ -78,6 +78,24 @@ struct ModeTraits {
   static constexpr int kEpiBufBytes = 32 * kEpiCols * kOutBytes;  // 32 rows x (64 or 128) bytes
 };
 
+// Host: whether the GEMM, convolution and matrix-vector kernels are launched
+// with programmatic dependent launch (on unless TTC_KNOB_PDL turns it off).
+bool pdl_enabled();
+
+// Host: appends the programmatic-stream-serialization attribute to `cfg`
+// when it is enabled (`attrs` has room for it after cfg.numAttrs entries).
+// The kernels so launched wait for the previous grid on the stream before
+// their first global access (grid_dependency_wait).
+inline void add_pdl_attribute(cudaLaunchConfig_t& cfg, cudaLaunchAttribute* attrs) {
+  if (!pdl_enabled()) return;
+  cudaLaunchAttribute& a = attrs[cfg.numAttrs];
+  a = cudaLaunchAttribute{};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs += 1;
+}
+
 struct GemmParams {
   CUtensorMap tmA;
   CUtensorMap tmB;
@@ -758,6 +776,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // the prologue above touched only shared and tensor memory and the kernel
+  // parameters; global memory comes after the previous grid on the stream
+  grid_dependency_wait();
+  grid_dependents_launch();
 
   if (warp < Tr::kProdWarps) {
     // ---------------------------------------------------------------- producer

@@ -43,7 +43,7 @@ int gemm_smem_bytes() {
     cfg.blockDim = dim3(ModeTraits<MODE>::kThreads, 1, 1);                                           \
     cfg.dynamicSmemBytes = smem;                                                                     \
     cfg.stream = stream;                                                                             \
-    cudaLaunchAttribute attr[1];                                                                     \
+    cudaLaunchAttribute attr[2];                                                                     \
     if (p.ksplit > 1) {                                                                              \
       attr[0].id = cudaLaunchAttributeClusterDimension;                                              \
       attr[0].val.clusterDim.x = p.ksplit;                                                           \
@@ -52,6 +52,7 @@ int gemm_smem_bytes() {
       cfg.attrs = attr;                                                                              \
       cfg.numAttrs = 1;                                                                              \
     }                                                                                                \
+    add_pdl_attribute(cfg, attr);                                                                    \
     e = cudaLaunchKernelEx(&cfg, gemm_kernel<BN, MODE>, p);                                          \
     if (e != cudaSuccess) return e;                                                                  \
     return cudaGetLastError();                                                                       \

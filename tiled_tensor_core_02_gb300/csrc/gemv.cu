@@ -59,6 +59,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(kThreads) gemv_rows_kernel(const GemvParams p) {
   const int lane = threadIdx.x & 31;
   const int warps = kThreads / 32;
+  grid_dependency_wait();  // every load and store after the previous grid on the stream
+  grid_dependents_launch();
   for (int i = blockIdx.x * warps + (threadIdx.x >> 5); i < p.rows; i += gridDim.x * warps) {
     const uint16_t* row = p.mat + (int64_t)i * p.ldm;
     float acc = 0.0f;
@@ -97,10 +99,15 @@ cudaError_t launch_gemv_rows(const GemvParams& p, int sm_count, cudaStream_t str
   int64_t grid = (p.rows + warps - 1) / warps;
   const int64_t cap = (int64_t)sm_count * 8;
   if (grid > cap) grid = cap;
-  if (p.bf16)
-    gemv_rows_kernel<true><<<(unsigned)grid, kThreads, 0, stream>>>(p);
-  else
-    gemv_rows_kernel<false><<<(unsigned)grid, kThreads, 0, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t le = p.bf16 ? cudaLaunchKernelEx(&cfg, gemv_rows_kernel<true>, p)
+                                : cudaLaunchKernelEx(&cfg, gemv_rows_kernel<false>, p);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 

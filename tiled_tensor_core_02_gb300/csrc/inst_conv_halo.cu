@@ -42,7 +42,15 @@ cudaError_t launch(const ConvHaloParams& hp, int smem_bytes, int clusters, cudaS
   if (smem_bytes > kHaloSmemLimit) return cudaErrorInvalidValue;
   const cudaError_t e = set_smem_attr<BN, kBF16>();
   if (e != cudaSuccess) return e;
-  conv_halo_kernel<BN, kBF16><<<2 * clusters, kHaloThreads, smem_bytes, stream>>>(hp);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);  // clusters of 2 from the kernel's __cluster_dims__
+  cfg.blockDim = dim3(kHaloThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, conv_halo_kernel<BN, kBF16>, hp);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace

@@ -39,7 +39,15 @@ template <int BN, bool kBF16>
 cudaError_t launch(const GemmParams& p, int clusters, cudaStream_t stream) {
   const cudaError_t e = set_smem_attr<BN, kBF16>();
   if (e != cudaSuccess) return e;
-  gemm_pair_kernel<BN, kBF16><<<2 * clusters, kPairThreads, PairCfg<BN>::kSmemBytes, stream>>>(p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * clusters, 1, 1);  // clusters of 2 from the kernel's __cluster_dims__
+  cfg.blockDim = dim3(kPairThreads, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<BN>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, kBF16>, p);
+  if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
 }  // namespace

@@ -142,6 +142,17 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start while the grid before it on the stream is still
+// running; `grid_dependency_wait` returns once that grid has completed and its
+// memory operations are visible (at once when there is none), so every global
+// load or store of the kernel comes after it.  `grid_dependents_launch` lets
+// the next such kernel on the stream start its own prologue early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // L2 cache policies (createpolicy), used as TMA cache hints.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
