@@ -172,6 +172,39 @@ def timed_loops(steps, launch, stream):
     return t0.elapsed_time(t1), [a.elapsed_time(b) for a, b in zip(starts, ends)], launches
 
 
+# Below this per-launch time the back-to-back pass is replayed from a CUDA
+# graph: the host cannot submit launches that short as fast as they run.
+GRAPH_BELOW_MS = 0.05
+
+
+def timed_graph(steps, launch_on, stream):
+    """The back-to-back pass from a CUDA graph holding the K steps' launches:
+    captured on a side stream, replayed once untimed, then replayed on
+    `stream` between one event pair.  launch_on(i, h) enqueues step i on the
+    stream whose handle is h.  Returns (total_ms, launches in the graph)."""
+    import torch
+    import tiled_tensor_core_02_gb300 as ttc
+    cap = torch.cuda.Stream()
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    n0 = ttc.ttc_launch_count()
+    with torch.cuda.graph(g, stream=cap):
+        for i in range(steps):
+            launch_on(i, cap.cuda_stream)
+    launches = ttc.ttc_launch_count() - n0
+    stream.wait_stream(cap)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1), launches
+
+
 def dist_setup():
     import torch
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -307,6 +340,9 @@ def main():
     ap.add_argument("--pair-tile-n", type=int, default=0, choices=[0, 256, 192, 128],
                     help="CTA-pair tile width: 0 planner, else forced")
     ap.add_argument("--group-m", type=int, default=0, help="tile rows per rasterization group (0: default)")
+    ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],
+                    help="GEMM workloads: replay the back-to-back pass from a CUDA graph (auto: when a "
+                         "launch takes under 50 us)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     spec = workload_spec(args.workload)
@@ -362,6 +398,7 @@ def main():
     bias = dev(p.bias) if p.bias is not None else None
     stream = torch.cuda.current_stream()
     s = stream.cuda_stream
+    stream_h = s
     lay = {"row": ttc.ROW_MAJOR, "col": ttc.COL_MAJOR}
 
     # Operands TMA cannot read (odd pitches) are repacked by ttc_gemm_ws into a
@@ -372,7 +409,8 @@ def main():
                                                   p.ldb, lay[p.layoutB], D.data_ptr(), N, ttc.DTYPE[p.dtype])
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda")
 
-    def step(Ap=A, Bp=B, Cp=C, Dp=D):
+    def step(Ap=A, Bp=B, Cp=C, Dp=D, h=None):
+        s = stream_h if h is None else h
         if nbatch > 1:
             st = ttc.ttc_gemm_strided_batched(
                 nbatch, M, N, K, Ap.data_ptr(), p.lda, p.A.size, lay[p.layoutA], Bp.data_ptr(), p.ldb, p.B.size,
@@ -403,9 +441,14 @@ def main():
     torch.cuda.synchronize()
     total_ms, kern_ms, launches = timed_loops(args.steps, lambda i: step(*copies[(args.warmup + i) % ncopy]),
                                               stream)
+    launch_mode = "stream"
+    if args.graph == "on" or (args.graph == "auto" and statistics.median(kern_ms) < GRAPH_BELOW_MS):
+        total_ms, launches = timed_graph(args.steps,
+                                         lambda i, h: step(*copies[(args.warmup + i) % ncopy], h=h), stream)
+        launch_mode = "cuda_graph"
     barrier(world)
     clocks = sampler.stop()
-    if ttc.ttc_get_device_error(s) != 0:
+    if ttc.ttc_get_device_error(stream_h) != 0:
         raise SystemExit("device error during the timed region")
     total_ms = max_over_ranks(total_ms, world)
     value = flops * args.steps * world / (total_ms * 1e-3) / 1e12
@@ -506,7 +549,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.dtype], "data": "synthetic",
-            "config": config_of(spec, name, world),
+            "config": dict(config_of(spec, name, world), launch=launch_mode),
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
