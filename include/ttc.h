@@ -27,7 +27,13 @@
  *
  * Asynchrony.  ttc_gemm only enqueues work on `stream` (a cudaStream_t; NULL
  * is the legacy default stream) and returns.  Calls on different host threads
- * are safe.
+ * are safe.  Work on one stream keeps stream order: the kernels are launched
+ * with programmatic dependent launch (TTC_KNOB_PDL), so a kernel may begin
+ * its set-up while the previous kernel on the stream finishes, but it reads
+ * and writes global memory only after that kernel has completed.  The calls
+ * may be captured into a CUDA graph: run each kind of call once outside a
+ * capture first, since the first use of a kernel variant on a device sets its
+ * shared-memory attribute and caches its occupancy.
  *
  * Errors.  Every entry point returns a status; none aborts or throws.
  *   TTC_ERR_INVALID_ARG: negative sizes; a leading dimension below the
