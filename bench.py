@@ -549,7 +549,7 @@ def main():
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAME[p.dtype], "data": "synthetic",
-            "config": dict(config_of(spec, name, world), launch=launch_mode),
+            "config": config_of(spec, name, world), "launch": launch_mode,
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
