@@ -543,6 +543,9 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc, used, _ = oracle_sample_rate(p, spec, args.cpu_budget)
         cpu = {"value": rate / 1e12, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": desc}
+        # the same oracle on one host core
+        rate1, desc1, _, _ = oracle_sample_rate(p, spec, args.cpu_budget / 3, threads=1)
+        cpu["single_core"] = {"value": rate1 / 1e12, "unit": "TFLOPS", "cores": 1, "sample": desc1}
 
     if rank == 0:
         line = {
@@ -813,7 +816,7 @@ def conv_bytes(cp):
     return 2 * (cp.N * cp.H * cp.W * cp.C + cp.K * cp.R * cp.S * cp.C + cp.M * cp.K)
 
 
-def conv_oracle_rate(cp, budget_s):
+def conv_oracle_rate(cp, budget_s, threads=0):
     """Times oracle.conv_elements on whole output rows; returns (flop/s, description, threads)."""
     import numpy as np
 
@@ -824,7 +827,7 @@ def conv_oracle_rate(cp, budget_s):
         mm = (np.arange(n, dtype=np.int64) // cp.K) % cp.M
         kk = np.arange(n, dtype=np.int64) % cp.K
         t0 = time.perf_counter()
-        _, _, used = oracle.conv_elements(cp, mm, kk)
+        _, _, used = oracle.conv_elements(cp, mm, kk, nthreads=threads)
         return time.perf_counter() - t0, used
 
     n = min(256, cp.M * cp.K)
@@ -988,6 +991,8 @@ def run_conv(args, spec, name):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, desc, used = conv_oracle_rate(cp, args.cpu_budget)
         cpu = {"value": rate / 1e12, "unit": "TFLOPS", "cores": used, "kind": "oracle", "sample": desc}
+        rate1, desc1, _ = conv_oracle_rate(cp, args.cpu_budget / 3, threads=1)
+        cpu["single_core"] = {"value": rate1 / 1e12, "unit": "TFLOPS", "cores": 1, "sample": desc1}
     if rank == 0:
         line = {
             "metric": C_METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,

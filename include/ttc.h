@@ -186,7 +186,10 @@ ttc_status ttc_gemm_ws(int64_t M, int64_t N, int64_t K,
 
 /*
  * Workspace bytes ttc_gemm_ws uses for these operands: 0 when TMA can read
- * both (or for invalid or empty arguments).  Pure host computation.
+ * both, for matrix-vector problems (one output row with B column-major, or one
+ * output column with A row-major: their kernel reads the operands with plain
+ * loads and needs no workspace), and for invalid or empty arguments.  Pure
+ * host computation.
  */
 size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, ttc_layout layoutA,

@@ -151,6 +151,21 @@ def test_static_scratch_rejects_oversized_problems(lib):
     assert st == 5 and ttc.ttc_status_string(st) == "TTC_ERR_SCRATCH_TOO_SMALL"
 
 
+def test_matrix_vector_problems_need_no_scratch(lib):
+    """A matrix-vector problem takes a kernel that reads its operands with plain
+    loads, whatever their pitch: the workspace query reports 0 for it and the
+    no-allocation entry point does not refuse it, however large its B.
+    M = 1, B column-major 4097 x 4096 with an odd pitch (33.6 MB of bf16)."""
+    assert ttc.ttc_gemm_workspace_size(1, 4096, 4097, P, 4097, R, P, 4097, C, BF16) == 0
+    assert ttc.ttc_gemm_workspace_size(1, 4096, 4097, P, 1, C, P, 4097, C, BF16) == 0  # 1 x K, lda free
+    assert ttc.ttc_gemm_workspace_size(4096, 1, 4097, P, 4097, R, P, 4097, C, BF16) == 0
+    # the same shape with B row-major goes to the tensor-core kernel: repacked
+    assert ttc.ttc_gemm_workspace_size(1, 4095, 4097, P, 4097, R, P, 4095, R, BF16) > 16 << 20
+    st = ttc.ttc_gemm_static_scratch(1, 4096, 4097, P, 4097, R, P, 4097, C, None, 4096, P * 2, 4096, 1.0, 0.0,
+                                     None, 0, BF16, None)
+    assert st != 5  # not refused (without a GPU the call then stops at the CUDA device query)
+
+
 def test_batched_validation(lib):
     sb = ttc.ttc_gemm_strided_batched
     # negative batch or stride; overlapping D batches; in-place C needs equal strides

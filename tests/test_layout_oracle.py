@@ -154,3 +154,68 @@ def test_composition_is_function_composition():
     tab = L.compose_table(a[0], a[1], b[0], b[1])
     for i in range(32):
         assert tab[i] == L.evaluate(a[0], a[1], L.evaluate(b[0], b[1], i))
+
+
+def test_zipped_divide_matches_transpose_closed_form():
+    """"4.21 What is CuTe?", transpose kernel: a tensor divided into 32 x 32
+    blocks and indexed as ((i, j), bx, by) holds element (bx*32 + i, by*32 + j)
+    of the undivided tensor.  For a row-major M x N tensor that element sits at
+    (bx*32 + i)*N + by*32 + j; for the kernel's column-major output view at
+    (bx*32 + i) + (by*32 + j)*M.  The divided domain is ((32, 32), (M/32, N/32)),
+    walked colexicographically, so the flat index of ((i, j), (bx, by)) is
+    i + 32 j + 1024 (bx + (M/32) by)."""
+    for M, N in [(32, 32), (64, 64), (96, 64), (64, 160), (128, 96)]:
+        nbx, nby = M // 32, N // 32
+        for stride, closed in [((N, 1), lambda r, c: r * N + c), ((1, M), lambda r, c: r + c * M)]:
+            dom, tab = L.zipped_divide_table((M, N), stride, (32, 32))
+            assert dom == ((32, 32), (nbx, nby))
+            assert len(tab) == M * N
+            for bx in range(nbx):
+                for by in range(nby):
+                    for i in range(32):
+                        for j in range(32):
+                            flat = i + 32 * j + 1024 * (bx + nbx * by)
+                            assert tab[flat] == closed(bx * 32 + i, by * 32 + j), (M, N, stride, bx, by, i, j)
+            # every element of the tensor appears exactly once
+            assert sorted(tab) == sorted(closed(r, c) for r in range(M) for c in range(N))
+
+
+def test_complement_multi_mode_hand_worked():
+    """complement(L, m), worked by hand from its definition: take L's modes in
+    order of stride; each gap between the range covered so far (the previous
+    extent x stride) and the next stride becomes a mode of the complement
+    (extent = stride / covered, stride = covered); a last mode repeats the
+    covered range up to m."""
+    # (2,2):(1,4) in 16.  Sorted: 2:1 covers [0,2); 4 / 2 = 2 -> mode 2:2; 2:4
+    # covers up to 8; 16 / 8 = 2 -> mode 2:8.  Image {0,1,4,5} + {0,2,8,10} = [0,16).
+    assert L.complement((2, 2), (1, 4), 16) == ((2, 2), (2, 8))
+    # 4:2 in 64.  The stride 2 leaves a gap of 2 -> mode 2:1; 4:2 covers up to 8;
+    # 64 / 8 = 8 -> mode 8:8.  Image {0,2,4,6} + {0,1} + {0,8,..,56} = [0,64).
+    assert L.complement(4, 2, 64) == ((2, 8), (1, 8))
+    # (4,2):(1,16) in 128.  4:1 covers [0,4); 16 / 4 = 4 -> mode 4:4; 2:16 covers
+    # up to 32; 128 / 32 = 4 -> mode 4:32.
+    assert L.complement((4, 2), (1, 16), 128) == ((4, 4), (4, 32))
+    # modes listed out of stride order give the same complement: (2,4):(8,1) in 64.
+    # 4:1 covers [0,4); 8 / 4 = 2 -> mode 2:4; 2:8 covers up to 16; 64 / 16 = 4 -> 4:16.
+    assert L.complement((2, 4), (8, 1), 64) == ((2, 4), (4, 16))
+    # a stride-0 (broadcast) mode and an extent-1 mode take no part
+    assert L.complement((3, 1, 4), (0, 7, 1), 8) == ((2,), (4,))
+    # defining property, for each case: L followed by its complement is a
+    # bijection onto [0, m)
+    for shape, stride, m in [((2, 2), (1, 4), 16), (4, 2, 64), ((4, 2), (1, 16), 128), ((2, 4), (8, 1), 64)]:
+        cs, cd = L.complement(shape, stride, m)
+        both_s = (shape, cs) if isinstance(shape, tuple) else ((shape,), cs)
+        both_d = (stride, cd) if isinstance(stride, tuple) else ((stride,), cd)
+        assert L.is_bijective_onto(both_s, both_d, m), (shape, stride, m)
+
+
+def test_logical_divide_by_strided_tiler_hand_worked():
+    """logical_divide(16:1, 4:2) = 16:1 o (4:2, complement(4:2, 16)).
+    complement(4:2, 16) = (2,2):(1,8) (the gap 2:1, then the repeat 2:8), so the
+    divided layout maps (i, (a, b)) to 2 i + a + 8 b: tile 0 = {0,2,4,6},
+    tile 1 = {1,3,5,7}, tile 2 = {8,..,14}, tile 3 = {9,..,15}."""
+    assert L.complement(4, 2, 16) == ((2, 2), (1, 8))
+    dom, tab = L.logical_divide_table(16, 1, 4, 2)
+    assert [L.size(m) for m in dom] == [4, 4]
+    tiles = [tab[4 * t:4 * t + 4] for t in range(4)]
+    assert tiles == [[0, 2, 4, 6], [1, 3, 5, 7], [8, 10, 12, 14], [9, 11, 13, 15]]

@@ -202,6 +202,19 @@ def test_activations_against_independent_forms():
     assert abs(oracle.act("gelu_tanh", -20.0)) < 1e-12
 
 
+def test_gelu_tanh_matches_float64_library_evaluation():
+    """The tanh-form GELU (constants sqrt(2/pi) and 0.044715) against torch's
+    own float64 evaluation of the same form, gelu(x, approximate='tanh').  Both
+    evaluate 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) in double; only the
+    rounding order differs, so they agree to ~1e-15.  A slip in the 4th digit
+    of either constant moves the result by > 1e-8 somewhere on the grid."""
+    xs = np.linspace(-12, 12, 9601)
+    ref = torch.nn.functional.gelu(torch.from_numpy(xs), approximate="tanh").numpy()
+    got = np.array([oracle.act("gelu_tanh", float(x)) for x in xs])
+    err = np.abs(got - ref)
+    assert err.max() <= 1e-12, (xs[err.argmax()], err.max())
+
+
 def test_f16_decode_matches_library_for_every_pattern():
     bits = np.arange(65536, dtype=np.uint16)
     ref = bits.view(np.float16).astype(np.float64)

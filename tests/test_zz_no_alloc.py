@@ -41,19 +41,37 @@ def _call(p, entry, alpha, beta, act):
     bias = to_dev(p.bias) if p.bias is not None else None
     D = torch.full((p.M * p.N,), -1, dtype=torch.int16, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
     args = (p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA], B.data_ptr(), p.ldb, LAY[p.layoutB],
             C.data_ptr() if C is not None else None, p.ldc, D.data_ptr(), p.N, alpha, beta,
             bias.data_ptr() if bias is not None else None, ttc.ACT[act], ttc.DTYPE[p.dtype])
     if entry == "static":
+        before = ttc.ttc_launch_count()
         st = ttc.ttc_gemm_static_scratch(*args, s)
     else:
-        need = ttc.ttc_gemm_workspace_size(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
-                                           B.data_ptr(), p.ldb, LAY[p.layoutB], ttc.DTYPE[p.dtype])
+        # the workspace entry point given room for its fastest path (operand
+        # repack and the aligned copy of D), as the static array provides
+        need = ttc.ttc_gemm_workspace_size_staged(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
+                                                  B.data_ptr(), p.ldb, LAY[p.layoutB], D.data_ptr(), p.N,
+                                                  ttc.DTYPE[p.dtype])
+        assert need <= ttc.STATIC_SCRATCH_BYTES
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        before = ttc.ttc_launch_count()
         st = ttc.ttc_gemm_ws(*args, ws.data_ptr(), need, s)
+    launches = ttc.ttc_launch_count() - before
     assert st == 0, ttc.STATUS.get(st, st)
     assert ttc.ttc_get_device_error(s) == 0
-    return D.cpu().numpy().view(np.uint16).reshape(p.M, p.N)
+    return D.cpu().numpy().view(np.uint16).reshape(p.M, p.N), launches
+
+
+def _expected_launches(p, beta, d_ptr_aligned=True):
+    """Kernels a call launches when the scratch is used: one repack per operand
+    whose pitch is not a 16-byte multiple, then, when D's pitch is not one
+    either, the copy of C into the aligned copy of D (beta != 0), the GEMM on
+    it and the copy back; otherwise the GEMM alone."""
+    rep = int((p.lda * 2) % 16 != 0) + int((p.ldb * 2) % 16 != 0)
+    staged = (p.N * 2) % 16 != 0 or not d_ptr_aligned
+    return rep + (int(beta != 0.0) + 2 if staged else 1)
 
 
 def test_static_scratch_matches_workspace_entry_twice():
@@ -68,8 +86,12 @@ def test_static_scratch_matches_workspace_entry_twice():
         need = ttc.ttc_gemm_workspace_size(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA],
                                            B.data_ptr(), p.ldb, LAY[p.layoutB], ttc.DTYPE[p.dtype])
         assert 0 < need <= ttc.STATIC_SCRATCH_BYTES  # the case that needs scratch
-        d_static = _call(p, "static", alpha, beta, act)
-        d_ws = _call(p, "ws", alpha, beta, act)
+        d_static, n_static = _call(p, "static", alpha, beta, act)
+        d_ws, n_ws = _call(p, "ws", alpha, beta, act)
+        # the static call really ran on its scratch: the same repack and D-staging
+        # kernels as the workspace call (a call that found no usable scratch would
+        # launch the GEMM alone, reading the operands with plain loads)
+        assert n_static == n_ws == _expected_launches(p, beta), (n_static, n_ws)
         r, sabs = oracle.gemm_full(p, alpha=alpha, beta=beta, act=act)
         # the two entry points agree within the parity tolerance (both against the
         # oracle's S_abs-based bound, and with each other)

@@ -336,6 +336,16 @@ void canonicalise(int64_t M, int64_t N, int64_t K, ttc_layout& layoutA, int64_t&
   }
 }
 
+// Problems the matrix-vector kernel takes (after canonicalise): one output row
+// (M == 1) or column (N == 1) whose reduction runs along the matrix operand's
+// contiguous dimension.  They read their operands with plain loads and use no
+// workspace.
+bool takes_gemv(int64_t M, int64_t N, int64_t K, ttc_layout layoutA, ttc_layout layoutB, ttc_dtype dtype,
+                int64_t batch) {
+  const bool rows = (M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR);
+  return rows && K > 0 && dtype != TTC_I8 && batch == 1 && !g_gemv_off.load();
+}
+
 // Which operands ttc_gemm_ws copies into its workspace (those TMA cannot
 // describe), with their memory-order shape and the padded pitch of the copy.
 struct RepackPlan {
@@ -540,8 +550,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // One output row (M == 1) or column (N == 1) whose reduction runs along the
   // matrix operand's contiguous dimension streams that operand with two FLOPs
   // per element: CUDA-core kernel, one warp per output, no tiles.
-  const bool gemv_rows = (M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR);
-  if (gemv_rows && K > 0 && dtype != TTC_I8 && batch == 1 && !g_gemv_off.load()) {
+  if (takes_gemv(M, N, K, layoutA, layoutB, dtype, batch)) {
     GemvParams gp;
     std::memset(&gp, 0, sizeof gp);
     if (M == 1) {
@@ -1108,6 +1117,7 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const void* A, i
     return 0;
   if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return 0;
   canonicalise(M, N, K, layoutA, lda, layoutB, ldb);
+  if (takes_gemv(M, N, K, layoutA, layoutB, dtype, 1)) return 0;
   return plan_repack(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype == TTC_I8 ? 1 : 2).bytes;
 }
 
@@ -1119,9 +1129,10 @@ size_t ttc_gemm_workspace_size_staged(int64_t M, int64_t N, int64_t K, const voi
     return 0;
   if (dtype != TTC_F16 && dtype != TTC_BF16 && dtype != TTC_I8) return 0;
   // matrix-vector problems take their own kernel and no workspace
-  const bool gemv = dtype != TTC_I8 && K > 0 &&
-                    ((M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR));
-  if (gemv) return 0;
+  int64_t lda_c = lda, ldb_c = ldb;
+  ttc_layout la = layoutA, lb = layoutB;
+  canonicalise(M, N, K, la, lda_c, lb, ldb_c);
+  if (takes_gemv(M, N, K, la, lb, dtype, 1)) return 0;
   const size_t ab = ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype);
   return ab + plan_dstage(M, N, D, ldd, dtype == TTC_I8 ? 4 : 2, ab).bytes;
 }
