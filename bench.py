@@ -337,7 +337,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pair", type=int, default=0, choices=[0, 1, 2],
                     help="kernel choice: 0 planner, 1 CTA-pair kernel where it applies, 2 single-CTA kernel")
-    ap.add_argument("--pair-tile-n", type=int, default=0, choices=[0, 256, 192, 128],
+    ap.add_argument("--pair-tile-n", type=int, default=0, choices=[0, 256, 224, 192, 128],
                     help="CTA-pair tile width: 0 planner, else forced")
     ap.add_argument("--group-m", type=int, default=0, help="tile rows per rasterization group (0: default)")
     ap.add_argument("--graph", default="auto", choices=["auto", "on", "off"],

@@ -290,7 +290,7 @@ const char* ttc_status_string(ttc_status status);
  *   TTC_KNOB_GROUP_M: tile rasterization: consecutive tiles walk this many
  *     tile rows per column of tiles (0: 16 for single CTAs, 8 for pairs).
  *   TTC_KNOB_PAIR_TILE_N: 0 lets the planner choose the CTA-pair tile width;
- *     256, 192 or 128 forces it (192 only with a column-major B).
+ *     256, 224, 192 or 128 forces it (224 and 192 only with a column-major B).
  *   TTC_KNOB_GEMV: 0 (default) runs matrix-vector problems whose reduction
  *     is contiguous (M == 1 with a column-major B, or N == 1 with a
  *     row-major A; fp16/bf16, K > 0, not batched) on the CUDA-core

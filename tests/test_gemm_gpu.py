@@ -455,11 +455,11 @@ def test_workspace_too_small_falls_back():
     check_full(p, d, 1.0, 1.0)
 
 
-@pytest.mark.parametrize("width", [192, 128])
+@pytest.mark.parametrize("width", [224, 192, 128])
 @pytest.mark.parametrize("la,lb", synth.MAJORNESS)
 def test_pair_tile_widths(width, la, lb):
-    if width == 192 and lb == "row":
-        pytest.skip("192-wide pair tiles take a column-major B only")
+    if width in (224, 192) and lb == "row":
+        pytest.skip("224- and 192-wide pair tiles take a column-major B only")
     ttc.ttc_set_knob("pair", 1)
     ttc.ttc_set_knob("pair_tile_n", width)
     try:

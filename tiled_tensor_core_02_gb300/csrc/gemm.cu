@@ -48,7 +48,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
-  int pair_clusters[2][3] = {{-1, -1, -1}, {-1, -1, -1}};  // resident CTA pairs [bf16][width 256/192/128]
+  int pair_clusters[2][4] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};  // resident CTA pairs [bf16][width 256/224/192/128]
   int halo_clusters[2][2] = {{-1, -1}, {-1, -1}};          // halo convolution pairs [bf16][width 256/128]
   uint32_t* err = nullptr;
 };
@@ -124,10 +124,11 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
 // CTA-pair tile width for an M x N problem (times batch): the width whose
 // tiles fill the resident pairs best, weighted by the width's measured
-// relative rate (a narrower tile stages more A per column: 1, 0.87, 0.64 for
-// 256, 192, 128 on bf16 8192^3) and by the share of its last column of tiles
-// that lies inside N.  192 needs a K-major B (its half, 96 columns, is not a
-// whole number of 64-column MN-major slabs).  bn == 0: no width fits.
+// relative rate (a narrower tile stages more A per column: 1, 0.95, 0.87,
+// 0.64 for 256, 224, 192, 128 on bf16 8192^3) and by the share of its last
+// column of tiles that lies inside N.  224 and 192 need a K-major B (their
+// halves, 112 and 96 columns, are not whole 64-column MN-major slabs).
+// bn == 0: no width fits.
 struct PairChoice {
   int bn = 0;
   int clusters = 0;
@@ -136,10 +137,11 @@ PairChoice choose_pair(DeviceInfo* dev, bool bf16, int64_t M, int64_t N, int64_t
   const int forced_pbn = g_pair_tile_n.load();
   PairChoice pc;
   double best = -1.0;
-  const int widths[3] = {256, 192, 128};
-  for (int wi = 0; wi < 3; ++wi) {
+  const int widths[4] = {256, 224, 192, 128};
+  const double rates[4] = {1.0, 0.95, 0.87, 0.64};
+  for (int wi = 0; wi < 4; ++wi) {
     const int w = widths[wi];
-    if ((forced_pbn != 0 && w != forced_pbn) || (b_mn && w == 192)) continue;
+    if ((forced_pbn != 0 && w != forced_pbn) || (b_mn && (w == 224 || w == 192))) continue;
     int& cl = dev->pair_clusters[bf16 ? 1 : 0][wi];
     if (cl < 0) {
       std::lock_guard<std::mutex> lk(g_mu);
@@ -151,8 +153,7 @@ PairChoice choose_pair(DeviceInfo* dev, bool bf16, int64_t M, int64_t N, int64_t
     const int64_t waves = (tiles + cl - 1) / cl;
     const double fill = (double)tiles / (double)(waves * cl);
     const double inside = (double)N / (double)(nb * w);
-    const double rate = w == 256 ? 1.0 : w == 192 ? 0.87 : 0.64;
-    const double score = fill * inside * rate;
+    const double score = fill * inside * rates[wi];
     if (score > best + 1e-9) {
       best = score;
       pc.bn = w;
@@ -473,7 +474,7 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       g_conv_halo.store((int)value);
       return TTC_OK;
     case TTC_KNOB_PAIR_TILE_N:
-      if (value != 0 && value != 256 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
+      if (value != 0 && value != 256 && value != 224 && value != 192 && value != 128) return TTC_ERR_INVALID_ARG;
       g_pair_tile_n.store((int)value);
       return TTC_OK;
   }
@@ -846,6 +847,12 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
       const int nclus = plan_pair_units(prm, pbn, clusters);
+      if (K > 0 && !b_mn && prm.tail_from < prm.num_units) {
+        // half units stage only their pbn / 4 columns of B per CTA
+        if (!encode_3d(&prm.tmBh, dt, 2, B, K, N, ldb, kBK, pbn / 4, CU_TENSOR_MAP_SWIZZLE_128B, bdB))
+          return TTC_ERR_CUDA;
+        prm.b_half_map = 1;
+      }
       prm.a_stream = prm.num_n_blocks == 1;
       prm.b_stream = prm.num_m_blocks == 1;
       if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
@@ -1077,6 +1084,10 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
       const int gmp = g_group_m.load() > 0 ? g_group_m.load() : 8;
       prm.group_m = prm.num_m_blocks < gmp ? prm.num_m_blocks : gmp;
       const int nclus = plan_pair_units(prm, pc.bn, pc.clusters);
+      if (Kg > 0 && prm.tail_from < prm.num_units) {
+        if (!encode_3d(&prm.tmBh, dt, 2, Wt, Kg, K, Kg, kBK, pc.bn / 4, CU_TENSOR_MAP_SWIZZLE_128B)) return TTC_ERR_CUDA;
+        prm.b_half_map = 1;
+      }
       if (launch_pair(bf16, pc.bn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TTC_ERR_CUDA;
       g_launches.fetch_add(1);

@@ -16,8 +16,14 @@
 //   empty[s]     both CTAs; the MMA's commit is multicast to both; producers wait.
 //   tmem_full[a] both CTAs; multicast commit after a tile's last k-block;
 //                epilogue warps wait.
-//   tmem_empty[a] even CTA only; all 8 epilogue warps of the pair arrive (the
+//   tmem_empty[a] even CTA only; all 16 epilogue warps of the pair arrive (the
 //                odd CTA's remotely); the MMA waits before reusing accumulator a.
+//                The arrive is relaxed: it follows tcgen05.wait::ld, so the
+//                warp's reads of the accumulator are complete, and it publishes
+//                no memory writes (a release arrive would also wait for the
+//                warp's outstanding C loads and stores).
+// Epilogue: eight warps, two per TMEM lane quarter; the first four drain the
+// left half of a tile's 32-column chunks, the other four the right half.
 // The layout of a CTA's half tiles, the epilogue and the error handling are
 // those of gemm_kernel (one CTA); every wait is bounded.
 //
@@ -31,9 +37,10 @@
 namespace ttc {
 
 constexpr int kPairBM = 256;
-constexpr int kPairThreads = 192;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..5 epilogue
+constexpr int kPairEpiWarps = 8;   // two per TMEM lane quarter, each taking half of a tile's columns
+constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..9 epilogue
 
-// Pair tile 256 x BN (BN = 256, 192 or 128): each CTA stages 128 A rows and
+// Pair tile 256 x BN (BN = 256, 224, 192 or 128): each CTA stages 128 A rows and
 // BN / 2 B columns per k-block.  A pipeline stage holds kKPS = 2 k-blocks
 // (128 of K, 8 MMAs per barrier round trip): measured on GB300, one full/empty
 // round trip per 4 MMAs holds the pair to ~85 ns per N = 256 MMA, one per 8
@@ -43,18 +50,18 @@ struct PairCfg {
   static constexpr int kBHalf = BN / 2;
   static constexpr int kKPS = 2;                        // k-blocks per stage
   static constexpr int kAHalfBytes = 128 * kBK * 2;     // one k-block of A rows: 16 KiB
-  static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // one k-block of B columns: 16 / 12 / 8 KiB
+  static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // one k-block of B columns: 16 / 14 / 12 / 8 KiB
   static constexpr int kKBlockBytes = kAHalfBytes + kBHalfBytes;
   static constexpr int kStageBytes = kKPS * kKBlockBytes;
   static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
-  static constexpr int kEpiBytes = kEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kEpiBytes = kPairEpiWarps * 2 * kEpiBufBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesRaw = (kSmemLimit - 1024 - kBarBytes - kEpiBytes) / kStageBytes;
   static constexpr int kStages = kStagesRaw > 8 ? 8 : kStagesRaw;
   static constexpr int kTmemCols = 2 * BN > 256 ? 512 : 256;  // two accumulators, a power of two
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
-  static_assert(BN == 256 || BN == 192 || BN == 128, "pair tile width");
+  static_assert(BN == 256 || BN == 224 || BN == 192 || BN == 128, "pair tile width");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
@@ -97,7 +104,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     if (lane < 2) {
       mbar_init(&tmem_full[lane], 1);
-      mbar_init(&tmem_empty[lane], 2 * kEpiWarps);
+      mbar_init(&tmem_empty[lane], 2 * kPairEpiWarps);
     }
     if (lane == 0) {
       mbar_init(stall_bar, 1);
@@ -108,6 +115,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (threadIdx.x == 0) {
     prefetch_tmap(&p.tmA);
     prefetch_tmap(&p.tmB);
+    if (p.b_half_map) prefetch_tmap(&p.tmBh);
     if (p.d_tma) prefetch_tmap(&p.tmD);
   }
   if (warp == 1) {
@@ -142,8 +150,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int za = bz * p.a_bc, zb = bz * p.b_bc;
         const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
         // this CTA's B columns: a half unit uses the first kBHalf / 2 of the
-        // usual box (the rest is loaded and not read)
+        // usual box, and loads only those where it can (MN-major slabs of 64
+        // columns, or the half-width map of a K-major B); otherwise it loads the
+        // whole box and the rest is not read
         const int n0 = nb * kPairBN + n_off + (int)rank * (half ? PairCfg::kBHalf / 2 : PairCfg::kBHalf);
+        const bool b_half_box = half && (p.b_mn || p.b_half_map);
+        const int b_bytes = b_half_box ? PairCfg::kBHalfBytes / 2 : PairCfg::kBHalfBytes;
+        const int b_slabs = b_half_box ? (PairCfg::kBHalf / 2 + 63) / 64 : PairCfg::kBHalf / 64;
         // convolution: window corner of output pixel m0 (rows past the end start
         // beyond the last image, where the im2col box reads zeros)
         int cv_n = 0, cv_h0 = 0, cv_w0 = 0;
@@ -163,7 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) {
-            mbar_arrive_expect_tx(&full[stage], 2 * nkb * PairCfg::kKBlockBytes);
+            mbar_arrive_expect_tx(&full[stage], 2 * nkb * (PairCfg::kAHalfBytes + b_bytes));
             armed_mask |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -186,10 +199,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol_a);
             }
             if (!p.b_mn) {
-              tma_load_3d_pair(b, &p.tmB, k0, n0, zb, full_leader, pol_b);
+              tma_load_3d_pair(b, b_half_box ? &p.tmBh : &p.tmB, k0, n0, zb, full_leader, pol_b);
             } else {
-#pragma unroll
-              for (int h = 0; h < PairCfg::kBHalf / 64; ++h)
+              for (int h = 0; h < b_slabs; ++h)
                 tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol_b);
             }
           }
@@ -275,6 +287,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int q = warp & 3;
+    const int part = ew >> 2;  // which half of a tile's columns this warp drains
     uint8_t* stage_buf = sEpi + ew * 2 * PairCfg::kEpiBufBytes;
     int buf = 0;
     int it = 0;
@@ -292,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       c_prefetch_row(p, epi_ptrs(p, pbz, 2), pmb * kPairBM + (int)rank * 128 + q * 32 + lane,
                      pnb * kPairBN + pn_off, phalf ? kPairBN / 2 : kPairBN);
     };
-    prefetch_c(pair);
+    if (part == 0) prefetch_c(pair);
     for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
       int t, n_off;
       bool half;
@@ -306,14 +319,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const int grow = m0 + q * 32 + lane;
       const bool row_ok = grow < p.M;
       const EpiPtrs ep = epi_ptrs(p, bz, 2);
-      prefetch_c(u + num_pairs);
+      if (part == 0) prefetch_c(u + num_pairs);
+      const int c_lo = part == 0 ? 0 : (chunks + 1) / 2;
+      const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
       // the first chunk's C is fetched before waiting for the accumulator
       CChunk16 cc;
-      c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
+      c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * kEpiCols), grow, n0 + c_lo * kEpiCols, lane, cc);
       if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
       tc_fence_after();
+      if (c_lo == c_hi) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+      }
 #pragma unroll 1
-      for (int c = 0; c < chunks; ++c) {
+      for (int c = c_lo; c < c_hi; ++c) {
         const int gcol0 = n0 + c * kEpiCols;
         uint32_t r[32];
         if (has_k) {
@@ -323,17 +343,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        if (c == chunks - 1) {
-          // this warp's accumulator rows are read: tell the even CTA's issuer
+        if (c == c_hi - 1) {
+          // this warp's accumulator columns are read: tell the even CTA's issuer
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
         const int cpath = c_path(p, ep, gcol0);
         uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, PairCfg::kEpiBufBytes, lane);
         epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
-        if (c + 1 < chunks)
+        if (c + 1 < c_hi)
           c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
         epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane,
                            ep);

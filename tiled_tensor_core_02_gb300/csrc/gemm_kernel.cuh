@@ -153,6 +153,11 @@ struct GemmParams {
   // tail_from + (u - tail_from) / 2), so that a last, partial wave keeps twice
   // as many pairs busy for half as long.  tail_from == num_units: whole tiles.
   int tail_from, num_units;
+  // CTA-pair kernel, K-major B: tmBh has boxes of a half unit's width per CTA
+  // (BN / 4 columns), so that half units stage only the B columns they use
+  // (b_half_map == 1; otherwise they load the whole box and read half of it)
+  int b_half_map;
+  CUtensorMap tmBh;
 };
 
 // Tile and column offset of work unit u of the CTA-pair walk (see tail_from).

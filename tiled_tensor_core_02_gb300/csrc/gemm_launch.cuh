@@ -14,7 +14,7 @@ template <int BN, int MODE>
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
 // CTA-pair (2-SM) fp16/bf16 kernel, defined in inst_pair.cu.
-// bn: the pair tile's width (256, 192 or 128).
+// bn: the pair tile's width (256, 224, 192 or 128).
 int pair_max_clusters(bool bf16, int bn);
 cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream);
 

@@ -56,6 +56,7 @@ cudaError_t launch(const GemmParams& p, int clusters, cudaStream_t stream) {
 int pair_max_clusters(bool bf16, int bn) {
   switch (bn) {
     case 256: return bf16 ? max_clusters<256, true>() : max_clusters<256, false>();
+    case 224: return bf16 ? max_clusters<224, true>() : max_clusters<224, false>();
     case 192: return bf16 ? max_clusters<192, true>() : max_clusters<192, false>();
     case 128: return bf16 ? max_clusters<128, true>() : max_clusters<128, false>();
   }
@@ -65,6 +66,7 @@ int pair_max_clusters(bool bf16, int bn) {
 cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream) {
   switch (bn) {
     case 256: return bf16 ? launch<256, true>(p, clusters, stream) : launch<256, false>(p, clusters, stream);
+    case 224: return bf16 ? launch<224, true>(p, clusters, stream) : launch<224, false>(p, clusters, stream);
     case 192: return bf16 ? launch<192, true>(p, clusters, stream) : launch<192, false>(p, clusters, stream);
     case 128: return bf16 ? launch<128, true>(p, clusters, stream) : launch<128, false>(p, clusters, stream);
   }
