@@ -446,6 +446,7 @@ def main():
         total_ms, launches = timed_graph(args.steps,
                                          lambda i, h: step(*copies[(args.warmup + i) % ncopy], h=h), stream)
         launch_mode = "cuda_graph"
+
     barrier(world)
     clocks = sampler.stop()
     if ttc.ttc_get_device_error(stream_h) != 0:
@@ -477,6 +478,11 @@ def main():
                      "tflops": flops / avg_kernel_s / 1e12, "achieved_gbs": alg_bytes / avg_kernel_s / 1e9,
                      "kernel_ms_mean": statistics.mean(kern_ms),
                      "kernel_ms_median": statistics.median(kern_ms), "kernel_ms_min": min(kern_ms)})
+    # the same ratio over the back-to-back pass (its launches overlap their
+    # prologues with the previous launch's tail): the steady-state rate
+    b2b_s = total_ms * 1e-3 / args.steps
+    b2b = flops / b2b_s / 1e12 if roofline["bound"] == "tensor" else alg_bytes / b2b_s / 1e9
+    roofline.update({"achieved_back_to_back": b2b, "frac_back_to_back": b2b / roofline["peak"]})
 
     # ---------------------------------------------------------------- end to end
     # Every step uploads its inputs from pinned host memory, runs the GEMM and

@@ -449,6 +449,31 @@ def test_workspace_staged_d_in_place_and_padding(beta):
     assert np.array_equal(rows[:, p.N:], p.C.reshape(-1)[: p.M * 305].reshape(p.M, 305)[:, p.N:])
 
 
+@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+@pytest.mark.parametrize("c_off,d_off", [(1, 3), (2, 5), (3, 7), (4, 6), (7, 1), (0, 2)])
+def test_unaligned_c_and_d_rows(pair, c_off, d_off):
+    """C and D rows at every 2-byte phase of a 16-byte block (odd pitches and
+    element offsets of the base pointers): the epilogue moves each row segment
+    as the aligned 16-byte blocks that cover it; the last column chunk is
+    partial.  Nothing outside D's M x N elements is written."""
+    M, N, K = 300, 300 if pair == 1 else 77, 128
+    ldc, ldd = N + 3, N + 5
+    p = synth.Problem(M, N, K, dtype="bf16", seed=50 + c_off, distC="uniform", dist_bias="normal:0.5", ldc=ldc)
+    ttc.ttc_set_knob("pair", pair)
+    try:
+        cbig = np.concatenate([np.zeros(c_off, np.uint16), p.C, np.zeros(8, np.uint16)])
+        C_dev = to_dev(cbig)[c_off:]
+        Dbig = torch.full((M * ldd + d_off + 8,), -1, dtype=torch.int16, device="cuda")
+        d = run(p, 1.0, 0.75, "gelu_tanh", C_dev=C_dev, D=Dbig[d_off:], ldd=ldd)
+        check_full(p, d, 1.0, 0.75, "gelu_tanh")
+        full = Dbig.cpu().numpy().view(np.uint16)
+        assert np.all(full[:d_off] == 0xFFFF) and np.all(full[d_off + M * ldd:] == 0xFFFF)
+        rows = full[d_off:d_off + M * ldd].reshape(M, ldd)
+        assert np.all(rows[:, N:] == 0xFFFF)
+    finally:
+        ttc.ttc_set_knob("pair", 0)
+
+
 def test_workspace_too_small_falls_back():
     p = synth.Problem(257, 131, 97, dtype="bf16", seed=32, distC="uniform", lda=98, ldb=99)
     d = run(p, 1.0, 1.0, workspace=64)

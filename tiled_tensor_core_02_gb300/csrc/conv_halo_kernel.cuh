@@ -351,7 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kHaloThreads, 1)
           if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, nullptr, lane, ep);
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, ep);
         if (c + 1 < chunks) c_fetch16(p, ep, cpath, grow, gcol0 + kEpiCols, lane, cc);
         halo_store_chunk(hp, packed, sbuf, lane, out_row, gcol0);
       }

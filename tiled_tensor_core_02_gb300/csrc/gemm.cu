@@ -9,13 +9,16 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "conv_halo.cuh"
 #include "gemm2sm_kernel.cuh"
 #include "gemm_launch.cuh"
 #include "gemv.cuh"
+#include "index_maps.hpp"
 #include "repack.cuh"
 #include "transpose.cuh"
 #include "ttc.h"
@@ -108,6 +111,55 @@ bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* ba
   cuuint32_t estr[3] = {1, 1, 1};
   return g_encode(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Tensor map of one operand as its BoxMap describes it: the matrix as stored
+// (`rows` x K with K contiguous when k_inner, rows contiguous otherwise), read
+// in boxes of box_inner x box_outer.
+bool encode_operand(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int64_t rows, int64_t K,
+                    int64_t ld, const BoxMap& bm, CUtensorMapSwizzle sw, BatchDim bd = BatchDim()) {
+  return bm.k_inner ? encode_3d(m, dt, esize, base, K, rows, ld, bm.box_inner, bm.box_outer, sw, bd)
+                    : encode_3d(m, dt, esize, base, rows, K, ld, bm.box_inner, bm.box_outer, sw, bd);
+}
+
+// The kernels' index maps for one tile configuration, derived from the
+// layouts once (index_maps.hpp) and kept: they depend only on the key.
+struct MapKey {
+  int tile_m, tile_n, ctas, a_rows, a_mn, b_mn, esize, swizzled, half_cols;
+  bool operator<(const MapKey& o) const {
+    return std::tie(tile_m, tile_n, ctas, a_rows, a_mn, b_mn, esize, swizzled, half_cols) <
+           std::tie(o.tile_m, o.tile_n, o.ctas, o.a_rows, o.a_mn, o.b_mn, o.esize, o.swizzled, o.half_cols);
+  }
+};
+std::map<MapKey, TileMaps> g_maps;
+
+// Fills `out` with the maps of `k`; false when the derivation fails or does
+// not describe the tile the kernels were compiled for (chunk width, one row
+// per epilogue thread, a lane per TMEM row).
+bool tile_maps(const MapKey& k, TileMaps& out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_maps.find(k);
+  if (it == g_maps.end()) {
+    TileMaps tm;
+    try {
+      tm = maps::derive(k.tile_m, k.tile_n, k.ctas, k.a_rows, k.a_mn != 0, k.b_mn != 0, k.esize, k.swizzled != 0,
+                        k.half_cols);
+    } catch (...) {
+      return false;
+    }
+    if (tm.epi_chunk != kEpiCols || tm.epi_row_step != 1 || tm.tmem_row_step != (1u << 16) ||
+        tm.tile_m != k.tile_m || tm.tile_n != k.tile_n)
+      return false;
+    it = g_maps.emplace(k, tm).first;
+  }
+  out = it->second;
+  return true;
+}
+
+// Bytes one k-block of an operand's boxes delivers (0 for more boxes than
+// the kernels' producers issue: kMaxBoxes, two in the CTA-pair kernel).
+int box_bytes(const BoxMap& b, int max_boxes = kMaxBoxes) {
+  return b.boxes >= 1 && b.boxes <= max_boxes ? b.boxes * b.smem_step : 0;
 }
 
 bool tma_ok(const void* p, int64_t ld, int esize) {
@@ -597,21 +649,20 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     const bool use_rp = rp.bytes > 0 && rp.bytes <= workspace_bytes;
     const DStage ds = plan_dstage(M, N, D, ldd, out_esize, use_rp ? rp.bytes : 0);
     if (use_rp) {
+      // one launch copies both operands
       uint8_t* ws = static_cast<uint8_t*>(workspace);
-      cudaStream_t s = static_cast<cudaStream_t>(stream);
+      RepackSpec specs[2];
+      int n = 0;
+      if (rp.a) specs[n++] = RepackSpec{A, lda, rp.a_rows, rp.a_cols, ws + rp.a_off, rp.a_ld, in_esize};
+      if (rp.b) specs[n++] = RepackSpec{B, ldb, rp.b_rows, rp.b_cols, ws + rp.b_off, rp.b_ld, in_esize};
+      if (launch_repack2(specs, n, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTC_ERR_CUDA;
+      g_launches.fetch_add(1);
       if (rp.a) {
-        if (launch_repack(A, lda, rp.a_rows, rp.a_cols, ws + rp.a_off, rp.a_ld, in_esize, dev->sm_count, s) !=
-            cudaSuccess)
-          return TTC_ERR_CUDA;
-        g_launches.fetch_add(1);
         A = ws + rp.a_off;
         lda = rp.a_ld;
       }
       if (rp.b) {
-        if (launch_repack(B, ldb, rp.b_rows, rp.b_cols, ws + rp.b_off, rp.b_ld, in_esize, dev->sm_count, s) !=
-            cudaSuccess)
-          return TTC_ERR_CUDA;
-        g_launches.fetch_add(1);
         B = ws + rp.b_off;
         ldb = rp.b_ld;
       }
@@ -745,29 +796,28 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   GemmParams prm;
   std::memset(&prm, 0, sizeof prm);
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  // rows of A worth loading per tile: all 128, or only those that exist (the
+  // raw int8 staging always takes whole 128-row boxes)
+  const int a_rows = M >= kBM || mode == kModeI8Tma ? kBM : (int)round_up(M, 8);
+  // the kernel's index maps: tile origins, TMA boxes (128-byte swizzled slabs,
+  // or the unswizzled int8 staging tiles) and the epilogue's thread maps
+  if (!tile_maps({kBM, bn, 1, a_rows, a_mn, b_mn, in_esize, mode != kModeI8Tma, 0}, prm.maps))
+    return TTC_ERR_UNSUPPORTED;
+  // the boxes must fit the kernel's shared-memory slots (raw int8 staging: one
+  // byte per element)
+  const int slot_esize = mode == kModeI8Tma ? 1 : 2;
+  const int a_bytes = box_bytes(prm.maps.a), b_bytes = box_bytes(prm.maps.b);
+  if (a_bytes == 0 || a_bytes > kBM * kBK * slot_esize || b_bytes == 0 || b_bytes > bn * kBK * slot_esize)
+    return TTC_ERR_UNSUPPORTED;
   if (K > 0 && mode == kModeI8Tma) {
-    // raw int8 tiles, unswizzled: K-major boxes of 64 k x rows, MN-major boxes of rows x 64 k
     const CUtensorMapDataType d8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    bool ok = !a_mn ? encode_3d(&prm.tmA, d8, 1, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE, bdA)
-                    : encode_3d(&prm.tmA, d8, 1, A, M, K, lda, kBM, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, bdA);
-    ok = ok && (!b_mn ? encode_3d(&prm.tmB, d8, 1, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_NONE, bdB)
-                      : encode_3d(&prm.tmB, d8, 1, B, N, K, ldb, bn, kBK, CU_TENSOR_MAP_SWIZZLE_NONE, bdB));
+    const bool ok = encode_operand(&prm.tmA, d8, 1, A, M, K, lda, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_NONE, bdA) &&
+                    encode_operand(&prm.tmB, d8, 1, B, N, K, ldb, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_NONE, bdB);
     if (!ok) return TTC_ERR_CUDA;
   }
-  // rows of A worth loading per tile: all 128, or only those that exist
-  const int a_rows = M >= kBM ? kBM : (int)round_up(M, 8);
-  prm.a_boxes = a_rows > 64 ? 2 : 1;
   if (K > 0 && (mode == kModeTmaF16 || mode == kModeTmaBF16)) {
-    bool ok;
-    if (!a_mn)
-      ok = encode_3d(&prm.tmA, dt, 2, A, K, M, lda, kBK, a_rows, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
-    else
-      ok = encode_3d(&prm.tmA, dt, 2, A, M, K, lda, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
-    if (!ok) return TTC_ERR_CUDA;
-    if (!b_mn)
-      ok = encode_3d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, bn, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
-    else
-      ok = encode_3d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
+    const bool ok = encode_operand(&prm.tmA, dt, 2, A, M, K, lda, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_128B, bdA) &&
+                    encode_operand(&prm.tmB, dt, 2, B, N, K, ldb, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
     if (!ok) return TTC_ERR_CUDA;
   }
   if (store_tma) {
@@ -816,7 +866,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   prm.ldd = ldd;
   prm.bias = bias;
   prm.act = (int)act;
-  prm.stage_tx = (uint32_t)((!a_mn ? a_rows * kBK * 2 : prm.a_boxes * 64 * kBK * 2) + bn * kBK * 2);
+  prm.stage_tx = (uint32_t)(box_bytes(prm.maps.a) + box_bytes(prm.maps.b));
   prm.d_tma = store_tma ? 1 : 0;
   prm.d_trans = swap ? 1 : 0;
   prm.err = dev->err;
@@ -833,11 +883,16 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     const int pbn = pc.bn, clusters = pc.clusters;
     const int64_t pair_tiles = pbn ? batch * ((M + kPairBM - 1) / kPairBM) * ((N + pbn - 1) / pbn) : 0;
     if (pbn != 0 && (pair_mode == 1 || pair_tiles * 4 >= dev->sm_count)) {
+      // each CTA of the pair stages 128 rows of A and its pbn / 2 columns of B
+      // per k-block; only 256-wide tiles are halved for a last wave
+      if (!tile_maps({kPairBM, pbn, 2, kBM, a_mn, b_mn, 2, 1, pbn == 256 ? pbn / 2 : 0}, prm.maps))
+        return TTC_ERR_UNSUPPORTED;
+      if (box_bytes(prm.maps.a, 2) != kABytes || box_bytes(prm.maps.b, 2) != pbn / 2 * kBK * 2 ||
+          (pbn == 256 && box_bytes(prm.maps.b_half, 2) != pbn / 4 * kBK * 2))
+        return TTC_ERR_UNSUPPORTED;
       if (K > 0) {
-        // each CTA loads whole 128-row A boxes and its pbn / 2 columns of the B tile
-        bool ok = a_mn || encode_3d(&prm.tmA, dt, 2, A, K, M, lda, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B, bdA);
-        ok = ok && (!b_mn ? encode_3d(&prm.tmB, dt, 2, B, K, N, ldb, kBK, pbn / 2, CU_TENSOR_MAP_SWIZZLE_128B, bdB)
-                          : encode_3d(&prm.tmB, dt, 2, B, N, K, ldb, 64, kBK, CU_TENSOR_MAP_SWIZZLE_128B, bdB));
+        const bool ok = encode_operand(&prm.tmA, dt, 2, A, M, K, lda, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_128B, bdA) &&
+                        encode_operand(&prm.tmB, dt, 2, B, N, K, ldb, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_128B, bdB);
         if (!ok) return TTC_ERR_CUDA;
       }
       prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
@@ -849,7 +904,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       const int nclus = plan_pair_units(prm, pbn, clusters);
       if (K > 0 && !b_mn && prm.tail_from < prm.num_units) {
         // half units stage only their pbn / 4 columns of B per CTA
-        if (!encode_3d(&prm.tmBh, dt, 2, B, K, N, ldb, kBK, pbn / 4, CU_TENSOR_MAP_SWIZZLE_128B, bdB))
+        if (!encode_operand(&prm.tmBh, dt, 2, B, N, K, ldb, prm.maps.b_half, CU_TENSOR_MAP_SWIZZLE_128B, bdB))
           return TTC_ERR_CUDA;
         prm.b_half_map = 1;
       }
@@ -961,6 +1016,8 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (store_tma && !encode_3d(&prm.tmD, dt, 2, D, K, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return TTC_ERR_CUDA;
+  // the im2col A and the filters are both K-major operands
+  if (!tile_maps({kBM, bn, 1, kBM, 0, 0, 2, 1, 0}, prm.maps)) return TTC_ERR_UNSUPPORTED;
   prm.A = X;
   prm.lda = Kg;
   prm.B = Wt;  // B(kk, k) = Wt[k Kg + kk]: the K-major ("column-major") B operand
@@ -1072,8 +1129,11 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
     const bool bf16 = dtype == TTC_BF16;
     const PairChoice pc = choose_pair(dev, bf16, M, K, 1, false);
     if (pc.bn != 0) {
+      if (!tile_maps({kPairBM, pc.bn, 2, kBM, 0, 0, 2, 1, pc.bn == 256 ? pc.bn / 2 : 0}, prm.maps))
+        return TTC_ERR_UNSUPPORTED;
+      // filters: the K x Kg matrix of output channels, K-major
       if (!encode_im2col(&prm.tmA, dt, X, N, H, W, C, R, S, pad_h, pad_w, stride_h, stride_w, dil_h, dil_w) ||
-          !encode_3d(&prm.tmB, dt, 2, Wt, Kg, K, Kg, kBK, pc.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B))
+          !encode_operand(&prm.tmB, dt, 2, Wt, K, Kg, Kg, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_128B))
         return TTC_ERR_CUDA;
       prm.cv_tma = 1;
       prm.cv_cblk = (int)(C / kBK);
@@ -1085,7 +1145,8 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
       prm.group_m = prm.num_m_blocks < gmp ? prm.num_m_blocks : gmp;
       const int nclus = plan_pair_units(prm, pc.bn, pc.clusters);
       if (Kg > 0 && prm.tail_from < prm.num_units) {
-        if (!encode_3d(&prm.tmBh, dt, 2, Wt, Kg, K, Kg, kBK, pc.bn / 4, CU_TENSOR_MAP_SWIZZLE_128B)) return TTC_ERR_CUDA;
+        if (!encode_operand(&prm.tmBh, dt, 2, Wt, K, Kg, Kg, prm.maps.b_half, CU_TENSOR_MAP_SWIZZLE_128B))
+          return TTC_ERR_CUDA;
         prm.b_half_map = 1;
       }
       if (launch_pair(bf16, pc.bn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)

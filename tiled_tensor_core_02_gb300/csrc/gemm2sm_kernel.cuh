@@ -66,6 +66,16 @@ struct PairCfg {
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
 
+// tma_load_boxes for the pair kernel: completion counted on the even CTA's
+// barrier (.cta_group::2).
+// A CTA's share of a pair tile is at most 128 rows (columns): one or two boxes.
+__device__ __forceinline__ void tma_load_boxes_pair(uint8_t* dst, const CUtensorMap* m, const BoxMap bm, int r0,
+                                                    int k0, int z, uint32_t bar_leader, uint64_t pol) {
+  const int x = bm.k_inner ? k0 : r0, y = bm.k_inner ? r0 : k0;
+  tma_load_3d_pair(dst, m, x, y, z, bar_leader, pol);
+  if (bm.boxes > 1) tma_load_3d_pair(dst + bm.smem_step, m, x + bm.box_step, y, z, bar_leader, pol);
+}
+
 template <int BN, bool kBF16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
@@ -144,19 +154,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         int t, n_off;
         bool half;
-        pair_unit(p, u, kPairBN / 2, t, n_off, half);
+        pair_unit(p, u, p.maps.half_n, t, n_off, half);
         int bz, mb, nb;
         tile_coords(t, p, bz, mb, nb);
         const int za = bz * p.a_bc, zb = bz * p.b_bc;
-        const int m0 = mb * kPairBM + (int)rank * 128;  // this CTA's A rows
-        // this CTA's B columns: a half unit uses the first kBHalf / 2 of the
+        const int m0 = mb * p.maps.tile_m + (int)rank * p.maps.cta_m;  // this CTA's A rows
+        // this CTA's B columns: a half unit uses the first cta_n_half of the
         // usual box, and loads only those where it can (MN-major slabs of 64
         // columns, or the half-width map of a K-major B); otherwise it loads the
         // whole box and the rest is not read
-        const int n0 = nb * kPairBN + n_off + (int)rank * (half ? PairCfg::kBHalf / 2 : PairCfg::kBHalf);
+        const int n0 = nb * p.maps.tile_n + n_off + (int)rank * (half ? p.maps.cta_n_half : p.maps.cta_n);
         const bool b_half_box = half && (p.b_mn || p.b_half_map);
-        const int b_bytes = b_half_box ? PairCfg::kBHalfBytes / 2 : PairCfg::kBHalfBytes;
-        const int b_slabs = b_half_box ? (PairCfg::kBHalf / 2 + 63) / 64 : PairCfg::kBHalf / 64;
+        const BoxMap amap = p.maps.a;
+        const BoxMap bmap = b_half_box ? p.maps.b_half : p.maps.b;
+        const CUtensorMap* tmb = b_half_box && !p.b_mn ? &p.tmBh : &p.tmB;
+        const int kblock_tx = amap.boxes * amap.smem_step + bmap.boxes * bmap.smem_step;
         // convolution: window corner of output pixel m0 (rows past the end start
         // beyond the last image, where the im2col box reads zeros)
         int cv_n = 0, cv_h0 = 0, cv_w0 = 0;
@@ -176,7 +188,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           const uint32_t full_leader = mapa_shared(smem_u32(&full[stage]), 0);
           if (leader) {
-            mbar_arrive_expect_tx(&full[stage], 2 * nkb * (PairCfg::kAHalfBytes + b_bytes));
+            mbar_arrive_expect_tx(&full[stage], 2 * nkb * kblock_tx);
             armed_mask |= 1u << stage;
             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
           }
@@ -192,18 +204,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
               const int ss = tap - rr * p.cv_s;
               tma_load_im2col_4d_pair(a, &p.tmA, c0, cv_w0, cv_h0, cv_n, (uint16_t)(ss * p.cv_dw),
                                       (uint16_t)(rr * p.cv_dh), full_leader, pol_a);
-            } else if (!p.a_mn) {
-              tma_load_3d_pair(a, &p.tmA, k0, m0, za, full_leader, pol_a);
             } else {
-              tma_load_3d_pair(a, &p.tmA, m0, k0, za, full_leader, pol_a);
-              tma_load_3d_pair(a + 8192, &p.tmA, m0 + 64, k0, za, full_leader, pol_a);
+              tma_load_boxes_pair(a, &p.tmA, amap, m0, k0, za, full_leader, pol_a);
             }
-            if (!p.b_mn) {
-              tma_load_3d_pair(b, b_half_box ? &p.tmBh : &p.tmB, k0, n0, zb, full_leader, pol_b);
-            } else {
-              for (int h = 0; h < b_slabs; ++h)
-                tma_load_3d_pair(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, full_leader, pol_b);
-            }
+            tma_load_boxes_pair(b, tmb, bmap, n0, k0, zb, full_leader, pol_b);
           }
           if (++stage == S) {
             stage = 0;
@@ -292,31 +296,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     int buf = 0;
     int it = 0;
     const bool has_k = p.num_k_blocks > 0;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    // this thread's accumulator row within the CTA's half of a tile, and the
+    // TMEM address of its warp's first row
+    const int row_in_tile = (q * 32 + lane) * p.maps.epi_row_step;
+    const uint32_t lane_base = (uint32_t)(q * 32) * p.maps.tmem_row_step;
+    const int chunk = p.maps.epi_chunk;
     // this thread's row of a tile's C, toward L2 one tile ahead of its epilogue
     // (the first tile's during the first mainloop)
     auto prefetch_c = [&](int unit) {
       if (unit >= p.num_units || p.beta == 0.0f) return;
       int pt, pn_off;
       bool phalf;
-      pair_unit(p, unit, kPairBN / 2, pt, pn_off, phalf);
+      pair_unit(p, unit, p.maps.half_n, pt, pn_off, phalf);
       int pbz, pmb, pnb;
       tile_coords(pt, p, pbz, pmb, pnb);
-      c_prefetch_row(p, epi_ptrs(p, pbz, 2), pmb * kPairBM + (int)rank * 128 + q * 32 + lane,
-                     pnb * kPairBN + pn_off, phalf ? kPairBN / 2 : kPairBN);
+      c_prefetch_row(p, epi_ptrs(p, pbz, 2), pmb * p.maps.tile_m + (int)rank * p.maps.cta_m + row_in_tile,
+                     pnb * p.maps.tile_n + pn_off, phalf ? p.maps.half_n : p.maps.tile_n);
     };
     if (part == 0) prefetch_c(pair);
     for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
       int t, n_off;
       bool half;
-      pair_unit(p, u, kPairBN / 2, t, n_off, half);
+      pair_unit(p, u, p.maps.half_n, t, n_off, half);
       const int chunks = (half ? kPairBN / 2 : kPairBN) / kEpiCols;
       const int acc = it & 1;
       int bz, mb, nb;
       tile_coords(t, p, bz, mb, nb);
-      const int m0 = mb * kPairBM + (int)rank * 128;
-      const int n0 = nb * kPairBN + n_off;
-      const int grow = m0 + q * 32 + lane;
+      const int m0 = mb * p.maps.tile_m + (int)rank * p.maps.cta_m;
+      const int n0 = nb * p.maps.tile_n + n_off;
+      const int grow = m0 + row_in_tile;
       const bool row_ok = grow < p.M;
       const EpiPtrs ep = epi_ptrs(p, bz, 2);
       if (part == 0) prefetch_c(u + num_pairs);
@@ -324,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
       // the first chunk's C is fetched before waiting for the accumulator
       CChunk16 cc;
-      c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * kEpiCols), grow, n0 + c_lo * kEpiCols, lane, cc);
+      c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * chunk), grow, n0 + c_lo * chunk, lane, cc);
       if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
       tc_fence_after();
       if (c_lo == c_hi) {
@@ -334,10 +342,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       }
 #pragma unroll 1
       for (int c = c_lo; c < c_hi; ++c) {
-        const int gcol0 = n0 + c * kEpiCols;
+        const int gcol0 = n0 + c * chunk;
         uint32_t r[32];
         if (has_k) {
-          tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * kEpiCols, r);
+          tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * chunk, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -350,13 +358,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
         uint32_t packed[16];
-        const int cpath = c_path(p, ep, gcol0);
-        uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, PairCfg::kEpiBufBytes, lane);
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
-        if (c + 1 < c_hi)
-          c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
-        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, PairCfg::kEpiBufBytes, buf, lane,
-                           ep);
+        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
+        if (c + 1 < c_hi) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
+        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
+                           PairCfg::kEpiBufBytes, buf, lane, ep);
       }
     }
     if (p.d_tma && lane == 0) bulk_wait_all();

@@ -32,6 +32,7 @@
 #include <cuda_fp16.h>
 
 #include "ptx.cuh"
+#include "tile_maps.h"
 #include "ttc_layout.hpp"
 
 namespace ttc {
@@ -104,7 +105,6 @@ struct GemmParams {
   const void* B;
   int64_t lda, ldb;
   int a_vec, b_vec;  // generic modes: 1 when 8-element groups may be read as one vector
-  int a_boxes;       // TMA modes: 64-row (MN-major) boxes of A per k-block, 1 or 2
   uint32_t stage_tx; // TMA modes: bytes the loads of one k-block deliver.  When M < 128
                      // only the rows that exist are loaded; the rest of the A tile keeps
                      // stale data, which only reaches accumulator rows that are never stored
@@ -153,12 +153,31 @@ struct GemmParams {
   // tail_from + (u - tail_from) / 2), so that a last, partial wave keeps twice
   // as many pairs busy for half as long.  tail_from == num_units: whole tiles.
   int tail_from, num_units;
+  // tile origins, per-CTA shares, TMA boxes and the epilogue's thread maps,
+  // derived on the host from the operand, output and TMEM layouts
+  TileMaps maps;
   // CTA-pair kernel, K-major B: tmBh has boxes of a half unit's width per CTA
   // (BN / 4 columns), so that half units stage only the B columns they use
   // (b_half_map == 1; otherwise they load the whole box and read half of it)
   int b_half_map;
   CUtensorMap tmBh;
 };
+
+// Loads the k-block tile of an operand whose rows start at r0 and whose K
+// starts at k0 as bm.boxes TMA boxes (see BoxMap; at most kMaxBoxes): box h
+// starts h * box_step further along the contiguous mode and h * smem_step
+// bytes further in shared memory.  Unrolled, with no loop: the producer
+// thread is on the MMA's critical path (a runtime loop here measured 7 %
+// slower on 8192^3).
+constexpr int kMaxBoxes = 4;  // an MN-major B tile 256 wide: four 64-column slabs
+template <int kMax = kMaxBoxes>
+__device__ __forceinline__ void tma_load_boxes(uint8_t* dst, const CUtensorMap* m, const BoxMap bm, int r0, int k0,
+                                               int z, uint64_t* bar, uint64_t pol) {
+  const int x = bm.k_inner ? k0 : r0, y = bm.k_inner ? r0 : k0;
+#pragma unroll
+  for (int h = 0; h < kMax; ++h)
+    if (h == 0 || h < bm.boxes) tma_load_3d(dst + h * bm.smem_step, m, x + h * bm.box_step, y, z, bar, pol);
+}
 
 // Tile and column offset of work unit u of the CTA-pair walk (see tail_from).
 __device__ __forceinline__ void pair_unit(const GemmParams& p, int u, int half_cols, int& t, int& n_off, bool& half) {
@@ -459,10 +478,81 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
 enum CPath : int {
   kCNone = 0,   // beta == 0: C is not read
   kCVec = 1,    // each thread loads its own row's 64 bytes as four 16-byte vectors
-  kCCoop = 2,   // C is not 16-byte aligned: lane l loads column gcol0 + l of the warp's
-                // 32 rows (one 64-byte segment per instruction), transposed in shared memory
+  kCRow = 2,    // C's rows are not 16-byte aligned: each thread loads the five aligned
+                // 16-byte blocks that cover its row's 64 bytes and shifts them into place
   kCTrans = 3,  // D^T orientation: lanes already hold consecutive elements of a C row
 };
+
+// ------------------------------------------------------------------ rows at any 2-byte boundary
+// A 32-element segment of a 16-bit row (64 bytes) that starts at an address
+// a with phase = a mod 16 lies in the 80-byte window of five aligned 16-byte
+// blocks from a - phase.  The window is held as 20 words; the shifts move its
+// bytes by `phase` (even, 0..14) in three conditional stages of 8, 4 and 2
+// bytes, so no register is indexed at run time.  Only an aligned block that
+// holds at least one byte of the segment is ever loaded or stored: such a
+// block lies in the same memory page as that byte.
+
+// Moves the window's bytes up by `phase`: byte i goes to i + phase.
+__device__ __forceinline__ void window_shift_up(uint32_t (&x)[20], uint32_t phase) {
+  const bool s8 = phase & 8, s4 = phase & 4, s2 = phase & 2;
+#pragma unroll
+  for (int k = 19; k >= 2; --k) x[k] = s8 ? x[k - 2] : x[k];
+  x[1] = s8 ? 0u : x[1];
+  x[0] = s8 ? 0u : x[0];
+#pragma unroll
+  for (int k = 19; k >= 1; --k) x[k] = s4 ? x[k - 1] : x[k];
+  x[0] = s4 ? 0u : x[0];
+#pragma unroll
+  for (int k = 19; k >= 1; --k) x[k] = s2 ? __byte_perm(x[k - 1], x[k], 0x5432) : x[k];
+  x[0] = s2 ? x[0] << 16 : x[0];
+}
+
+// Moves the window's bytes down by `phase`: byte i + phase goes to i.
+__device__ __forceinline__ void window_shift_down(uint32_t (&x)[20], uint32_t phase) {
+  const bool s8 = phase & 8, s4 = phase & 4, s2 = phase & 2;
+#pragma unroll
+  for (int k = 0; k < 18; ++k) x[k] = s8 ? x[k + 2] : x[k];
+#pragma unroll
+  for (int k = 0; k < 19; ++k) x[k] = s4 ? x[k + 1] : x[k];
+#pragma unroll
+  for (int k = 0; k < 19; ++k) x[k] = s2 ? __byte_perm(x[k], x[k + 1], 0x5432) : x[k];
+}
+
+// Writes bytes [s, e) (even offsets, 0 <= s < e <= 16) of the aligned 16-byte
+// block v to `blk` with aligned 8-, 4- and 2-byte stores.
+__device__ __forceinline__ void store_block_part(uint8_t* blk, const uint4 v, int s, int e) {
+  int b = s;
+#pragma unroll 1
+  while (b < e) {
+    const int wi = b >> 2;
+    const uint32_t word = wi == 0 ? v.x : wi == 1 ? v.y : wi == 2 ? v.z : v.w;
+    if ((b & 7) == 0 && b + 8 <= e) {
+      *reinterpret_cast<uint2*>(blk + b) = make_uint2(word, wi == 0 ? v.y : v.w);
+      b += 8;
+    } else if ((b & 3) == 0 && b + 4 <= e) {
+      *reinterpret_cast<uint32_t*>(blk + b) = word;
+      b += 4;
+    } else {
+      *reinterpret_cast<uint16_t*>(blk + b) = (uint16_t)(word >> ((b & 2) * 8));
+      b += 2;
+    }
+  }
+}
+
+// Stores bytes [lo, hi) of the window x, which starts at the aligned `base`:
+// whole blocks as 16-byte vectors, the partial ones in pieces.
+__device__ __forceinline__ void store_window(uint8_t* base, const uint32_t (&x)[20], int lo, int hi) {
+#pragma unroll
+  for (int blk = 0; blk < 5; ++blk) {
+    const int s = max(lo - 16 * blk, 0), e = min(hi - 16 * blk, 16);
+    if (s >= e) continue;
+    const uint4 v = make_uint4(x[4 * blk], x[4 * blk + 1], x[4 * blk + 2], x[4 * blk + 3]);
+    if (s == 0 && e == 16)
+      *reinterpret_cast<uint4*>(base + 16 * blk) = v;
+    else
+      store_block_part(base + 16 * blk, v, s, e);
+  }
+}
 
 // The C and D of the batch a tile belongs to, and its batch index (the TMA
 // store's third coordinate).
@@ -485,7 +575,7 @@ __device__ __forceinline__ int c_path(const GemmParams& p, const EpiPtrs& e, int
   if (p.d_trans) return kCTrans;
   const bool vec =
       ((p.ldc & 7) == 0) && ((reinterpret_cast<uintptr_t>(e.C) & 15) == 0) && (gcol0 + 32 <= p.N);
-  return vec ? kCVec : kCCoop;
+  return vec ? kCVec : kCRow;
 }
 
 // Pulls row `grow` of a tile's C, columns [n0, n0 + ncols), toward L2 ahead of
@@ -504,9 +594,9 @@ __device__ __forceinline__ void c_prefetch_row(const GemmParams& p, const EpiPtr
 // C values of one chunk, fetched one chunk ahead of their use so that the
 // load latency overlaps the previous chunk's work.
 struct CChunk16 {
-  uint4 v[4];       // kCVec: this thread's row, 32 values
-  uint16_t e[32];   // kCCoop: column (gcol0 + lane) of the warp's 32 rows (kept unpacked: the
-                    // loads are not waited on until the values are staged, a chunk later)
+  uint4 v[5];      // kCVec: this thread's row, 32 values in v[0..3]; kCRow: the five aligned
+                   // blocks that cover them
+  uint32_t phase;  // kCRow: the row segment's address mod 16
 };
 
 __device__ __forceinline__ void c_fetch16(const GemmParams& p, const EpiPtrs& e, int path, int grow, int gcol0,
@@ -521,29 +611,30 @@ __device__ __forceinline__ void c_fetch16(const GemmParams& p, const EpiPtrs& e,
 #pragma unroll
       for (int u = 0; u < 4; ++u) cc.v[u] = make_uint4(0u, 0u, 0u, 0u);
     }
-  } else if (path == kCCoop) {
-    const int row0 = grow - lane;
-    const int col = gcol0 + lane;
-    const uint16_t* cbase = reinterpret_cast<const uint16_t*>(e.C);
+  } else if (path == kCRow) {
+    cc.phase = 0;
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int g = row0 + rr;
-      cc.e[rr] = (g < p.M && col < p.N) ? __ldg(cbase + (int64_t)g * p.ldc + col) : (uint16_t)0;
+    for (int u = 0; u < 5; ++u) cc.v[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (grow < p.M && gcol0 < p.N) {
+      const uint8_t* a = reinterpret_cast<const uint8_t*>(e.C) + ((int64_t)grow * p.ldc + gcol0) * 2;
+      const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15u);
+      const int hi = (int)ph + 2 * min(32, p.N - gcol0);  // the segment's bytes in the window
+      const uint4* base = reinterpret_cast<const uint4*>(a - ph);
+      cc.phase = ph;
+#pragma unroll
+      for (int u = 0; u < 5; ++u)
+        if (16 * u < hi) cc.v[u] = __ldg(base + u);
     }
   }
 }
 
 // fp16/bf16 epilogue of one 32-column chunk of the calling thread's row:
 // v = alpha * acc (+ beta * C) (+ bias), activation, round to nearest even.
-// `cc` holds this chunk's C as fetched by c_fetch16 for `cpath`; kCCoop
-// transposes it through `cstage`, 2 KB of shared memory the warp owns for the
-// call (32 x 32 16-bit values, 16-byte words XOR-swizzled by row so that both
-// the column-wise writes and the row-wise reads are free of bank conflicts).
+// `cc` holds this chunk's C as fetched by c_fetch16 for `cpath`.
 template <bool kBF16>
 __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32_t (&r)[32], bool row_ok,
                                                int grow, int gcol0, uint32_t (&packed)[16], int cpath,
-                                               const CChunk16& cc, uint8_t* cstage, int lane,
-                                               const EpiPtrs& e) {
+                                               const CChunk16& cc, const EpiPtrs& e) {
   float v[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) v[j] = p.alpha * __uint_as_float(r[j]);
@@ -569,20 +660,23 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
         }
       }
     }
-  } else if (cpath == kCCoop) {
-    uint16_t* w16 = reinterpret_cast<uint16_t*>(cstage);
+  } else if (cpath == kCRow) {
+    if (row_ok) {
+      uint32_t x[20];
 #pragma unroll
-    for (int rr = 0; rr < 32; ++rr) {
-      const int word = rr * 16 + ((lane >> 1) ^ ((rr >> 1) & 15));
-      w16[word * 2 + (lane & 1)] = cc.e[rr];
-    }
-    __syncwarp();
+      for (int u = 0; u < 5; ++u) {
+        x[4 * u] = cc.v[u].x;
+        x[4 * u + 1] = cc.v[u].y;
+        x[4 * u + 2] = cc.v[u].z;
+        x[4 * u + 3] = cc.v[u].w;
+      }
+      window_shift_down(x, cc.phase);
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const int word = lane * 16 + ((j >> 1) ^ ((lane >> 1) & 15));
-      v[j] = fmaf(p.beta, half_bits_to_float<kBF16>(w16[word * 2 + (j & 1)]), v[j]);
+      for (int h = 0; h < 16; ++h) {
+        v[2 * h] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(x[h] & 0xFFFFu)), v[2 * h]);
+        v[2 * h + 1] = fmaf(p.beta, half_bits_to_float<kBF16>((uint16_t)(x[h] >> 16)), v[2 * h + 1]);
+      }
     }
-    __syncwarp();
   }
   if (p.bias != nullptr) {
     if (p.d_trans) {
@@ -603,18 +697,6 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) packed[j] = pack2<kBF16>(v[2 * j], v[2 * j + 1]);
-}
-
-// Shared memory the kCCoop path may use for one chunk: with TMA stores, the
-// staging buffer the next store will use, once its previous store has
-// finished reading it; with plain stores, the warp's first staging buffer.
-__device__ __forceinline__ uint8_t* c_stage_buffer(const GemmParams& p, int cpath, uint8_t* stage_buf, int buf,
-                                                   int buf_bytes, int lane) {
-  if (cpath != kCCoop) return nullptr;
-  if (!p.d_tma) return stage_buf;
-  if (lane == 0) bulk_wait_read<1>();
-  __syncwarp();
-  return stage_buf + buf * buf_bytes;
 }
 
 // Writes one 32-column chunk of the calling thread's row: through a swizzled
@@ -653,6 +735,20 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
       bulk_commit();
     }
     buf ^= 1;
+  } else if (kOutBytes == 2 && !p.d_trans) {
+    // 16-bit rows TMA cannot describe: each thread stores its own row's
+    // 64 bytes as the aligned blocks that cover them
+    if (row_ok && gcol0 < p.N) {
+      uint8_t* a = reinterpret_cast<uint8_t*>(e.D) + ((int64_t)grow * p.ldd + gcol0) * 2;
+      const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15u);
+      uint32_t x[20];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = packed[j];
+#pragma unroll
+      for (int j = 16; j < 20; ++j) x[j] = 0u;
+      window_shift_up(x, ph);
+      store_window(a - ph, x, (int)ph, (int)ph + 2 * min(32, p.N - gcol0));
+    }
   } else if (!p.d_trans) {
     // plain stores, coalesced through the warp's staging area (both buffers):
     // each thread writes its row, then lane l stores column gcol0 + l of the
@@ -800,8 +896,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
           int bz, mb, nb;
           tile_coords(t, p, bz, mb, nb);
-          const int m0 = mb * kBM, n0 = nb * BN;
+          const int m0 = mb * p.maps.tile_m, n0 = nb * p.maps.tile_n;
           const int za = bz * p.a_bc, zb = bz * p.b_bc;
+          const BoxMap am = p.maps.a, bmp = p.maps.b;
           for (int kb = k_lo; kb < k_hi; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, wc)) {
               ok = false;
@@ -811,19 +908,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* a = sA + stage * kABytes;
             uint8_t* b = sB + stage * Cfg::kBBytes;
             const int k0 = kb * kBK;
-            if (!p.a_mn) {
-              tma_load_3d(a, &p.tmA, k0, m0, za, &full[stage], pol_a);
-            } else {
-              tma_load_3d(a, &p.tmA, m0, k0, za, &full[stage], pol_a);
-              if (p.a_boxes > 1) tma_load_3d(a + kABytes / 2, &p.tmA, m0 + 64, k0, za, &full[stage], pol_a);
-            }
-            if (!p.b_mn) {
-              tma_load_3d(b, &p.tmB, k0, n0, zb, &full[stage], pol_b);
-            } else {
-#pragma unroll
-              for (int h = 0; h < BN / 64; ++h)
-                tma_load_3d(b + h * 8192, &p.tmB, n0 + 64 * h, k0, zb, &full[stage], pol_b);
-            }
+            tma_load_boxes(a, &p.tmA, am, m0, k0, za, &full[stage], pol_a);
+            tma_load_boxes(b, &p.tmB, bmp, n0, k0, zb, &full[stage], pol_b);
             issued_mask |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == S) {
@@ -852,8 +938,9 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
             int bz, mb, nb;
             tile_coords(t, p, bz, mb, nb);
-            const int m0 = mb * kBM, n0 = nb * BN;
+            const int m0 = mb * p.maps.tile_m, n0 = nb * p.maps.tile_n;
             const int za = bz * p.a_bc, zb = bz * p.b_bc;
+            const BoxMap am = p.maps.a, bmp = p.maps.b;
             for (int kb = k_lo; kb < k_hi; ++kb) {
               if (!mbar_wait(&empty8[st8], ph8 ^ 1u, wc)) {
                 ok = false;
@@ -863,14 +950,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               uint8_t* a = s8 + st8 * Cfg::kStage8Bytes;
               uint8_t* b = a + kBM * kBK;
               const int k0 = kb * kBK;
-              if (!p.a_mn)
-                tma_load_3d(a, &p.tmA, k0, m0, za, &full8[st8], pol_a);
-              else
-                tma_load_3d(a, &p.tmA, m0, k0, za, &full8[st8], pol_a);
-              if (!p.b_mn)
-                tma_load_3d(b, &p.tmB, k0, n0, zb, &full8[st8], pol_b);
-              else
-                tma_load_3d(b, &p.tmB, n0, k0, zb, &full8[st8], pol_b);
+              tma_load_boxes(a, &p.tmA, am, m0, k0, za, &full8[st8], pol_a);
+              tma_load_boxes(b, &p.tmB, bmp, n0, k0, zb, &full8[st8], pol_b);
               issued_mask |= 1u << st8;
               issued_parity = (issued_parity & ~(1u << st8)) | (ph8 << st8);
               if (++st8 == S8) {
@@ -930,7 +1011,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       for (int t = cluster_id; t < p.num_tiles; t += num_clusters) {
         int bz, mb, nb;
         tile_coords(t, p, bz, mb, nb);
-        const int m0 = mb * kBM, n0 = nb * BN;
+        const int m0 = mb * p.maps.tile_m, n0 = nb * p.maps.tile_n;
         constexpr int kInBytes = kI8 ? 1 : 2;
         const void* Ab = static_cast<const char*>(p.A) + (int64_t)bz * p.a_bs * kInBytes;
         const void* Bb = static_cast<const char*>(p.B) + (int64_t)bz * p.b_bs * kInBytes;
@@ -1035,18 +1116,19 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - Tr::kEpiWarp0;  // epilogue warp 0..3 (owns a staging area)
     const int q = warp & 3;               // TMEM lane quarter this warp may access
-    const int row_in_tile = q * 32 + lane;
+    const int row_in_tile = (q * 32 + lane) * p.maps.epi_row_step;
     uint8_t* stage_buf = sEpi + ew * 2 * Tr::kEpiBufBytes;
     int buf = 0;
     int unit = 0;
     const bool has_k = nkb > 0;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const uint32_t lane_base = (uint32_t)(q * 32) * p.maps.tmem_row_step;
+    const int chunk = p.maps.epi_chunk;
     bool ok = true;
     int red_it = 0;  // split-K: partial-sum chunks exchanged so far
     for (int t = cluster_id; ok && t < p.num_tiles; t += num_clusters) {
       int bz, mb, nb;
       tile_coords(t, p, bz, mb, nb);
-      const int m0 = mb * kBM, n0 = nb * BN;
+      const int m0 = mb * p.maps.tile_m, n0 = nb * p.maps.tile_n;
       const int grow = m0 + row_in_tile;
       const bool row_ok = grow < p.M;
       const EpiPtrs ep = epi_ptrs(p, bz, Tr::kOutBytes);
@@ -1067,13 +1149,13 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
 #pragma unroll 1
             for (int c = 0; c < BN / kEpiCols; ++c) {
               uint32_t r[32], sm[32];
-              tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * kEpiCols, r);
-              if (u > 0) tmem_ld_32x32b_x32(sum_cols + c * kEpiCols, sm);
+              tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * chunk, r);
+              if (u > 0) tmem_ld_32x32b_x32(sum_cols + c * chunk, sm);
               tmem_ld_wait();
 #pragma unroll
               for (int j = 0; j < 32; ++j)
                 sm[j] = (uint32_t)((u > 0 ? (int32_t)sm[j] : 0) + __float2int_rn(__uint_as_float(r[j])));
-              tmem_st_32x32b_x32(sum_cols + c * kEpiCols, sm);
+              tmem_st_32x32b_x32(sum_cols + c * chunk, sm);
             }
             tmem_st_wait();
           }
@@ -1096,14 +1178,14 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
 
 #pragma unroll 1
       for (int c = 0; c < BN / kEpiCols; ++c) {
-        const int gcol0 = n0 + c * kEpiCols;
+        const int gcol0 = n0 + c * chunk;
         uint32_t packed[Tr::kOutBytes == 4 ? 32 : 16];
         if constexpr (kI8) {
           // D = sum (+ C when beta == 1); alpha == 1 (checked on the host)
           int32_t v[32];
           if (has_k) {
             uint32_t sm[32];
-            tmem_ld_32x32b_x32(sum_cols + c * kEpiCols, sm);
+            tmem_ld_32x32b_x32(sum_cols + c * chunk, sm);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = (int32_t)sm[j];
@@ -1140,7 +1222,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
         } else {
           uint32_t r[32];
           if (has_k) {
-            tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * kEpiCols, r);
+            tmem_ld_32x32b_x32(tmem_base + lane_base + acc * BN + c * chunk, r);
             tmem_ld_wait();
           } else {
 #pragma unroll
@@ -1200,14 +1282,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
                 for (int pr = 1; pr < p.ksplit; ++pr) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(re), (uint32_t)pr));
             }
           }
-          const int cpath = c_path(p, ep, gcol0);
-          uint8_t* cstage = c_stage_buffer(p, cpath, stage_buf, buf, Tr::kEpiBufBytes, lane);
-          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, cpath, cc, cstage, lane, ep);
-          if (c + 1 < BN / kEpiCols)
-            c_fetch16(p, ep, c_path(p, ep, gcol0 + kEpiCols), grow, gcol0 + kEpiCols, lane, cc);
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
+          if (c + 1 < BN / kEpiCols) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
         }
 
-        epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, m0 + q * 32, stage_buf, Tr::kEpiBufBytes, buf,
+        epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf, Tr::kEpiBufBytes, buf,
                                        lane, ep);
       }
       if constexpr (!kI8) ++unit;

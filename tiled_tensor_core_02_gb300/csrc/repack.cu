@@ -5,58 +5,121 @@
 //
 // The matrix is taken in memory order: `rows` rows of `cols` contiguous
 // elements, `src_ld` elements apart (for a column-major operand the "rows"
-// are its columns).  Each thread writes one 16-byte chunk of a destination
-// row; elements past `cols` in the last chunk are written as zero (they lie
-// in the row's padding, which TMA never reads since the tensor map keeps the
-// true extent).  Reads are element-wise (the source is only element-aligned)
-// and coalesced across the warp.
+// are its columns).  One launch copies up to two matrices (A and B).
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
+#include "gemm_kernel.cuh"
 #include "repack.cuh"
 
 namespace ttc {
 
-template <typename T>
-__global__ void __launch_bounds__(256) repack_rows_kernel(const T* __restrict__ src, int64_t src_ld, int64_t rows,
-                                                          int64_t cols, T* __restrict__ dst, int64_t dst_ld) {
-  constexpr int V = 16 / (int)sizeof(T);
-  const int64_t chunks_per_row = (cols + V - 1) / V;
-  const int64_t total = rows * chunks_per_row;
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t r = idx / chunks_per_row;
-    const int64_t c0 = (idx - r * chunks_per_row) * V;
-    const T* s = src + r * src_ld + c0;
-    union {
-      T e[V];
-      uint4 u;
-    } v;
+// One matrix of a repack launch, in bytes.
+struct RepackJob {
+  const uint8_t* src;
+  int64_t src_ld;  // bytes between source rows
+  int64_t rows;
+  int64_t cols;    // bytes per row
+  uint8_t* dst;
+  int64_t dst_ld;  // bytes between destination rows (a multiple of 16)
+  int64_t chunks_per_row;
+  int64_t first;   // index of the job's first 16-byte chunk among the launch's chunks
+};
+
+struct RepackParams {
+  RepackJob job[2];
+  int jobs;
+  int64_t total;  // chunks of all jobs
+};
+
+// Bytes i + phase of the 8-word window go to i (phase 0..15), in stages of
+// 8, 4, 2 and 1 bytes.
+__device__ __forceinline__ void window8_shift_down(uint32_t (&x)[8], uint32_t phase) {
+  const bool s8 = phase & 8, s4 = phase & 4, s2 = phase & 2, s1 = phase & 1;
 #pragma unroll
-    for (int j = 0; j < V; ++j) v.e[j] = (c0 + j < cols) ? __ldg(s + j) : T(0);
-    *reinterpret_cast<uint4*>(dst + r * dst_ld + c0) = v.u;
+  for (int k = 0; k < 6; ++k) x[k] = s8 ? x[k + 2] : x[k];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) x[k] = s4 ? x[k + 1] : x[k];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) x[k] = s2 ? __byte_perm(x[k], x[k + 1], 0x5432) : x[k];
+#pragma unroll
+  for (int k = 0; k < 7; ++k) x[k] = s1 ? __byte_perm(x[k], x[k + 1], 0x4321) : x[k];
+}
+
+// Each thread writes one 16-byte chunk of a destination row.  Its source
+// bytes start at any alignment: the thread loads the one or two aligned
+// 16-byte blocks that hold them (only blocks with at least one byte of the
+// row's data, so never one outside the memory pages the matrix occupies) and
+// shifts the bytes into place in registers.  Bytes past the row's end are
+// written as zero (the padding, which TMA never reads since the tensor map
+// keeps the true extent).  Launched with programmatic dependent launch: it
+// waits for the previous grid before its first global access and lets the
+// next grid (the GEMM, which waits for this one in turn) start its prologue.
+__global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant__ RepackParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" :::);
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < p.total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const RepackJob& j = (p.jobs > 1 && idx >= p.job[1].first) ? p.job[1] : p.job[0];
+    const int64_t q = idx - j.first;
+    const int64_t r = q / j.chunks_per_row;
+    const int64_t c0 = (q - r * j.chunks_per_row) * 16;
+    const int64_t n = j.cols - c0 < 16 ? j.cols - c0 : 16;  // bytes of the row in this chunk
+    const uint8_t* s = j.src + r * j.src_ld + c0;
+    const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(s) & 15u);
+    const uint4* blk = reinterpret_cast<const uint4*>(s - ph);
+    const uint4 b0 = __ldg(blk);
+    const uint4 b1 = (int64_t)ph + n > 16 ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
+    uint32_t x[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    window8_shift_down(x, ph);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t keep = n - 4 * k;  // bytes of word k inside the row
+      x[k] = keep >= 4 ? x[k] : keep <= 0 ? 0u : (x[k] & ((1u << (8 * keep)) - 1u));
+    }
+    *reinterpret_cast<uint4*>(j.dst + r * j.dst_ld + c0) = make_uint4(x[0], x[1], x[2], x[3]);
   }
+}
+
+cudaError_t launch_repack2(const RepackSpec* specs, int count, int sm_count, cudaStream_t stream) {
+  if (count < 1 || count > 2) return cudaErrorInvalidValue;
+  RepackParams p{};
+  p.jobs = count;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    const RepackSpec& sp = specs[i];
+    RepackJob& j = p.job[i];
+    j.src = static_cast<const uint8_t*>(sp.src);
+    j.src_ld = sp.src_ld * sp.elem_bytes;
+    j.rows = sp.rows;
+    j.cols = sp.cols * sp.elem_bytes;
+    j.dst = static_cast<uint8_t*>(sp.dst);
+    j.dst_ld = sp.dst_ld * sp.elem_bytes;
+    if (j.dst_ld % 16 || reinterpret_cast<uintptr_t>(j.dst) % 16 || j.dst_ld < j.cols) return cudaErrorInvalidValue;
+    j.chunks_per_row = (j.cols + 15) / 16;
+    j.first = total;
+    total += j.rows * j.chunks_per_row;
+  }
+  p.total = total;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, repack_rows_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_repack(const void* src, int64_t src_ld, int64_t rows, int64_t cols, void* dst, int64_t dst_ld,
                           int elem_bytes, int sm_count, cudaStream_t stream) {
-  const int64_t v = 16 / elem_bytes;
-  const int64_t chunks = rows * ((cols + v - 1) / v);
-  int64_t blocks = (chunks + 255) / 256;
-  const int64_t cap = (int64_t)sm_count * 8;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  if (elem_bytes == 4)
-    repack_rows_kernel<uint32_t><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint32_t*>(src), src_ld, rows, cols, static_cast<uint32_t*>(dst), dst_ld);
-  else if (elem_bytes == 2)
-    repack_rows_kernel<uint16_t><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint16_t*>(src), src_ld, rows, cols, static_cast<uint16_t*>(dst), dst_ld);
-  else
-    repack_rows_kernel<uint8_t><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const uint8_t*>(src), src_ld, rows, cols, static_cast<uint8_t*>(dst), dst_ld);
-  return cudaGetLastError();
+  const RepackSpec sp{src, src_ld, rows, cols, dst, dst_ld, elem_bytes};
+  return launch_repack2(&sp, 1, sm_count, stream);
 }
 
 // The reverse copy: rows of an aligned, padded-pitch matrix back to a

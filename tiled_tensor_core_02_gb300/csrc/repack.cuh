@@ -9,6 +9,17 @@ namespace ttc {
 // Copies `rows` rows of `cols` elements (elem_bytes = 1, 2 or 4), `src_ld`
 // elements apart, to `dst` with pitch `dst_ld` (a multiple of 16 bytes;
 // `dst` 16-byte aligned).
+struct RepackSpec {
+  const void* src;
+  int64_t src_ld, rows, cols;
+  void* dst;
+  int64_t dst_ld;
+  int elem_bytes;
+};
+
+// One launch for one or two such copies (count 1 or 2).
+cudaError_t launch_repack2(const RepackSpec* specs, int count, int sm_count, cudaStream_t stream);
+
 cudaError_t launch_repack(const void* src, int64_t src_ld, int64_t rows, int64_t cols, void* dst, int64_t dst_ld,
                           int elem_bytes, int sm_count, cudaStream_t stream);
 
