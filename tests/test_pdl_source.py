@@ -57,10 +57,11 @@ def _pdl_launched_kernels(srcs):
 
 def test_pdl_launches_found():
     names = _pdl_launched_kernels(_sources())
-    assert {"gemm_kernel", "gemm_pair_kernel", "conv_halo_kernel", "gemv_rows_kernel"} <= names, names
+    assert {"gemm_kernel", "gemm_pair_kernel", "conv_halo_kernel", "gemv_rows_kernel", "repack_rows_kernel"} <= names, names
 
 
-@pytest.mark.parametrize("kernel", ["gemm_kernel", "gemm_pair_kernel", "conv_halo_kernel", "gemv_rows_kernel"])
+@pytest.mark.parametrize("kernel", ["gemm_kernel", "gemm_pair_kernel", "conv_halo_kernel", "gemv_rows_kernel",
+                                    "repack_rows_kernel"])
 def test_kernel_waits_before_global_access(kernel):
     srcs = _sources()
     body = None
@@ -79,9 +80,11 @@ def test_kernel_waits_before_global_access(kernel):
 
 
 def test_launches_without_the_attribute_do_not_signal():
-    """Kernels launched in plain stream order (repack, unpack, transpose) do
-    not signal dependents, so a kernel after them waits for their completion."""
+    """Kernels launched in plain stream order (unpack, transpose) do not
+    signal dependents, so a kernel after them waits for their completion."""
     srcs = _sources()
-    for name in ("repack.cu", "transpose.cu"):
-        assert "grid_dependents_launch" not in srcs[name], name
-        assert "add_pdl_attribute" not in srcs[name], name
+    assert "grid_dependents_launch" not in srcs["transpose.cu"]
+    assert "add_pdl_attribute" not in srcs["transpose.cu"]
+    body = _kernel_body(srcs["repack.cu"], "unpack_rows_kernel")
+    assert body is not None and "grid_dependents_launch" not in body and "griddepcontrol" not in body
+    assert "cudaLaunchKernelEx" not in srcs["repack.cu"].split("launch_unpack(")[-1]

@@ -57,8 +57,8 @@ __device__ __forceinline__ void window8_shift_down(uint32_t (&x)[8], uint32_t ph
 // waits for the previous grid before its first global access and lets the
 // next grid (the GEMM, which waits for this one in turn) start its prologue.
 __global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant__ RepackParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" :::);
+  grid_dependency_wait();
+  grid_dependents_launch();
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < p.total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const RepackJob& j = (p.jobs > 1 && idx >= p.job[1].first) ? p.job[1] : p.job[0];
