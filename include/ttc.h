@@ -198,14 +198,15 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
 
 /*
  * Workspace bytes for ttc_gemm_ws's fastest path: ttc_gemm_workspace_size's
- * operand repack plus, when D's rows cannot be written as 16-byte vectors
- * (ldd times the element size, or D itself, not a multiple of 16 bytes), an
- * aligned copy of D placed after it.  Given a workspace at least this large,
- * ttc_gemm_ws copies C (when beta != 0) into that copy, runs the GEMM on it in
- * place and copies the result to D, all on `stream`; with less it behaves as
- * with ttc_gemm_workspace_size bytes.  The result is the same either way.
- * 0 for invalid or empty arguments and for matrix-vector problems (which use
- * no workspace).  Pure host computation.
+ * operand repack plus, for an int32 D (int8 problems) whose rows cannot be
+ * written as 16-byte vectors (ldd times 4, or D itself, not a multiple of 16
+ * bytes), an aligned copy of D placed after it.  Given a workspace at least
+ * this large, ttc_gemm_ws copies C (when beta != 0) into that copy, runs the
+ * GEMM on it in place and copies the result to D, all on `stream`; with less
+ * it behaves as with ttc_gemm_workspace_size bytes.  The result is the same
+ * either way.  fp16/bf16 outputs need no copy: the GEMM writes rows at any
+ * 2-byte boundary itself.  0 for invalid or empty arguments and for
+ * matrix-vector problems (which use no workspace).  Pure host computation.
  */
 size_t ttc_gemm_workspace_size_staged(int64_t M, int64_t N, int64_t K,
                                       const void* A, int64_t lda, ttc_layout layoutA,

@@ -437,8 +437,9 @@ def test_workspace_int8_odd_pitch(ws):
 
 @pytest.mark.parametrize("beta", [0.0, 1.0])
 def test_workspace_staged_d_in_place_and_padding(beta):
-    """D staged through the workspace: C == D in place at an odd pitch, and
-    the pitch padding of D left untouched."""
+    """The staged workspace size with a bf16 D at an odd pitch (written
+    directly, no copy of D): C == D in place, and the pitch padding of D left
+    untouched."""
     p = synth.Problem(260, 301, 96, dtype="bf16", layoutA="col", layoutB="row", seed=34, distC="uniform",
                       lda=261, ldb=303, ldc=305)
     D = to_dev(p.C.copy())  # C and D share storage, pitch 305
@@ -449,14 +450,17 @@ def test_workspace_staged_d_in_place_and_padding(beta):
     assert np.array_equal(rows[:, p.N:], p.C.reshape(-1)[: p.M * 305].reshape(p.M, 305)[:, p.N:])
 
 
-@pytest.mark.parametrize("pair", [1, 2], ids=["pair", "single"])
+@pytest.mark.parametrize("pair,N", [(1, 300), (2, 77), (1, 320), (2, 96)])
 @pytest.mark.parametrize("c_off,d_off", [(1, 3), (2, 5), (3, 7), (4, 6), (7, 1), (0, 2)])
-def test_unaligned_c_and_d_rows(pair, c_off, d_off):
+def test_unaligned_c_and_d_rows(pair, N, c_off, d_off):
     """C and D rows at every 2-byte phase of a 16-byte block (odd pitches and
     element offsets of the base pointers): the epilogue moves each row segment
-    as the aligned 16-byte blocks that cover it; the last column chunk is
-    partial.  Nothing outside D's M x N elements is written."""
-    M, N, K = 300, 300 if pair == 1 else 77, 128
+    as the aligned 16-byte blocks that cover it, and the block two chunks of a
+    row share is stored once with the second.  N = 300 and 77 end inside a
+    32-column chunk; N = 320 and 96 end at a chunk boundary inside a tile, so
+    the tile's last chunks hold no columns.  Nothing outside D's M x N
+    elements is written."""
+    M, K = 300, 128
     ldc, ldd = N + 3, N + 5
     p = synth.Problem(M, N, K, dtype="bf16", seed=50 + c_off, distC="uniform", dist_bias="normal:0.5", ldc=ldc)
     ttc.ttc_set_knob("pair", pair)

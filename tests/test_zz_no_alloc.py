@@ -64,14 +64,12 @@ def _call(p, entry, alpha, beta, act):
     return D.cpu().numpy().view(np.uint16).reshape(p.M, p.N), launches
 
 
-def _expected_launches(p, beta, d_ptr_aligned=True):
+def _expected_launches(p, beta):
     """Kernels a call launches when the scratch is used: one repack (of every
-    operand whose pitch is not a 16-byte multiple), then, when D's pitch is not
-    one either, the copy of C into the aligned copy of D (beta != 0), the GEMM
-    on it and the copy back; otherwise the GEMM alone."""
+    operand whose pitch is not a 16-byte multiple), then the GEMM, which
+    writes fp16/bf16 rows at any alignment itself."""
     rep = int((p.lda * 2) % 16 != 0 or (p.ldb * 2) % 16 != 0)
-    staged = (p.N * 2) % 16 != 0 or not d_ptr_aligned
-    return rep + (int(beta != 0.0) + 2 if staged else 1)
+    return rep + 1
 
 
 def test_static_scratch_matches_workspace_entry_twice():

@@ -441,9 +441,13 @@ struct DStage {
   int64_t ld = 0;
   size_t off = 0, bytes = 0;
 };
+// Only int32 outputs (int8 problems) are staged: the 16-bit epilogue stores
+// rows at any 2-byte boundary itself (aligned 16-byte blocks shifted in
+// registers), which measured faster than staging (4099 x 3001 x 1023 bf16,
+// beta = 1, tight pitches: 38.6 us per step direct against 52.1 us staged).
 DStage plan_dstage(int64_t M, int64_t N, const void* D, int64_t ldd, int esize, size_t after) {
   DStage d;
-  if (M <= 0 || N <= 0 || tma_ok(D, ldd, esize)) return d;
+  if (esize != 4 || M <= 0 || N <= 0 || tma_ok(D, ldd, esize)) return d;
   d.on = true;
   d.ld = round_up(N, 16 / esize);
   d.off = after;

@@ -340,6 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
       }
+      RowCarry carry{};
 #pragma unroll 1
       for (int c = c_lo; c < c_hi; ++c) {
         const int gcol0 = n0 + c * chunk;
@@ -361,7 +362,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
         if (c + 1 < c_hi) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
         epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
-                           PairCfg::kEpiBufBytes, buf, lane, ep);
+                           PairCfg::kEpiBufBytes, buf, carry, c == c_hi - 1, lane, ep);
       }
     }
     if (p.d_tma && lane == 0) bulk_wait_all();

@@ -539,20 +539,24 @@ __device__ __forceinline__ void store_block_part(uint8_t* blk, const uint4 v, in
   }
 }
 
-// Stores bytes [lo, hi) of the window x, which starts at the aligned `base`:
-// whole blocks as 16-byte vectors, the partial ones in pieces.
-__device__ __forceinline__ void store_window(uint8_t* base, const uint32_t (&x)[20], int lo, int hi) {
-#pragma unroll
-  for (int blk = 0; blk < 5; ++blk) {
-    const int s = max(lo - 16 * blk, 0), e = min(hi - 16 * blk, 16);
-    if (s >= e) continue;
-    const uint4 v = make_uint4(x[4 * blk], x[4 * blk + 1], x[4 * blk + 2], x[4 * blk + 3]);
-    if (s == 0 && e == 16)
-      *reinterpret_cast<uint4*>(base + 16 * blk) = v;
-    else
-      store_block_part(base + 16 * blk, v, s, e);
-  }
+// Stores bytes [s, e) of the aligned block v at blk: one 16-byte vector when
+// whole, pieces otherwise, nothing when empty.
+__device__ __forceinline__ void store_block(uint8_t* blk, const uint4 v, int s, int e) {
+  if (s == 0 && e >= 16)
+    *reinterpret_cast<uint4*>(blk) = v;
+  else if (s < e)
+    store_block_part(blk, v, s, min(e, 16));
 }
+
+// The aligned block a thread's row segment shares with the next 32-column
+// chunk of the same row: consecutive chunks of a row have the same phase, so
+// the last block of one chunk's window is the first block of the next one's,
+// each holding the bytes the other lacks (zeros elsewhere).  Carried over, it
+// is stored once, whole, with the next chunk.
+struct RowCarry {
+  uint4 v;
+  int on;
+};
 
 // The C and D of the batch a tile belongs to, and its batch index (the TMA
 // store's third coordinate).
@@ -703,10 +707,14 @@ __device__ __forceinline__ void epi_f16_values(const GemmParams& p, const uint32
 // shared-memory staging buffer and a TMA store of the warp's 32 x 32 block
 // (rows tile_row .. tile_row + 31), or with predicated stores when TMA cannot
 // describe D.  `buf` alternates between the warp's two staging buffers.
+// `carry` and `last` serve the unaligned 16-bit path: the block shared with
+// the calling thread's next chunk (see RowCarry) and whether this is the last
+// chunk the thread stores of this row.
 template <int kOutBytes, int kPacked>
 __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint32_t (&packed)[kPacked], bool row_ok,
                                                 int grow, int gcol0, int tile_row, uint8_t* stage_buf,
-                                                int buf_bytes, int& buf, int lane, const EpiPtrs& e) {
+                                                int buf_bytes, int& buf, RowCarry& carry, bool last, int lane,
+                                                const EpiPtrs& e) {
   if (p.d_tma) {
     // staging buffer `buf` was last used two chunks ago; its store must
     // have finished reading shared memory
@@ -737,17 +745,41 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
     buf ^= 1;
   } else if (kOutBytes == 2 && !p.d_trans) {
     // 16-bit rows TMA cannot describe: each thread stores its own row's
-    // 64 bytes as the aligned blocks that cover them
+    // 64 bytes as the aligned blocks that cover them; the block it shares with
+    // its next chunk is carried over and stored whole with that chunk
     if (row_ok && gcol0 < p.N) {
       uint8_t* a = reinterpret_cast<uint8_t*>(e.D) + ((int64_t)grow * p.ldd + gcol0) * 2;
       const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(a) & 15u);
+      uint8_t* base = a - ph;
       uint32_t x[20];
 #pragma unroll
       for (int j = 0; j < 16; ++j) x[j] = packed[j];
 #pragma unroll
       for (int j = 16; j < 20; ++j) x[j] = 0u;
       window_shift_up(x, ph);
-      store_window(a - ph, x, (int)ph, (int)ph + 2 * min(32, p.N - gcol0));
+      const int ncols = min(32, p.N - gcol0);
+      const int hi = (int)ph + 2 * ncols;  // the chunk's bytes in the window: [ph, hi)
+      uint4 b0 = make_uint4(x[0], x[1], x[2], x[3]);
+      if (carry.on) b0 = make_uint4(b0.x | carry.v.x, b0.y | carry.v.y, b0.z | carry.v.z, b0.w | carry.v.w);
+      store_block(base, b0, carry.on ? 0 : (int)ph, hi);
+#pragma unroll
+      for (int blk = 1; blk < 4; ++blk)
+        store_block(base + 16 * blk, make_uint4(x[4 * blk], x[4 * blk + 1], x[4 * blk + 2], x[4 * blk + 3]), 0,
+                    hi - 16 * blk);
+      const uint4 b4 = make_uint4(x[16], x[17], x[18], x[19]);
+      carry.on = 0;
+      if (hi > 64) {
+        // carried only when this thread's next chunk has columns to store,
+        // so it is merged there
+        if (ncols == 32 && !last && gcol0 + 32 < p.N) {
+          carry.v = b4;
+          carry.on = 1;
+        } else {
+          store_block(base + 64, b4, 0, hi - 64);
+        }
+      }
+    } else {
+      carry.on = 0;
     }
   } else if (!p.d_trans) {
     // plain stores, coalesced through the warp's staging area (both buffers):
@@ -1176,6 +1208,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       }
       const int acc = unit & 1;  // fp16/bf16: the unit being drained below
 
+      RowCarry carry{};
 #pragma unroll 1
       for (int c = 0; c < BN / kEpiCols; ++c) {
         const int gcol0 = n0 + c * chunk;
@@ -1286,8 +1319,8 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
           if (c + 1 < BN / kEpiCols) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
         }
 
-        epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf, Tr::kEpiBufBytes, buf,
-                                       lane, ep);
+        epi_store_chunk<Tr::kOutBytes>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
+                                       Tr::kEpiBufBytes, buf, carry, c == BN / kEpiCols - 1, lane, ep);
       }
       if constexpr (!kI8) ++unit;
       if (!ok) break;
