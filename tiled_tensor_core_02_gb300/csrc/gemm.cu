@@ -339,7 +339,8 @@ template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
     case 256:
-      if constexpr (MODE != kModeI8 && MODE != kModeI8Tma) return launch_gemm<256, MODE>(prm, grid, s);
+      if constexpr (MODE != kModeI8 && MODE != kModeI8Tma && MODE != kModeI8TmemA)
+        return launch_gemm<256, MODE>(prm, grid, s);
       return cudaErrorInvalidValue;
     case 128: return launch_gemm<128, MODE>(prm, grid, s);
     case 64: return launch_gemm<64, MODE>(prm, grid, s);
@@ -356,6 +357,7 @@ cudaError_t launch(int mode, int bn, const GemmParams& prm, int grid, cudaStream
     case kModeGenBF16: return launch_mode<kModeGenBF16>(bn, prm, grid, s);
     case kModeI8: return launch_mode<kModeI8>(bn, prm, grid, s);
     case kModeI8Tma: return launch_mode<kModeI8Tma>(bn, prm, grid, s);
+    case kModeI8TmemA: return launch_mode<kModeI8TmemA>(bn, prm, grid, s);
     case kModeConvF16: return launch_mode<kModeConvF16>(bn, prm, grid, s);
     case kModeConvBF16: return launch_mode<kModeConvBF16>(bn, prm, grid, s);
     default: return cudaErrorInvalidValue;
@@ -783,7 +785,9 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
                                        tma_batch_ok(batch, sB, 1)));
   int mode;
   if (dtype == TTC_I8)
-    mode = load_tma_i8 ? kModeI8Tma : kModeI8;
+    // a K-major A is widened straight into tensor memory (less shared-memory
+    // traffic per k-block than staging its fp16 copy in shared memory)
+    mode = load_tma_i8 ? (a_mn ? kModeI8Tma : kModeI8TmemA) : kModeI8;
   else if (load_tma)
     mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
   else
@@ -802,20 +806,25 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   // rows of A worth loading per tile: all 128, or only those that exist (the
   // raw int8 staging always takes whole 128-row boxes)
-  const int a_rows = M >= kBM || mode == kModeI8Tma ? kBM : (int)round_up(M, 8);
+  const bool staged_i8 = mode == kModeI8Tma || mode == kModeI8TmemA;
+  const int a_rows = M >= kBM || staged_i8 ? kBM : (int)round_up(M, 8);
   // the kernel's index maps: tile origins, TMA boxes (128-byte swizzled slabs,
   // or the unswizzled int8 staging tiles) and the epilogue's thread maps
-  if (!tile_maps({kBM, bn, 1, a_rows, a_mn, b_mn, in_esize, mode != kModeI8Tma, 0}, prm.maps))
+  if (!tile_maps({kBM, bn, 1, a_rows, a_mn, b_mn, in_esize, !staged_i8, 0}, prm.maps))
     return TTC_ERR_UNSUPPORTED;
   // the boxes must fit the kernel's shared-memory slots (raw int8 staging: one
   // byte per element)
-  const int slot_esize = mode == kModeI8Tma ? 1 : 2;
+  const int slot_esize = staged_i8 ? 1 : 2;
   const int a_bytes = box_bytes(prm.maps.a), b_bytes = box_bytes(prm.maps.b);
   if (a_bytes == 0 || a_bytes > kBM * kBK * slot_esize || b_bytes == 0 || b_bytes > bn * kBK * slot_esize)
     return TTC_ERR_UNSUPPORTED;
-  if (K > 0 && mode == kModeI8Tma) {
+  if (K > 0 && staged_i8) {
+    // the A tile that is widened into tensor memory row by row is written with
+    // the 64-byte swizzle (64-byte rows), so the converters read it without
+    // bank conflicts
     const CUtensorMapDataType d8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-    const bool ok = encode_operand(&prm.tmA, d8, 1, A, M, K, lda, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_NONE, bdA) &&
+    const CUtensorMapSwizzle swa = mode == kModeI8TmemA ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    const bool ok = encode_operand(&prm.tmA, d8, 1, A, M, K, lda, prm.maps.a, swa, bdA) &&
                     encode_operand(&prm.tmB, d8, 1, B, N, K, ldb, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_NONE, bdB);
     if (!ok) return TTC_ERR_CUDA;
   }

@@ -60,6 +60,8 @@ enum Mode : int {
   kModeI8Tma = 5,    // TMA loads of int8 into a staging ring, converter warps widen to fp16; int32 out
   kModeConvF16 = 6,  // implicit-GEMM convolution: A gathered from the NHWC input (plain loads), fp16
   kModeConvBF16 = 7, // the same, bf16
+  kModeI8TmemA = 8,  // as kModeI8Tma for a K-major A, whose converter warps widen A straight into
+                     // tensor memory (the MMA reads A from there) and only B into shared memory
 };
 
 template <int MODE>
@@ -68,8 +70,9 @@ struct ModeTraits {
   static constexpr bool kBF16 =
       MODE == kModeTmaBF16 || MODE == kModeGenBF16 || MODE == kModeConvBF16;  // tensor-core input type
   static constexpr bool kConv = MODE == kModeConvF16 || MODE == kModeConvBF16;
-  static constexpr bool kStaged = MODE == kModeI8Tma;  // TMA int8 staging + converter warps
-  static constexpr bool kI8 = MODE == kModeI8 || MODE == kModeI8Tma;
+  static constexpr bool kStaged = MODE == kModeI8Tma || MODE == kModeI8TmemA;  // TMA int8 staging + converters
+  static constexpr bool kATmem = MODE == kModeI8TmemA;  // the MMA's A operand lives in tensor memory
+  static constexpr bool kI8 = MODE == kModeI8 || kStaged;
   // producer warps: 1 TMA thread; 4 plain-load warps; or 1 TMA warp + kConvWarps converter warps
   static constexpr int kProdWarps = kTmaLoad ? 1 : (kStaged ? 1 + kConvWarps : 4);
   static constexpr int kMmaWarp = kProdWarps;
@@ -196,7 +199,8 @@ template <int BN, int MODE>
 struct TileCfg {
   using T = ModeTraits<MODE>;
   static constexpr int kBBytes = BN * kBK * 2;
-  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kAStageBytes = T::kATmem ? 0 : kABytes;  // fp16 A in shared memory per stage
+  static constexpr int kStageBytes = kAStageBytes + kBBytes;
   static constexpr int kEpiBytes = kEpiWarps * 2 * T::kEpiBufBytes;
   static constexpr int kBarBytes = 512;
   static constexpr int kSmemLimit = 227 * 1024;  // opt-in dynamic shared memory per block
@@ -209,11 +213,18 @@ struct TileCfg {
   // int8 staging ring (staged mode): the raw int8 A and B tiles of one k-block
   static constexpr int kStage8Bytes = T::kStaged ? (kBM + BN) * kBK : 0;
   static constexpr int kStagesRaw = kStageBudget / (kStageBytes + kStage8Bytes);
-  static constexpr int kStages = kStagesRaw > 12 ? 12 : kStagesRaw;
-  static constexpr int kStages8 = T::kStaged ? kStages : 0;
+  // with A in tensor memory, a stage also takes 32 TMEM columns (64 k of fp16)
+  static constexpr int kStageCap = T::kATmem ? 4 : 12;
+  static constexpr int kStages = kStagesRaw > kStageCap ? kStageCap : kStagesRaw;
+  // int8 staging ring: as deep as the fp16 ring, or, with A in tensor memory
+  // (whose fp16 ring holds only B), as deep as the rest of shared memory
+  // allows: the raw tiles in flight are what hides the load latency
+  static constexpr int kStages8Raw = (kStageBudget - kStages * kStageBytes) / (kStage8Bytes > 0 ? kStage8Bytes : 1);
+  static constexpr int kStages8 = !T::kStaged ? 0 : !T::kATmem ? kStages : kStages8Raw > 12 ? 12 : kStages8Raw;
   // two accumulators of BN columns; int8 adds BN columns of exact int32 running
   // sums after them; allocations are powers of two of at least 32 columns
-  static constexpr int kTmemUsed = (T::kI8 ? 3 : 2) * BN;
+  static constexpr int kATmemCol0 = 3 * BN;  // kATmem: stage s of A in columns [kATmemCol0 + 32 s, + 32)
+  static constexpr int kTmemUsed = (T::kI8 ? 3 : 2) * BN + (T::kATmem ? 32 * kStages : 0);
   static constexpr int kTmemCols = kTmemUsed <= 32 ? 32 : kTmemUsed <= 64 ? 64 : kTmemUsed <= 128 ? 128
                                    : kTmemUsed <= 256 ? 256 : 512;
   static_assert(kTmemUsed <= 512, "TMEM columns");
@@ -473,6 +484,32 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
   }
 }
 
+// Widens row `r` of a raw K-major int8 tile (rows of 64 bytes, written by TMA
+// with the 64-byte swizzle: 16-byte chunk c of a row stored at chunk
+// c ^ (address bits 7-8)) into 32 words of exact fp16 pairs in k order, the
+// layout of one tensor-memory lane of an A operand.  Row r's four chunks sit
+// in different banks from those of rows r + 1 .. r + 7, so a warp reading 32
+// rows has no bank conflicts.  The tile must start on a 512-byte boundary.
+__device__ __forceinline__ void convert_i8_row_sw64(const uint8_t* s8, int r, uint32_t (&w)[32]) {
+  constexpr layout::SwizzleBytes64 swz{};
+  const __half2 bias2 = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 v = *reinterpret_cast<const uint4*>(s8 + swz((uint32_t)(r * 64 + c * 16)));
+    const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t u = ws[j] ^ 0x80808080u;
+      uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+      uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+      __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias2);
+      __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias2);
+      w[8 * c + 2 * j] = *reinterpret_cast<uint32_t*>(&l2);
+      w[8 * c + 2 * j + 1] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ epilogue helpers
 // How one 32-column chunk of fp16/bf16 C is read (the same for the whole warp).
 enum CPath : int {
@@ -592,6 +629,20 @@ __device__ __forceinline__ void c_prefetch_row(const GemmParams& p, const EpiPtr
   const uint16_t* row = static_cast<const uint16_t*>(e.C) + (int64_t)grow * p.ldc;
   const uintptr_t a0 = (reinterpret_cast<uintptr_t>(row + n0) + 15) & ~uintptr_t(15);
   const uintptr_t a1 = reinterpret_cast<uintptr_t>(row + n1) & ~uintptr_t(15);
+  if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
+}
+
+// D^T orientation: pulls the tile's C toward L2 ahead of its epilogue.  Kernel
+// row i, column j is C[j * ldc + i]: the tile's columns n0 .. n0 + ncols - 1
+// are C rows, each holding the 128 contiguous elements of rows m0 .. m0 + 127;
+// epilogue thread t takes C row n0 + t.
+__device__ __forceinline__ void c_prefetch_trans(const GemmParams& p, const EpiPtrs& e, int m0, int n0, int ncols,
+                                                 int t) {
+  if (p.beta == 0.0f || !p.d_trans || t >= ncols || n0 + t >= p.N || m0 >= p.M) return;
+  const uint16_t* row = static_cast<const uint16_t*>(e.C) + (int64_t)(n0 + t) * p.ldc;
+  const int i1 = min(m0 + kBM, p.M);
+  const uintptr_t a0 = (reinterpret_cast<uintptr_t>(row + m0) + 15) & ~uintptr_t(15);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(row + i1) & ~uintptr_t(15);
   if (a1 > a0) prefetch_l2_bulk(reinterpret_cast<const void*>(a0), (uint32_t)(a1 - a0));
 }
 
@@ -833,7 +884,7 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + S * kABytes;
+  uint8_t* sB = sA + S * Cfg::kAStageBytes;
   uint8_t* s8 = sB + S * Cfg::kBBytes;  // int8 staging ring (staged mode only)
   constexpr int S8 = Cfg::kStages8;
   uint8_t* sEpi = s8 + S8 * Cfg::kStage8Bytes;
@@ -1017,17 +1068,28 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             }
             const uint8_t* a8 = s8 + st8 * Cfg::kStage8Bytes;
             const uint8_t* b8 = a8 + kBM * kBK;
-            uint8_t* a = sA + stage * kABytes;
             uint8_t* b = sB + stage * Cfg::kBBytes;
-            if (!p.a_mn)
-              convert_i8_tile<kBM, kBK, 32 * kConvGroupWarps>(a8, a, gtid);
-            else
-              convert_i8_tile<kBK, kBM, 32 * kConvGroupWarps>(a8, a, gtid);
+            if constexpr (Tr::kATmem) {
+              // the group's four warps cover the four TMEM lane quarters: lane l
+              // of the warp in quarter q widens A row 32 q + l into that lane
+              const int qa = warp & 3;
+              uint32_t w[32];
+              convert_i8_row_sw64(a8, qa * 32 + lane, w);
+              tmem_st_32x32b_x32(tmem_base + ((uint32_t)(qa * 32) << 16) + Cfg::kATmemCol0 + stage * 32, w);
+              tmem_st_wait();
+            } else {
+              uint8_t* a = sA + stage * kABytes;
+              if (!p.a_mn)
+                convert_i8_tile<kBM, kBK, 32 * kConvGroupWarps>(a8, a, gtid);
+              else
+                convert_i8_tile<kBK, kBM, 32 * kConvGroupWarps>(a8, a, gtid);
+            }
             if (!p.b_mn)
               convert_i8_tile<BN, kBK, 32 * kConvGroupWarps>(b8, b, gtid);
             else
               convert_i8_tile<kBK, BN, 32 * kConvGroupWarps>(b8, b, gtid);
             fence_proxy_async_smem();
+            if constexpr (Tr::kATmem) tc_fence_before();  // the tensor-memory stores, before the arrive
             __syncwarp();
             if (lane == 0) {
               mbar_arrive(&full[stage]);
@@ -1119,11 +1181,19 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
               break;
             }
             tc_fence_after();
-            const uint64_t ad = a_desc0 + (uint32_t)stage * (kABytes >> 4);
             const uint64_t bd = b_desc0 + (uint32_t)stage * (Cfg::kBBytes >> 4);
-            mma_f16(d_tmem, ad, bd, idesc, kb != kb0);
+            if constexpr (Tr::kATmem) {
+              // A from tensor memory: 16 k of fp16 = 8 columns per MMA
+              const uint32_t at = tmem_base + Cfg::kATmemCol0 + (uint32_t)stage * 32;
+              mma_f16_ta(d_tmem, at, bd, idesc, kb != kb0);
 #pragma unroll
-            for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+              for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16_ta(d_tmem, at + 8 * k, bd + k * b_kstep, idesc, 1u);
+            } else {
+              const uint64_t ad = a_desc0 + (uint32_t)stage * (kABytes >> 4);
+              mma_f16(d_tmem, ad, bd, idesc, kb != kb0);
+#pragma unroll
+              for (int k = 1; k < kBK / kUmmaK; ++k) mma_f16(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+            }
             any_mma = true;
             mma_commit(&empty[stage]);
             if (++stage == S) {
@@ -1202,7 +1272,10 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
       const bool writes_out = p.ksplit == 1 || rank == 0;
       CChunk16 cc;
       if constexpr (!kI8) {
-        if (writes_out) c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
+        if (writes_out) {
+          c_prefetch_trans(p, ep, m0, n0, BN, row_in_tile);
+          c_fetch16(p, ep, c_path(p, ep, n0), grow, n0, lane, cc);
+        }
         if (!mbar_wait(&tmem_full[unit & 1], (unit >> 1) & 1, wc)) break;
         tc_fence_after();
       }
