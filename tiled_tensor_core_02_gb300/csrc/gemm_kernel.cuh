@@ -452,21 +452,42 @@ __device__ __forceinline__ void im2col_load_tile(uint8_t* sdst, const GemmParams
 // swizzle) into the fp16 128-byte-swizzled layout the tensor core reads (the
 // same placement as generic_load_tile).  Exact: with u = x + 128 (a byte),
 // the fp16 bit pattern 0x6400 | u is 1024 + u, and subtracting 1152 leaves x.
+// Raw chunks a thread widens: chunk tid + NT i of the tile, i < kIters.
 template <int ROWS, int COLS, int NT>
-__device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16, int tid) {
-  constexpr int kChunksPerRow = COLS / 16;
-  constexpr int kChunks = ROWS * kChunksPerRow;
-  constexpr int kIters = (kChunks + NT - 1) / NT;
+struct I8Tile {
+  static constexpr int kPerRow = COLS / 16;
+  static constexpr int kChunks = ROWS * kPerRow;
+  static constexpr int kIters = (kChunks + NT - 1) / NT;
+};
+
+// convert_i8_tile in two steps, so a caller can put other work between the
+// loads and the stores: the compiler may not move a shared-memory load above
+// a store to the same space, so loads interleaved with stores would each wait
+// out their own latency.
+template <int ROWS, int COLS, int NT>
+__device__ __forceinline__ void i8_tile_load(const uint8_t* s8, uint4 (&w)[I8Tile<ROWS, COLS, NT>::kIters], int tid) {
+  using T = I8Tile<ROWS, COLS, NT>;
+#pragma unroll
+  for (int i = 0; i < T::kIters; ++i) {
+    const int q = tid + NT * i;
+    if (T::kChunks % NT == 0 || q < T::kChunks)
+      w[i] = *reinterpret_cast<const uint4*>(s8 + (q / T::kPerRow) * COLS + (q % T::kPerRow) * 16);
+  }
+}
+
+template <int ROWS, int COLS, int NT>
+__device__ __forceinline__ void i8_tile_widen_store(uint8_t* s16, const uint4 (&w)[I8Tile<ROWS, COLS, NT>::kIters],
+                                                    int tid) {
+  using T = I8Tile<ROWS, COLS, NT>;
   constexpr layout::SwizzleBytes128 swz{};
   const __half2 bias2 = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
 #pragma unroll
-  for (int i = 0; i < kIters; ++i) {
+  for (int i = 0; i < T::kIters; ++i) {
     const int q = tid + NT * i;
-    if (kChunks % NT != 0 && q >= kChunks) break;
-    const int r = q / kChunksPerRow;
-    const int c = (q % kChunksPerRow) * 16;
-    const uint4 w = *reinterpret_cast<const uint4*>(s8 + r * COLS + c);
-    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    if (T::kChunks % NT != 0 && q >= T::kChunks) break;
+    const int r = q / T::kPerRow;
+    const int c = (q % T::kPerRow) * 16;
+    const uint32_t ws[4] = {w[i].x, w[i].y, w[i].z, w[i].w};
     uint32_t h[8];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -482,6 +503,13 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16,
     *reinterpret_cast<uint4*>(s16 + swz(base)) = make_uint4(h[0], h[1], h[2], h[3]);
     *reinterpret_cast<uint4*>(s16 + swz(base + 16)) = make_uint4(h[4], h[5], h[6], h[7]);
   }
+}
+
+template <int ROWS, int COLS, int NT>
+__device__ __forceinline__ void convert_i8_tile(const uint8_t* s8, uint8_t* s16, int tid) {
+  uint4 w[I8Tile<ROWS, COLS, NT>::kIters];
+  i8_tile_load<ROWS, COLS, NT>(s8, w, tid);
+  i8_tile_widen_store<ROWS, COLS, NT>(s16, w, tid);
 }
 
 // Widens row `r` of a raw K-major int8 tile (rows of 64 bytes, written by TMA
@@ -1071,11 +1099,25 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
             uint8_t* b = sB + stage * Cfg::kBBytes;
             if constexpr (Tr::kATmem) {
               // the group's four warps cover the four TMEM lane quarters: lane l
-              // of the warp in quarter q widens A row 32 q + l into that lane
+              // of the warp in quarter q widens A row 32 q + l into that lane.
+              // B's raw chunks are read first and its fp16 stores overlap the
+              // tensor-memory store of A
+              constexpr int kNT = 32 * kConvGroupWarps;
+              constexpr int kBIt = I8Tile<BN, kBK, kNT>::kIters;
+              static_assert(kBIt == I8Tile<kBK, BN, kNT>::kIters, "B chunks per thread, either majorness");
+              uint4 wb[kBIt];
+              if (!p.b_mn)
+                i8_tile_load<BN, kBK, kNT>(b8, wb, gtid);
+              else
+                i8_tile_load<kBK, BN, kNT>(b8, wb, gtid);
               const int qa = warp & 3;
               uint32_t w[32];
               convert_i8_row_sw64(a8, qa * 32 + lane, w);
               tmem_st_32x32b_x32(tmem_base + ((uint32_t)(qa * 32) << 16) + Cfg::kATmemCol0 + stage * 32, w);
+              if (!p.b_mn)
+                i8_tile_widen_store<BN, kBK, kNT>(b, wb, gtid);
+              else
+                i8_tile_widen_store<kBK, BN, kNT>(b, wb, gtid);
               tmem_st_wait();
             } else {
               uint8_t* a = sA + stage * kABytes;
@@ -1083,11 +1125,11 @@ __global__ void __launch_bounds__(ModeTraits<MODE>::kThreads, 1) gemm_kernel(con
                 convert_i8_tile<kBM, kBK, 32 * kConvGroupWarps>(a8, a, gtid);
               else
                 convert_i8_tile<kBK, kBM, 32 * kConvGroupWarps>(a8, a, gtid);
+              if (!p.b_mn)
+                convert_i8_tile<BN, kBK, 32 * kConvGroupWarps>(b8, b, gtid);
+              else
+                convert_i8_tile<kBK, BN, 32 * kConvGroupWarps>(b8, b, gtid);
             }
-            if (!p.b_mn)
-              convert_i8_tile<BN, kBK, 32 * kConvGroupWarps>(b8, b, gtid);
-            else
-              convert_i8_tile<kBK, BN, 32 * kConvGroupWarps>(b8, b, gtid);
             fence_proxy_async_smem();
             if constexpr (Tr::kATmem) tc_fence_before();  // the tensor-memory stores, before the arrive
             __syncwarp();
