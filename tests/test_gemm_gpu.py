@@ -251,6 +251,25 @@ def test_int8_small_all_layouts(la, lb):
     check_full(p, d, 1.0, 0.0)
 
 
+@pytest.mark.parametrize("tile_n", [128, 64, 32])
+@pytest.mark.parametrize("K", [32, 64, 192, 960, 1088])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_int8_k_tails(la, lb, K, tile_n):
+    """int8 K tails on every tile width: the two converter groups take
+    alternate k-blocks, so an odd count leaves one group a k-block short; K
+    below one k-block leaves most of the raw tile zero-filled.  Both majorness
+    of B (the MN-major one from 64 columns up)."""
+    if lb == "row" and tile_n < 64:
+        pytest.skip("an MN-major B needs whole 64-column slabs")
+    ttc.ttc_set_knob("tile_n", tile_n)
+    try:
+        p = synth.Problem(136, 200, K, dtype="i8", layoutA=la, layoutB=lb, seed=29, distA="int8", distB="int8")
+        d = run(p, 1.0, 0.0)
+        check_full(p, d, 1.0, 0.0)
+    finally:
+        ttc.ttc_set_knob("tile_n", 0)
+
+
 def test_int8_beta_one_adds_c():
     p = synth.Problem(130, 70, 64, dtype="i8", seed=23, distA="int8", distB="int8")
     rng = np.random.default_rng(0)
