@@ -74,7 +74,7 @@ def test_kernel_waits_before_global_access(kernel):
     assert w >= 0, f"{kernel} never waits for the previous grid"
     # global-memory helpers that must not run before the wait
     first = [body.find(tok) for tok in ("tma_load", "__ldg(", "__ldcs(", "c_fetch16(", "error_raised(",
-                                        "mbar_wait(", "mbar_wait_cluster(")]
+                                        "mbar_wait(", "mbar_wait_cluster(", "repack_load(")]
     first = [x for x in first if x >= 0]
     assert first and w < min(first), f"{kernel}: a global access precedes grid_dependency_wait()"
 

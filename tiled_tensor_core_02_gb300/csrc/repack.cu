@@ -47,38 +47,68 @@ __device__ __forceinline__ void window8_shift_down(uint32_t (&x)[8], uint32_t ph
   for (int k = 0; k < 7; ++k) x[k] = s1 ? __byte_perm(x[k], x[k + 1], 0x4321) : x[k];
 }
 
-// Each thread writes one 16-byte chunk of a destination row.  Its source
-// bytes start at any alignment: the thread loads the one or two aligned
-// 16-byte blocks that hold them (only blocks with at least one byte of the
-// row's data, so never one outside the memory pages the matrix occupies) and
-// shifts the bytes into place in registers.  Bytes past the row's end are
-// written as zero (the padding, which TMA never reads since the tensor map
-// keeps the true extent).  Launched with programmatic dependent launch: it
-// waits for the previous grid before its first global access and lets the
-// next grid (the GEMM, which waits for this one in turn) start its prologue.
-__global__ void __launch_bounds__(256) repack_rows_kernel(const __grid_constant__ RepackParams p) {
+// Destination chunk `idx` of the launch (a 16-byte piece of a destination
+// row) and its source bytes, which start at any alignment: the one or two
+// aligned 16-byte blocks that hold them (only blocks with at least one byte of
+// the row's data, so never one outside the memory pages the matrix occupies).
+struct RepackChunk {
+  uint4 b0, b1;
+  uint8_t* dst;
+  uint32_t phase;  // source address mod 16
+  int n;           // bytes of the row in this chunk (1..16)
+};
+
+__device__ __forceinline__ void repack_load(const RepackParams& p, int64_t idx, RepackChunk& c) {
+  const RepackJob& j = (p.jobs > 1 && idx >= p.job[1].first) ? p.job[1] : p.job[0];
+  // a job's chunk count is below 2^31 (checked on the host): 32-bit division
+  const uint32_t q = (uint32_t)(idx - j.first);
+  const uint32_t cpr = (uint32_t)j.chunks_per_row;
+  const uint32_t r = q / cpr;
+  const int64_t c0 = (int64_t)(q - r * cpr) * 16;
+  c.n = j.cols - c0 < 16 ? (int)(j.cols - c0) : 16;
+  const uint8_t* s = j.src + (int64_t)r * j.src_ld + c0;
+  c.phase = (uint32_t)(reinterpret_cast<uintptr_t>(s) & 15u);
+  const uint4* blk = reinterpret_cast<const uint4*>(s - c.phase);
+  c.b0 = __ldg(blk);
+  c.b1 = (int)c.phase + c.n > 16 ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
+  c.dst = j.dst + (int64_t)r * j.dst_ld + c0;
+}
+
+// Shifts the chunk's bytes into place, zeroes the bytes past the row's end
+// (the padding, which TMA never reads since the tensor map keeps the true
+// extent) and stores the 16 bytes.
+__device__ __forceinline__ void repack_store(const RepackChunk& c) {
+  uint32_t x[8] = {c.b0.x, c.b0.y, c.b0.z, c.b0.w, c.b1.x, c.b1.y, c.b1.z, c.b1.w};
+  window8_shift_down(x, c.phase);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int keep = c.n - 4 * k;  // bytes of word k inside the row
+    x[k] = keep >= 4 ? x[k] : keep <= 0 ? 0u : (x[k] & ((1u << (8 * keep)) - 1u));
+  }
+  *reinterpret_cast<uint4*>(c.dst) = make_uint4(x[0], x[1], x[2], x[3]);
+}
+
+// Each thread writes destination chunks idx, idx + stride, ..., two per
+// iteration with both chunks' loads in flight before either store.
+// Launched with programmatic dependent launch: it waits for the previous grid
+// before its first global access and lets the next grid (the GEMM, which
+// waits for this one in turn) start its prologue.
+__global__ void __launch_bounds__(256, 8) repack_rows_kernel(const __grid_constant__ RepackParams p) {
   grid_dependency_wait();
   grid_dependents_launch();
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < p.total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
-    const RepackJob& j = (p.jobs > 1 && idx >= p.job[1].first) ? p.job[1] : p.job[0];
-    const int64_t q = idx - j.first;
-    const int64_t r = q / j.chunks_per_row;
-    const int64_t c0 = (q - r * j.chunks_per_row) * 16;
-    const int64_t n = j.cols - c0 < 16 ? j.cols - c0 : 16;  // bytes of the row in this chunk
-    const uint8_t* s = j.src + r * j.src_ld + c0;
-    const uint32_t ph = (uint32_t)(reinterpret_cast<uintptr_t>(s) & 15u);
-    const uint4* blk = reinterpret_cast<const uint4*>(s - ph);
-    const uint4 b0 = __ldg(blk);
-    const uint4 b1 = (int64_t)ph + n > 16 ? __ldg(blk + 1) : make_uint4(0u, 0u, 0u, 0u);
-    uint32_t x[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    window8_shift_down(x, ph);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t keep = n - 4 * k;  // bytes of word k inside the row
-      x[k] = keep >= 4 ? x[k] : keep <= 0 ? 0u : (x[k] & ((1u << (8 * keep)) - 1u));
-    }
-    *reinterpret_cast<uint4*>(j.dst + r * j.dst_ld + c0) = make_uint4(x[0], x[1], x[2], x[3]);
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; idx + stride < p.total; idx += 2 * stride) {
+    RepackChunk c0, c1;
+    repack_load(p, idx, c0);
+    repack_load(p, idx + stride, c1);
+    repack_store(c0);
+    repack_store(c1);
+  }
+  if (idx < p.total) {
+    RepackChunk c0;
+    repack_load(p, idx, c0);
+    repack_store(c0);
   }
 }
 
@@ -98,6 +128,7 @@ cudaError_t launch_repack2(const RepackSpec* specs, int count, int sm_count, cud
     j.dst_ld = sp.dst_ld * sp.elem_bytes;
     if (j.dst_ld % 16 || reinterpret_cast<uintptr_t>(j.dst) % 16 || j.dst_ld < j.cols) return cudaErrorInvalidValue;
     j.chunks_per_row = (j.cols + 15) / 16;
+    if (j.rows * j.chunks_per_row >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
     j.first = total;
     total += j.rows * j.chunks_per_row;
   }
