@@ -206,7 +206,14 @@ size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
  * it behaves as with ttc_gemm_workspace_size bytes.  The result is the same
  * either way.  fp16/bf16 outputs need no copy: the GEMM writes rows at any
  * 2-byte boundary itself.  0 for invalid or empty arguments and for
- * matrix-vector problems (which use no workspace).  Pure host computation.
+ * matrix-vector problems (which use no workspace).
+ * int8 problems of at least 64 tiles of 256 x 256 (TTC_KNOB_I8_WIDE) whose
+ * operands TMA can read as int8 and whose D it can write as int32 instead
+ * get fp16 copies of A and B (2 bytes per element, rows padded to 16
+ * elements): given that much, ttc_gemm_ws widens the operands into them and
+ * runs the product on the CTA-pair kernel, exactly as before (int8 values
+ * and products are exact in fp16 and fp32, and the kernel adds 1024-deep
+ * partial sums as int32).  Pure host computation.
  */
 size_t ttc_gemm_workspace_size_staged(int64_t M, int64_t N, int64_t K,
                                       const void* A, int64_t lda, ttc_layout layoutA,
@@ -312,6 +319,11 @@ const char* ttc_status_string(ttc_status status);
  *     start its prologue (barrier set-up, tensor-memory allocation) while the
  *     previous kernel on the stream finishes, and touches global memory only
  *     once that kernel has completed; 1 launches them in plain stream order.
+ *   TTC_KNOB_I8_WIDE: 0 (default) lets ttc_gemm_ws run int8 problems of at
+ *     least 64 tiles of 256 x 256 on the CTA-pair kernel when its workspace
+ *     holds fp16 copies of A and B (ttc_gemm_workspace_size_staged); 1 does
+ *     so from one tile up; 2 never (the single-CTA int8 kernels, which widen
+ *     the operands in shared memory, take every int8 problem).
  * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
  */
 typedef enum {
@@ -328,7 +340,8 @@ typedef enum {
   TTC_KNOB_GEMV = 10,
   TTC_KNOB_CONV_HALO = 11,
   TTC_KNOB_PAIR_TAIL = 12,
-  TTC_KNOB_PDL = 13
+  TTC_KNOB_PDL = 13,
+  TTC_KNOB_I8_WIDE = 14
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -142,6 +142,34 @@ def test_staged_workspace_size_query(lib):
     assert staged(64, 64, 64, P, 64, 9, P, 64, C, P, 64, BF16) == 0
 
 
+def test_int8_pair_path_workspace_size(lib):
+    """int8 problems of at least 64 tiles of 256 x 256 whose operands TMA can
+    read and whose int32 D it can write ask for fp16 copies of A and B (rows
+    padded to 16 elements, each copy rounded to 256 bytes); smaller ones, and
+    any with the knob at 2, need only what the single-CTA path needs."""
+    r256 = lambda b: (b + 255) // 256 * 256
+    staged = ttc.ttc_gemm_workspace_size_staged
+    # 8192^3, A row-major, B column-major: two 8192 x 8192 fp16 copies
+    assert staged(8192, 8192, 8192, P, 8192, R, P, 8192, C, P, 8192, I8) == 2 * 8192 * 8192 * 2
+    # K = 1000 pads each row to 1008 elements; B row-major: K rows of N
+    assert staged(2048, 3000, 1000, P, 1008, R, P, 3008, R, P, 3000, I8) == \
+        r256(2048 * 1008 * 2) + r256(1000 * 3008 * 2)
+    # 36 tiles: below the threshold, and the pitch-only query never changes
+    assert staged(1536, 1536, 4096, P, 4096, R, P, 4096, C, P, 1536, I8) == 0
+    assert ttc.ttc_gemm_workspace_size(8192, 8192, 8192, P, 8192, R, P, 8192, C, I8) == 0
+    # an int32 D that TMA cannot write keeps the single-CTA path (and its aligned
+    # copy of D, whose pitch is N rounded to 16 bytes)
+    assert staged(8192, 8192, 8192, P, 8192, R, P, 8192, C, P, 8194, I8) == r256(8192 * 8192 * 4)
+    try:
+        assert ttc.ttc_set_knob("i8_wide", 1) == 0
+        assert staged(1536, 1536, 4096, P, 4096, R, P, 4096, C, P, 1536, I8) == 2 * r256(1536 * 4096 * 2)
+        assert ttc.ttc_set_knob("i8_wide", 2) == 0
+        assert staged(8192, 8192, 8192, P, 8192, R, P, 8192, C, P, 8192, I8) == 0
+        assert ttc.ttc_set_knob("i8_wide", 3) == 1
+    finally:
+        ttc.ttc_set_knob("i8_wide", 0)
+
+
 def test_static_scratch_rejects_oversized_problems(lib):
     # 4099 x 8192 bf16 with an odd pitch needs ~64 MiB of repacked A: beyond the
     # fixed 16 MiB, refused before any device work

@@ -270,6 +270,66 @@ def test_int8_k_tails(la, lb, K, tile_n):
         ttc.ttc_set_knob("tile_n", 0)
 
 
+def _run_i8_wide(p, beta=0.0, force=True):
+    """Runs p through ttc_gemm_ws with the workspace for fp16 copies of the
+    operands; returns the output and the number of kernels launched."""
+    ttc.ttc_set_knob("i8_wide", 1 if force else 0)
+    try:
+        n0 = ttc.ttc_launch_count()
+        d = run(p, 1.0, beta, workspace=-2)
+        return d, ttc.ttc_launch_count() - n0
+    finally:
+        ttc.ttc_set_knob("i8_wide", 0)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 64), (300, 520, 1000), (520, 600, 2112), (257, 300, 1088)])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_int8_pair_path_exact(la, lb, M, N, K):
+    """int8 on the CTA-pair kernel (fp16 copies of the operands, 1024-deep
+    partial sums added as int32): bit-exact, with ragged tiles, K tails of an
+    odd number of k-blocks, and more than one partial per tile.  Two launches:
+    the widening copy and the pair kernel."""
+    p = synth.Problem(M, N, K, dtype="i8", layoutA=la, layoutB=lb, seed=33, distA="int8", distB="int8")
+    d, launches = _run_i8_wide(p)
+    assert launches == 2
+    check_full(p, d, 1.0, 0.0)
+
+
+def test_int8_pair_path_adds_c_and_stays_exact():
+    """beta = 1 adds an int32 C; -128 * -128 over K = 8192 reaches K * 2^14 =
+    2^27, eight 1024-deep partials of 2^24 each."""
+    M, N, K = 256, 512, 8192
+    p = synth.Problem.from_logical(np.full((M, K), -128, np.int8), np.full((K, N), -128, np.int8), dtype="i8")
+    d, launches = _run_i8_wide(p)
+    assert launches == 2 and np.all(d == K * 16384)
+    q = synth.Problem(300, 600, 1500, dtype="i8", seed=34, distA="int8", distB="int8")
+    rng = np.random.default_rng(1)
+    c = rng.integers(-2**20, 2**20, size=(q.M, q.N)).astype(np.int32)
+    q.C_log = c
+    q.C, q.ldc = synth.to_layout(c, "row")
+    d, launches = _run_i8_wide(q, beta=1.0)
+    assert launches == 2
+    check_full(q, d, 1.0, 1.0)
+
+
+def test_int8_pair_path_half_tile_tail():
+    """81 pair tiles on the resident pairs: the last partial wave runs as half
+    tiles (N = 128 units); the planner takes the pair path by itself."""
+    p = synth.Problem(2304, 2304, 192, dtype="i8", layoutA="row", layoutB="col", seed=35, distA="int8",
+                      distB="int8")
+    d, launches = _run_i8_wide(p, force=False)
+    assert launches == 2
+    check_full(p, d, 1.0, 0.0)
+
+
+def test_int8_8192_pair_path_sampled_and_freivalds():
+    p, a, b, act = synth.make(synth.WORKLOADS["i8_8192"])
+    d, launches = _run_i8_wide(p, force=False)
+    assert launches == 2
+    check_sampled(p, d, a, b, act, seed=5)
+    freivalds(p, d, a, b, seed=5)
+
+
 def test_int8_beta_one_adds_c():
     p = synth.Problem(130, 70, 64, dtype="i8", seed=23, distA="int8", distB="int8")
     rng = np.random.default_rng(0)

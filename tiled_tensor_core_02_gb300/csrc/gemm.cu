@@ -44,6 +44,7 @@ std::atomic<int> g_conv_halo{0};
 std::atomic<int> g_pair_tail{0};
 std::atomic<int> g_gemv_off{0};
 std::atomic<int> g_pdl_off{0};
+std::atomic<int> g_i8_wide{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -53,6 +54,7 @@ struct DeviceInfo {
   int sm_count = 0;
   int pair_clusters[2][4] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};  // resident CTA pairs [bf16][width 256/224/192/128]
   int halo_clusters[2][2] = {{-1, -1}, {-1, -1}};          // halo convolution pairs [bf16][width 256/128]
+  int pair_clusters_i8 = -1;                                // resident CTA pairs of the int8 pair kernel
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -335,6 +337,118 @@ int plan_pair_units(GemmParams& prm, int pbn, int clusters) {
   return split_last_wave(prm.num_tiles, clusters, pbn == 256, prm.tail_from, prm.num_units);
 }
 
+// int8 on the CTA-pair kernel: ttc_gemm_ws widens A and B into fp16 copies in
+// the workspace (in their own layouts, rows padded to 16 elements) and runs
+// the pair kernel's int8 variant on them.  Taken for problems of at least
+// kI8WideMinTiles 256 x 256 tiles whose operand rows TMA could read as int8
+// and whose int32 D TMA can write; the widening reads each operand once and
+// writes twice its bytes.  Measured against the single-CTA int8 kernels
+// (graph replay): 8192^3 679 vs 1318 us, 4096^3 110 vs 179 us, 2048 x 3000 x
+// 1024 (96 tiles) 22.6 vs 24.3 us, but 1536 x 1536 x 4096 (36 tiles) 31.3 vs
+// 29.6 us.
+constexpr int64_t kI8WideMinTiles = 64;
+struct I8Wide {
+  bool on = false;
+  int64_t a_rows = 0, a_cols = 0, a_ld = 0, b_rows = 0, b_cols = 0, b_ld = 0;
+  size_t a_off = 0, b_off = 0, bytes = 0;
+};
+
+I8Wide plan_i8_wide(int64_t M, int64_t N, int64_t K, const void* A, int64_t lda, ttc_layout layoutA, const void* B,
+                    int64_t ldb, ttc_layout layoutB, const void* D, int64_t ldd) {
+  I8Wide w;
+  const int mode = g_i8_wide.load();
+  if (mode == 2 || K <= 0 || M < kPairBM || N < 256) return w;
+  if (mode == 0 && ((M + kPairBM - 1) / kPairBM) * ((N + 255) / 256) < kI8WideMinTiles) return w;
+  if (!tma_ok(A, lda, 1) || !tma_ok(B, ldb, 1) || !tma_ok(D, ldd, 4)) return w;
+  w.a_rows = layoutA == TTC_ROW_MAJOR ? M : K;
+  w.a_cols = layoutA == TTC_ROW_MAJOR ? K : M;
+  w.b_rows = layoutB == TTC_ROW_MAJOR ? K : N;
+  w.b_cols = layoutB == TTC_ROW_MAJOR ? N : K;
+  w.a_ld = round_up(w.a_cols, 16);
+  w.b_ld = round_up(w.b_cols, 16);
+  w.a_off = 0;
+  w.b_off = (size_t)round_up(w.a_rows * w.a_ld * 2, 256);
+  w.bytes = w.b_off + (size_t)round_up(w.b_rows * w.b_ld * 2, 256);
+  w.on = true;
+  return w;
+}
+
+ttc_status gemm_i8_wide(DeviceInfo* dev, const I8Wide& w, int64_t M, int64_t N, int64_t K, const void* A,
+                        int64_t lda, ttc_layout layoutA, const void* B, int64_t ldb, ttc_layout layoutB,
+                        const void* C, int64_t ldc, void* D, int64_t ldd, float beta, void* workspace,
+                        void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const bool a_mn = layoutA == TTC_COL_MAJOR;
+  const bool b_mn = layoutB == TTC_ROW_MAJOR;
+  if (dev->pair_clusters_i8 < 0) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (dev->pair_clusters_i8 < 0) dev->pair_clusters_i8 = pair_max_clusters_i8();
+  }
+  const int clusters = dev->pair_clusters_i8;
+  if (clusters <= 0) return TTC_ERR_CUDA;
+  GemmParams prm;
+  std::memset(&prm, 0, sizeof prm);
+  // the maps of the fp16 pair path: 128 A rows and 128 B columns per CTA and
+  // k-block, 64-column B boxes for the half units of a last wave
+  if (!tile_maps({kPairBM, 256, 2, kBM, a_mn, b_mn, 2, 1, 128}, prm.maps)) return TTC_ERR_UNSUPPORTED;
+  if (box_bytes(prm.maps.a, 2) != kABytes || box_bytes(prm.maps.b, 2) != 128 * kBK * 2 ||
+      box_bytes(prm.maps.b_half, 2) != 64 * kBK * 2)
+    return TTC_ERR_UNSUPPORTED;
+  const void* A16 = ws + w.a_off;
+  const void* B16 = ws + w.b_off;
+  const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  if (!encode_operand(&prm.tmA, f16, 2, A16, M, K, w.a_ld, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_operand(&prm.tmB, f16, 2, B16, N, K, w.b_ld, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+    return TTC_ERR_CUDA;
+  prm.A = A16;
+  prm.B = B16;
+  prm.lda = w.a_ld;
+  prm.ldb = w.b_ld;
+  prm.M = (int)M;
+  prm.N = (int)N;
+  prm.K = (int)K;
+  prm.num_m_blocks = (int)((M + kPairBM - 1) / kPairBM);
+  prm.num_n_blocks = (int)((N + 255) / 256);
+  prm.num_k_blocks = (int)((K + kBK - 1) / kBK);
+  prm.tiles_per_batch = prm.num_m_blocks * prm.num_n_blocks;
+  prm.num_tiles = prm.tiles_per_batch;
+  prm.batch = 1;
+  const int gm = g_group_m.load() > 0 ? g_group_m.load() : 8;
+  prm.group_m = prm.num_m_blocks < gm ? prm.num_m_blocks : gm;
+  prm.ksplit = 1;
+  prm.kb_split = prm.num_k_blocks;
+  prm.a_mn = a_mn;
+  prm.b_mn = b_mn;
+  prm.alpha = 1.0f;
+  prm.beta = beta;
+  prm.C = beta != 0.0f ? C : nullptr;
+  prm.ldc = ldc;
+  prm.D = D;
+  prm.ldd = ldd;
+  prm.d_tma = 1;
+  prm.err = dev->err;
+  prm.timeout_ns = (uint64_t)g_timeout_ns.load();
+  prm.inject_stall = g_inject_stall.load();
+  const int nclus = plan_pair_units(prm, 256, clusters);
+  if (!b_mn && prm.tail_from < prm.num_units) {
+    // half units stage only their 64 columns of B per CTA
+    if (!encode_operand(&prm.tmBh, f16, 2, B16, N, K, w.b_ld, prm.maps.b_half, CU_TENSOR_MAP_SWIZZLE_128B))
+      return TTC_ERR_CUDA;
+    prm.b_half_map = 1;
+  }
+  prm.a_stream = prm.num_n_blocks == 1;
+  prm.b_stream = prm.num_m_blocks == 1;
+  const WidenSpec specs[2] = {{A, lda, w.a_rows, w.a_cols, ws + w.a_off, w.a_ld},
+                              {B, ldb, w.b_rows, w.b_cols, ws + w.b_off, w.b_ld}};
+  if (launch_widen_i8(specs, 2, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  if (launch_pair_i8(prm, nclus, s) != cudaSuccess) return TTC_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return TTC_OK;
+}
+
 template <int MODE>
 cudaError_t launch_mode(int bn, const GemmParams& prm, int grid, cudaStream_t s) {
   switch (bn) {
@@ -519,6 +633,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_gemv_off.store((int)value);
       return TTC_OK;
+    case TTC_KNOB_I8_WIDE:
+      if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
+      g_i8_wide.store((int)value);
+      return TTC_OK;
     case TTC_KNOB_PAIR_TAIL:
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_pair_tail.store((int)value);
@@ -646,6 +764,15 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     if (launch_gemv_rows(gp, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
     g_launches.fetch_add(1);
     return TTC_OK;
+  }
+
+  // ------------------------------------------------------------ int8 on the CTA-pair kernel (workspace)
+  if (dtype == TTC_I8 && batch == 1 && workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 256 == 0 &&
+      !g_force_generic_load.load() && !g_force_generic_store.load()) {
+    const I8Wide w = plan_i8_wide(M, N, K, A, lda, layoutA, B, ldb, layoutB, D, ldd);
+    if (w.on && w.bytes <= workspace_bytes)
+      return gemm_i8_wide(dev, w, M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, beta, workspace,
+                          stream);
   }
 
   // ------------------------------------------------------------ workspace: repack what TMA cannot read
@@ -1218,6 +1345,11 @@ size_t ttc_gemm_workspace_size_staged(int64_t M, int64_t N, int64_t K, const voi
   ttc_layout la = layoutA, lb = layoutB;
   canonicalise(M, N, K, la, lda_c, lb, ldb_c);
   if (takes_gemv(M, N, K, la, lb, dtype, 1)) return 0;
+  if (dtype == TTC_I8) {
+    // int8 problems the CTA-pair kernel takes: fp16 copies of A and B
+    const I8Wide w = plan_i8_wide(M, N, K, A, lda_c, la, B, ldb_c, lb, D, ldd);
+    if (w.on) return w.bytes;
+  }
   const size_t ab = ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype);
   return ab + plan_dstage(M, N, D, ldd, dtype == TTC_I8 ? 4 : 2, ab).bytes;
 }

@@ -31,6 +31,14 @@
 // a last partial wave, half tiles of N = BN / 2 columns.  A half unit issues
 // MMAs with N = BN / 2, and each CTA uses the first BN / 4 columns of its
 // usual B box, which it loads starting at its own columns.
+//
+// int8 (kI8): the operands are fp16 copies of int8 matrices (every int8 value
+// is exact in fp16, every product exact in fp32).  The issuer starts a fresh
+// accumulator every kI8ChunkKBlocks k-blocks (1024 of K), so each partial sum
+// is an integer below 2^24 in magnitude and exact in fp32; the epilogue warps
+// add the partials as int32 into running sums held in their registers (a
+// thread's row, its half of the tile's columns) and store the int32 tile once
+// per unit, after the last partial.
 #pragma once
 #include "gemm_kernel.cuh"
 
@@ -45,7 +53,7 @@ constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // warp 0 producer, warp 
 // (128 of K, 8 MMAs per barrier round trip): measured on GB300, one full/empty
 // round trip per 4 MMAs holds the pair to ~85 ns per N = 256 MMA, one per 8
 // MMAs to the tensor pipe's own ~67 ns, with as few as 2 stages.
-template <int BN>
+template <int BN, bool kI8 = false>
 struct PairCfg {
   static constexpr int kBHalf = BN / 2;
   static constexpr int kKPS = 2;                        // k-blocks per stage
@@ -53,8 +61,12 @@ struct PairCfg {
   static constexpr int kBHalfBytes = kBHalf * kBK * 2;  // one k-block of B columns: 16 / 14 / 12 / 8 KiB
   static constexpr int kKBlockBytes = kAHalfBytes + kBHalfBytes;
   static constexpr int kStageBytes = kKPS * kKBlockBytes;
-  static constexpr int kEpiBufBytes = 32 * kEpiCols * 2;
-  static constexpr int kEpiBytes = kPairEpiWarps * 2 * kEpiBufBytes;
+  static constexpr int kOutBytes = kI8 ? 4 : 2;
+  static constexpr int kEpiBufBytes = 32 * kEpiCols * kOutBytes;
+  // staging buffers per epilogue warp: two, or one for int8, whose warps
+  // store their chunks once per tile
+  static constexpr int kEpiBufs = kI8 ? 1 : 2;
+  static constexpr int kEpiBytes = kPairEpiWarps * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesRaw = (kSmemLimit - 1024 - kBarBytes - kEpiBytes) / kStageBytes;
@@ -62,6 +74,7 @@ struct PairCfg {
   static constexpr int kTmemCols = 2 * BN > 256 ? 512 : 256;  // two accumulators, a power of two
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
   static_assert(BN == 256 || BN == 224 || BN == 192 || BN == 128, "pair tile width");
+  static_assert(!kI8 || BN == 256, "int8: 256-wide tiles (a warp's running sums cover at most 4 chunks)");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
@@ -76,10 +89,11 @@ __device__ __forceinline__ void tma_load_boxes_pair(uint8_t* dst, const CUtensor
   if (bm.boxes > 1) tma_load_3d_pair(dst + bm.smem_step, m, x + bm.box_step, y, z, bar_leader, pol);
 }
 
-template <int BN, bool kBF16>
+template <int BN, bool kBF16, bool kI8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
-  using PairCfg = ttc::PairCfg<BN>;
+  static_assert(!(kI8 && kBF16), "int8 runs on fp16 copies");
+  using PairCfg = ttc::PairCfg<BN, kI8>;
   constexpr int kPairBN = BN;
   constexpr int S = PairCfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -238,47 +252,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sA), p.a_mn ? 8192u : 16u, 1024);
       const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sB), p.b_mn ? 8192u : 16u, 1024);
       const uint64_t a_kstep = p.a_mn ? 2048u >> 4 : 32u >> 4, b_kstep = p.b_mn ? 2048u >> 4 : 32u >> 4;
-      for (int u = pair; ok && u < p.num_units; u += num_pairs, ++it) {
+      // k-blocks per accumulator: a unit's all, or for int8 1024-deep chunks
+      // (a multiple of KPS, so the stages of a unit never straddle two)
+      const int nkbt = p.num_k_blocks;
+      const int chunk_kb = kI8 ? kI8ChunkKBlocks : (nkbt > 0 ? nkbt : 1);
+      const int chunks_per_unit = nkbt > 0 ? (nkbt + chunk_kb - 1) / chunk_kb : 1;
+      static_assert(!kI8 || kI8ChunkKBlocks % KPS == 0, "accumulator chunks hold whole stages");
+      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
         const uint32_t idesc = u >= p.tail_from ? idesc_half : idesc_full;
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * kPairBN;
-        for (int kb0 = 0; kb0 < p.num_k_blocks; kb0 += KPS) {
-          const int nkb = min(KPS, p.num_k_blocks - kb0);
-          if (!mbar_wait(&full[stage], phase, wc)) {
+        for (int kc = 0; ok && kc < chunks_per_unit; ++kc, ++it) {
+          const int acc = it & 1;
+          const uint32_t acc_phase = (it >> 1) & 1;
+          if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1u, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t d_tmem = tmem_base + acc * kPairBN;
+          const int kbeg = kc * chunk_kb, kend = min(nkbt, kbeg + chunk_kb);
+          for (int kb0 = kbeg; kb0 < kend; kb0 += KPS) {
+            const int nkb = min(KPS, kend - kb0);
+            if (!mbar_wait(&full[stage], phase, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
 #pragma unroll
-          for (int j = 0; j < KPS; ++j) {
-            if (j < nkb) {
-              const uint64_t ad = a_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kAHalfBytes >> 4);
-              const uint64_t bd = b_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kBHalfBytes >> 4);
-              mma_f16_pair(d_tmem, ad, bd, idesc, (kb0 | j) != 0);
+            for (int j = 0; j < KPS; ++j) {
+              if (j < nkb) {
+                const uint64_t ad = a_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kAHalfBytes >> 4);
+                const uint64_t bd = b_desc0 + (uint32_t)(stage * KPS + j) * (PairCfg::kBHalfBytes >> 4);
+                mma_f16_pair(d_tmem, ad, bd, idesc, ((kb0 - kbeg) | j) != 0);
 #pragma unroll
-              for (int k = 1; k < kBK / kUmmaK; ++k)
-                mma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+                for (int k = 1; k < kBK / kUmmaK; ++k)
+                  mma_f16_pair(d_tmem, ad + k * a_kstep, bd + k * b_kstep, idesc, 1u);
+              }
+            }
+            any_mma = true;
+            mma_commit_pair(&empty[stage], 0x3);
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
             }
           }
-          any_mma = true;
-          mma_commit_pair(&empty[stage], 0x3);
-          if (++stage == S) {
-            stage = 0;
-            phase ^= 1u;
+          if (!ok) break;
+          if (kend <= kbeg) {
+            mbar_arrive(&tmem_full[acc]);
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[acc]), 1));
+          } else {
+            mma_commit_pair(&tmem_full[acc], 0x3);
           }
-        }
-        if (!ok) break;
-        if (p.num_k_blocks == 0) {
-          mbar_arrive(&tmem_full[acc]);
-          mbar_arrive_cluster(mapa_shared(smem_u32(&tmem_full[acc]), 1));
-        } else {
-          mma_commit_pair(&tmem_full[acc], 0x3);
         }
       }
       if (any_mma) {
@@ -292,7 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const int ew = warp - 2;
     const int q = warp & 3;
     const int part = ew >> 2;  // which half of a tile's columns this warp drains
-    uint8_t* stage_buf = sEpi + ew * 2 * PairCfg::kEpiBufBytes;
+    uint8_t* stage_buf = sEpi + ew * PairCfg::kEpiBufs * PairCfg::kEpiBufBytes;
     int buf = 0;
     int it = 0;
     const bool has_k = p.num_k_blocks > 0;
@@ -313,56 +336,147 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
       c_prefetch_row(p, epi_ptrs(p, pbz, 2), pmb * p.maps.tile_m + (int)rank * p.maps.cta_m + row_in_tile,
                      pnb * p.maps.tile_n + pn_off, phalf ? p.maps.half_n : p.maps.tile_n);
     };
-    if (part == 0) prefetch_c(pair);
-    for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
-      int t, n_off;
-      bool half;
-      pair_unit(p, u, p.maps.half_n, t, n_off, half);
-      const int chunks = (half ? kPairBN / 2 : kPairBN) / kEpiCols;
-      const int acc = it & 1;
-      int bz, mb, nb;
-      tile_coords(t, p, bz, mb, nb);
-      const int m0 = mb * p.maps.tile_m + (int)rank * p.maps.cta_m;
-      const int n0 = nb * p.maps.tile_n + n_off;
-      const int grow = m0 + row_in_tile;
-      const bool row_ok = grow < p.M;
-      const EpiPtrs ep = epi_ptrs(p, bz, 2);
-      if (part == 0) prefetch_c(u + num_pairs);
-      const int c_lo = part == 0 ? 0 : (chunks + 1) / 2;
-      const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
-      // the first chunk's C is fetched before waiting for the accumulator
-      CChunk16 cc;
-      c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * chunk), grow, n0 + c_lo * chunk, lane, cc);
-      if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
-      tc_fence_after();
-      if (c_lo == c_hi) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
-      }
-      RowCarry carry{};
-#pragma unroll 1
-      for (int c = c_lo; c < c_hi; ++c) {
-        const int gcol0 = n0 + c * chunk;
-        uint32_t r[32];
-        if (has_k) {
-          tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * chunk, r);
-          tmem_ld_wait();
-        } else {
+    if constexpr (kI8) {
+      // int8: running int32 sums of this thread's row over its part's (at most
+      // four) 32-column chunks, one accumulator chunk (1024 of K) at a time
+      const int nkbt = p.num_k_blocks;
+      const int chunks_per_unit = nkbt > 0 ? (nkbt + kI8ChunkKBlocks - 1) / kI8ChunkKBlocks : 1;
+      bool ok = true;
+      for (int u = pair; ok && u < p.num_units; u += num_pairs) {
+        int t, n_off;
+        bool half;
+        pair_unit(p, u, p.maps.half_n, t, n_off, half);
+        const int chunks = (half ? kPairBN / 2 : kPairBN) / kEpiCols;
+        int bz, mb, nb;
+        tile_coords(t, p, bz, mb, nb);
+        const int m0 = mb * p.maps.tile_m + (int)rank * p.maps.cta_m;
+        const int n0 = nb * p.maps.tile_n + n_off;
+        const int grow = m0 + row_in_tile;
+        const bool row_ok = grow < p.M;
+        const EpiPtrs ep = epi_ptrs(p, bz, 4);
+        const int c_lo = part == 0 ? 0 : (chunks + 1) / 2;
+        const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
+        int32_t sums[4][32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) r[j] = 0u;
-        }
-        if (c == c_hi - 1) {
+        for (int cc = 0; cc < 4; ++cc)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sums[cc][j] = 0;
+        for (int kc = 0; kc < chunks_per_unit; ++kc, ++it) {
+          const int acc = it & 1;
+          if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (has_k) {
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+              if (c_lo + cc < c_hi) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + (c_lo + cc) * chunk, r);
+                tmem_ld_wait();
+                // an integer below 2^24 in magnitude: exact in fp32 and in the conversion
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sums[cc][j] += __float2int_rn(__uint_as_float(r[j]));
+              }
+            }
+          }
           // this warp's accumulator columns are read: tell the even CTA's issuer
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
         }
-        uint32_t packed[16];
-        epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
-        if (c + 1 < c_hi) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
-        epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
-                           PairCfg::kEpiBufBytes, buf, carry, c == c_hi - 1, lane, ep);
+        if (!ok) break;
+        RowCarry carry{};
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int c = c_lo + cc;
+          if (c < c_hi) {
+            const int gcol0 = n0 + c * chunk;
+            uint32_t packed[32];
+            if (p.beta != 0.0f && row_ok) {
+              // D = sums + C (beta == 1, checked on the host)
+              const int32_t* crow = reinterpret_cast<const int32_t*>(ep.C) + (int64_t)grow * p.ldc + gcol0;
+              const bool vec = ((p.ldc & 3) == 0) && ((reinterpret_cast<uintptr_t>(ep.C) & 15) == 0) &&
+                               (gcol0 + 32 <= p.N);
+              if (vec) {
+#pragma unroll
+                for (int u4 = 0; u4 < 8; ++u4) {
+                  const int4 w = __ldg(reinterpret_cast<const int4*>(crow) + u4);
+                  packed[4 * u4] = (uint32_t)(sums[cc][4 * u4] + w.x);
+                  packed[4 * u4 + 1] = (uint32_t)(sums[cc][4 * u4 + 1] + w.y);
+                  packed[4 * u4 + 2] = (uint32_t)(sums[cc][4 * u4 + 2] + w.z);
+                  packed[4 * u4 + 3] = (uint32_t)(sums[cc][4 * u4 + 3] + w.w);
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                  packed[j] = (uint32_t)(sums[cc][j] + (gcol0 + j < p.N ? __ldg(crow + j) : 0));
+              }
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) packed[j] = (uint32_t)sums[cc][j];
+            }
+            // one staging buffer per warp: the previous chunk's store must have read it
+            if (lane == 0) bulk_wait_read<0>();
+            __syncwarp();
+            epi_store_chunk<4>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf, 0, buf,
+                               carry, c == c_hi - 1, lane, ep);
+          }
+        }
+      }
+    } else {
+      if (part == 0) prefetch_c(pair);
+      for (int u = pair; u < p.num_units; u += num_pairs, ++it) {
+        int t, n_off;
+        bool half;
+        pair_unit(p, u, p.maps.half_n, t, n_off, half);
+        const int chunks = (half ? kPairBN / 2 : kPairBN) / kEpiCols;
+        const int acc = it & 1;
+        int bz, mb, nb;
+        tile_coords(t, p, bz, mb, nb);
+        const int m0 = mb * p.maps.tile_m + (int)rank * p.maps.cta_m;
+        const int n0 = nb * p.maps.tile_n + n_off;
+        const int grow = m0 + row_in_tile;
+        const bool row_ok = grow < p.M;
+        const EpiPtrs ep = epi_ptrs(p, bz, 2);
+        if (part == 0) prefetch_c(u + num_pairs);
+        const int c_lo = part == 0 ? 0 : (chunks + 1) / 2;
+        const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
+        // the first chunk's C is fetched before waiting for the accumulator
+        CChunk16 cc;
+        c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * chunk), grow, n0 + c_lo * chunk, lane, cc);
+        if (!mbar_wait(&tmem_full[acc], (it >> 1) & 1, wc)) break;
+        tc_fence_after();
+        if (c_lo == c_hi) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+        }
+        RowCarry carry{};
+  #pragma unroll 1
+        for (int c = c_lo; c < c_hi; ++c) {
+          const int gcol0 = n0 + c * chunk;
+          uint32_t r[32];
+          if (has_k) {
+            tmem_ld_32x32b_x32(tmem_base + lane_base + acc * kPairBN + c * chunk, r);
+            tmem_ld_wait();
+          } else {
+  #pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = 0u;
+          }
+          if (c == c_hi - 1) {
+            // this warp's accumulator columns are read: tell the even CTA's issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&tmem_empty[acc]), 0));
+          }
+          uint32_t packed[16];
+          epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
+          if (c + 1 < c_hi) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
+          epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
+                             PairCfg::kEpiBufBytes, buf, carry, c == c_hi - 1, lane, ep);
+        }
       }
     }
     if (p.d_tma && lane == 0) bulk_wait_all();

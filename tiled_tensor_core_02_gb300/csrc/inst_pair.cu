@@ -8,7 +8,7 @@
 namespace ttc {
 
 namespace {
-template <int BN, bool kBF16>
+template <int BN, bool kBF16, bool kI8 = false>
 cudaError_t set_smem_attr() {
   static std::atomic<bool> done[64];
   int dev = 0;
@@ -16,37 +16,37 @@ cudaError_t set_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev].load()) {
-    e = cudaFuncSetAttribute(gemm_pair_kernel<BN, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg<BN>::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<BN, kBF16, kI8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg<BN, kI8>::kSmemBytes);
     if (e != cudaSuccess) return e;
     done[dev].store(true);
   }
   return cudaSuccess;
 }
 
-template <int BN, bool kBF16>
+template <int BN, bool kBF16, bool kI8 = false>
 int max_clusters() {
-  if (set_smem_attr<BN, kBF16>() != cudaSuccess) return 0;
+  if (set_smem_attr<BN, kBF16, kI8>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<BN>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<BN, kI8>::kSmemBytes;
   int n = 0;
-  return cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, kBF16>, &cfg) == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, kBF16, kI8>, &cfg) == cudaSuccess ? n : 0;
 }
 
-template <int BN, bool kBF16>
+template <int BN, bool kBF16, bool kI8 = false>
 cudaError_t launch(const GemmParams& p, int clusters, cudaStream_t stream) {
-  const cudaError_t e = set_smem_attr<BN, kBF16>();
+  const cudaError_t e = set_smem_attr<BN, kBF16, kI8>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);  // clusters of 2 from the kernel's __cluster_dims__
   cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<BN>::kSmemBytes;
+  cfg.dynamicSmemBytes = PairCfg<BN, kI8>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   add_pdl_attribute(cfg, attr);
-  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, kBF16>, p);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, kBF16, kI8>, p);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -61,6 +61,13 @@ int pair_max_clusters(bool bf16, int bn) {
     case 128: return bf16 ? max_clusters<128, true>() : max_clusters<128, false>();
   }
   return 0;
+}
+
+// The int8 variant (fp16 copies of int8 operands, exact int32 sums): 256-wide tiles.
+int pair_max_clusters_i8() { return max_clusters<256, false, true>(); }
+
+cudaError_t launch_pair_i8(const GemmParams& p, int clusters, cudaStream_t stream) {
+  return launch<256, false, true>(p, clusters, stream);
 }
 
 cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream) {

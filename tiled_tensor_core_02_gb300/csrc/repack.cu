@@ -153,6 +153,127 @@ cudaError_t launch_repack(const void* src, int64_t src_ld, int64_t rows, int64_t
   return launch_repack2(&sp, 1, sm_count, stream);
 }
 
+// ---------------------------------------------------------------- int8 -> fp16 widening
+// For the CTA-pair int8 path: fp16 copies of the int8 operands, in their own
+// layouts, rows padded to whole 16-element chunks.  A chunk is 16 int8 values
+// read as one 16-byte vector (its row starts 16-byte aligned, so the vector
+// lies inside the row's memory pages) and written as two; values past the
+// row's end are written as zero.  Exact: with u = x + 128 (one byte), the fp16
+// bit pattern 0x6400 | u is 1024 + u, and subtracting 1152 leaves x.
+struct WidenJob {
+  const uint8_t* src;
+  int64_t src_ld;  // bytes
+  int64_t rows, cols;
+  uint16_t* dst;
+  int64_t dst_ld;  // elements
+  int64_t chunks_per_row;
+  int64_t first;
+};
+
+struct WidenParams {
+  WidenJob job[2];
+  int jobs;
+  int64_t total;
+};
+
+struct WidenChunk {
+  uint4 v;
+  uint16_t* dst;
+  int n;  // values of the row in this chunk (1..16)
+};
+
+__device__ __forceinline__ void widen_load(const WidenParams& p, int64_t idx, WidenChunk& c) {
+  const WidenJob& j = (p.jobs > 1 && idx >= p.job[1].first) ? p.job[1] : p.job[0];
+  const uint32_t q = (uint32_t)(idx - j.first);
+  const uint32_t cpr = (uint32_t)j.chunks_per_row;
+  const uint32_t r = q / cpr;
+  const int64_t c0 = (int64_t)(q - r * cpr) * 16;
+  c.n = j.cols - c0 < 16 ? (int)(j.cols - c0) : 16;
+  c.v = __ldg(reinterpret_cast<const uint4*>(j.src + (int64_t)r * j.src_ld + c0));
+  c.dst = j.dst + (int64_t)r * j.dst_ld + c0;
+}
+
+__device__ __forceinline__ void widen_store(const WidenChunk& c) {
+  const __half2 bias2 = __halves2half2(__ushort_as_half(0x6480u), __ushort_as_half(0x6480u));  // 1152
+  const uint32_t ws[4] = {c.v.x, c.v.y, c.v.z, c.v.w};
+  uint32_t h[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t u = ws[k] ^ 0x80808080u;
+    uint32_t lo = __byte_perm(u, 0x64646464u, 0x4140);
+    uint32_t hi = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 l2 = __hsub2(*reinterpret_cast<__half2*>(&lo), bias2);
+    const __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&hi), bias2);
+    h[2 * k] = *reinterpret_cast<const uint32_t*>(&l2);
+    h[2 * k + 1] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int keep = c.n - 2 * k;  // values of word k inside the row
+    h[k] = keep >= 2 ? h[k] : keep == 1 ? (h[k] & 0xFFFFu) : 0u;
+  }
+  uint4* d = reinterpret_cast<uint4*>(c.dst);
+  d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+  d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// Two chunks per thread per iteration, both loads in flight before either
+// store; programmatic dependent launch as repack_rows_kernel.
+__global__ void __launch_bounds__(256, 8) widen_i8_kernel(const __grid_constant__ WidenParams p) {
+  grid_dependency_wait();
+  grid_dependents_launch();
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (; idx + stride < p.total; idx += 2 * stride) {
+    WidenChunk c0, c1;
+    widen_load(p, idx, c0);
+    widen_load(p, idx + stride, c1);
+    widen_store(c0);
+    widen_store(c1);
+  }
+  if (idx < p.total) {
+    WidenChunk c0;
+    widen_load(p, idx, c0);
+    widen_store(c0);
+  }
+}
+
+cudaError_t launch_widen_i8(const WidenSpec* specs, int count, int sm_count, cudaStream_t stream) {
+  if (count < 1 || count > 2) return cudaErrorInvalidValue;
+  WidenParams p{};
+  p.jobs = count;
+  int64_t total = 0;
+  for (int i = 0; i < count; ++i) {
+    const WidenSpec& sp = specs[i];
+    WidenJob& j = p.job[i];
+    j.src = static_cast<const uint8_t*>(sp.src);
+    j.src_ld = sp.src_ld;
+    j.rows = sp.rows;
+    j.cols = sp.cols;
+    j.dst = static_cast<uint16_t*>(sp.dst);
+    j.dst_ld = sp.dst_ld;
+    j.chunks_per_row = (j.cols + 15) / 16;
+    if (reinterpret_cast<uintptr_t>(j.src) % 16 || j.src_ld % 16 || reinterpret_cast<uintptr_t>(j.dst) % 16 ||
+        j.dst_ld % 16 || j.dst_ld < j.chunks_per_row * 16 || j.rows * j.chunks_per_row >= (int64_t(1) << 31))
+      return cudaErrorInvalidValue;
+    j.first = total;
+    total += j.rows * j.chunks_per_row;
+  }
+  p.total = total;
+  if (total == 0) return cudaSuccess;
+  int64_t blocks = (total + 255) / 256;
+  const int64_t cap = (int64_t)sm_count * 8;
+  if (blocks > cap) blocks = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, widen_i8_kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // The reverse copy: rows of an aligned, padded-pitch matrix back to a
 // destination whose rows are only element-aligned.  Element per thread, so
 // each load and store instruction covers 32 consecutive elements of one row;
