@@ -186,10 +186,11 @@ ttc_status ttc_gemm_ws(int64_t M, int64_t N, int64_t K,
 
 /*
  * Workspace bytes ttc_gemm_ws uses for these operands: 0 when TMA can read
- * both, for matrix-vector problems (one output row with B column-major, or one
- * output column with A row-major: their kernel reads the operands with plain
- * loads and needs no workspace), and for invalid or empty arguments.  Pure
- * host computation.
+ * both, for matrix-vector problems (one output row or column, fp16/bf16, with
+ * the matrix operand's reduction or its outputs contiguous, the latter from
+ * 1024 outputs or for K up to 8192: their kernels read the operands with
+ * plain loads and need no workspace), and for invalid or empty arguments.
+ * Pure host computation.
  */
 size_t ttc_gemm_workspace_size(int64_t M, int64_t N, int64_t K,
                                const void* A, int64_t lda, ttc_layout layoutA,
@@ -299,11 +300,12 @@ const char* ttc_status_string(ttc_status status);
  *     tile rows per column of tiles (0: 16 for single CTAs, 8 for pairs).
  *   TTC_KNOB_PAIR_TILE_N: 0 lets the planner choose the CTA-pair tile width;
  *     256, 224, 192 or 128 forces it (224 and 192 only with a column-major B).
- *   TTC_KNOB_GEMV: 0 (default) runs matrix-vector problems whose reduction
- *     is contiguous (M == 1 with a column-major B, or N == 1 with a
- *     row-major A; fp16/bf16, K > 0, not batched) on the CUDA-core
- *     matrix-vector kernel; 1 sends them to the tensor-core kernels like any
- *     other shape.
+ *   TTC_KNOB_GEMV: 0 (default) runs matrix-vector problems (fp16/bf16,
+ *     K > 0, not batched) on the CUDA-core matrix-vector kernels: M == 1 with
+ *     a column-major B or N == 1 with a row-major A (the reduction
+ *     contiguous), and M == 1 with a row-major B or N == 1 with a
+ *     column-major A (the outputs contiguous; from 1024 outputs, or K up to
+ *     8192); 1 sends them to the tensor-core kernels like any other shape.
  *   TTC_KNOB_PAIR_TAIL: 0 (default) lets the CTA-pair kernels run a last,
  *     partial wave of tiles (or a problem of at most half a wave) as half
  *     tiles on twice as many pairs; 1 keeps whole tiles.

@@ -186,8 +186,12 @@ def test_matrix_vector_problems_need_no_scratch(lib):
     assert ttc.ttc_gemm_workspace_size(1, 4096, 4097, P, 4097, R, P, 4097, C, BF16) == 0
     assert ttc.ttc_gemm_workspace_size(1, 4096, 4097, P, 1, C, P, 4097, C, BF16) == 0  # 1 x K, lda free
     assert ttc.ttc_gemm_workspace_size(4096, 1, 4097, P, 4097, R, P, 4097, C, BF16) == 0
-    # the same shape with B row-major goes to the tensor-core kernel: repacked
-    assert ttc.ttc_gemm_workspace_size(1, 4095, 4097, P, 4097, R, P, 4095, R, BF16) > 16 << 20
+    # the same with B row-major (the outputs contiguous in B): the other
+    # matrix-vector kernel, no scratch either
+    assert ttc.ttc_gemm_workspace_size(1, 4095, 4097, P, 4097, R, P, 4095, R, BF16) == 0
+    assert ttc.ttc_gemm_workspace_size(4095, 1, 4097, P, 4095, C, P, 4097, C, BF16) == 0
+    # two output rows are a GEMM for the tensor-core kernels: repacked
+    assert ttc.ttc_gemm_workspace_size(2, 4095, 4097, P, 4097, R, P, 4095, R, BF16) > 16 << 20
     st = ttc.ttc_gemm_static_scratch(1, 4096, 4097, P, 4097, R, P, 4097, C, None, 4096, P * 2, 4096, 1.0, 0.0,
                                      None, 0, BF16, None)
     assert st != 5  # not refused (without a GPU the call then stops at the CUDA device query)

@@ -25,8 +25,8 @@ def check(p, d, alpha, beta, act="none"):
     assert ok, f"worst error ratio {worst:.3f} at {divmod(w, p.N)}"
 
 
-SHAPES = [(1, 4096, 4096), (1, 300, 1000), (1, 7, 5), (1, 64, 4099), (1, 1, 777),
-          (4096, 1, 4096), (1000, 1, 300), (5, 1, 7), (4099, 1, 64)]
+SHAPES = [(1, 4096, 4096), (1, 300, 1000), (1, 7, 5), (1, 64, 4099), (1, 1, 777), (1, 5000, 20000),
+          (4096, 1, 4096), (1000, 1, 300), (5, 1, 7), (4099, 1, 64), (5000, 1, 20000)]
 
 
 @pytest.mark.parametrize("gemv_off", [0, 1])
@@ -60,8 +60,11 @@ def test_matrix_vector_odd_pitches(la, lb):
         check(p, run(p, 1.0, 1.0, ldd=N + 3), 1.0, 1.0)
 
 
-def test_matrix_vector_is_one_launch():
-    p = synth.Problem(1, 4096, 4096, dtype="bf16", seed=2)
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+def test_matrix_vector_is_one_launch(la, lb):
+    """Either matrix-vector kernel (the reduction or the outputs contiguous in
+    B) is one launch, with no workspace."""
+    p = synth.Problem(1, 4096, 4096, dtype="bf16", layoutA=la, layoutB=lb, seed=2)
     n0 = ttc.ttc_launch_count()
     run(p, 1.0, 0.0)
     assert ttc.ttc_launch_count() == n0 + 1

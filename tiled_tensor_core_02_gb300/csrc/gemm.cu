@@ -505,14 +505,26 @@ void canonicalise(int64_t M, int64_t N, int64_t K, ttc_layout& layoutA, int64_t&
   }
 }
 
-// Problems the matrix-vector kernel takes (after canonicalise): one output row
-// (M == 1) or column (N == 1) whose reduction runs along the matrix operand's
-// contiguous dimension.  They read their operands with plain loads and use no
-// workspace.
+// Problems the matrix-vector kernels take (after canonicalise): one output row
+// (M == 1) or column (N == 1).  The reduction runs along the matrix operand's
+// contiguous dimension (gemv_rows_kernel), or the outputs do (gemv_cols_kernel;
+// taken when its K slices can fill the SMs, at least 1024 outputs, or K is at
+// most 8192).  They read their operands with plain loads and use no workspace.
+enum GemvKind { kGemvNone = 0, kGemvRows = 1, kGemvCols = 2 };
+GemvKind gemv_kind(int64_t M, int64_t N, int64_t K, ttc_layout layoutA, ttc_layout layoutB, ttc_dtype dtype,
+                   int64_t batch) {
+  if (K <= 0 || dtype == TTC_I8 || batch != 1 || g_gemv_off.load()) return kGemvNone;
+  if ((M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR)) return kGemvRows;
+  const int64_t outputs = M == 1 ? N : M;
+  if (((M == 1 && layoutB == TTC_ROW_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_COL_MAJOR)) &&
+      (outputs >= 1024 || K <= 8192))
+    return kGemvCols;
+  return kGemvNone;
+}
+
 bool takes_gemv(int64_t M, int64_t N, int64_t K, ttc_layout layoutA, ttc_layout layoutB, ttc_dtype dtype,
                 int64_t batch) {
-  const bool rows = (M == 1 && layoutB == TTC_COL_MAJOR) || (N == 1 && M > 1 && layoutA == TTC_ROW_MAJOR);
-  return rows && K > 0 && dtype != TTC_I8 && batch == 1 && !g_gemv_off.load();
+  return gemv_kind(M, N, K, layoutA, layoutB, dtype, batch) != kGemvNone;
 }
 
 // Which operands ttc_gemm_ws copies into its workspace (those TMA cannot
@@ -727,11 +739,13 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   // One output row (M == 1) or column (N == 1) whose reduction runs along the
   // matrix operand's contiguous dimension streams that operand with two FLOPs
   // per element: CUDA-core kernel, one warp per output, no tiles.
-  if (takes_gemv(M, N, K, layoutA, layoutB, dtype, batch)) {
+  const GemvKind gk = gemv_kind(M, N, K, layoutA, layoutB, dtype, batch);
+  if (gk != kGemvNone) {
     GemvParams gp;
     std::memset(&gp, 0, sizeof gp);
     if (M == 1) {
-      // D[0, n] = sum_k A[0, k] B[k, n]; column n of B is K-contiguous
+      // D[0, n] = sum_k A[0, k] B[k, n]: column n of B is K-contiguous (rows
+      // kernel), or row k of B is N-contiguous (cols kernel); same pointer and pitch
       gp.x = static_cast<const uint16_t*>(A);
       gp.incx = layoutA == TTC_ROW_MAJOR ? 1 : lda;
       gp.mat = static_cast<const uint16_t*>(B);
@@ -741,7 +755,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       gp.incc = 1;
       gp.incb = 1;
     } else {
-      // D[m, 0] = sum_k A[m, k] B[k, 0]; row m of A is K-contiguous
+      // D[m, 0] = sum_k A[m, k] B[k, 0]: row m of A is K-contiguous (rows
+      // kernel), or column k of A is M-contiguous (cols kernel)
       gp.x = static_cast<const uint16_t*>(B);
       gp.incx = layoutB == TTC_COL_MAJOR ? 1 : ldb;
       gp.mat = static_cast<const uint16_t*>(A);
@@ -759,9 +774,15 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     gp.beta = beta;
     gp.act = (int)act;
     gp.bf16 = dtype == TTC_BF16;
-    gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0 && gp.incx == 1 &&
-             reinterpret_cast<uintptr_t>(gp.x) % 16 == 0;
-    if (launch_gemv_rows(gp, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (gk == kGemvRows) {
+      gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0 && gp.incx == 1 &&
+               reinterpret_cast<uintptr_t>(gp.x) % 16 == 0;
+      if (launch_gemv_rows(gp, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+    } else {
+      gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0;
+      if (launch_gemv_cols(gp, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+    }
     g_launches.fetch_add(1);
     return TTC_OK;
   }

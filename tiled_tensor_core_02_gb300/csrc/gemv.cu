@@ -4,12 +4,12 @@
 // CUDA cores in fp32 do the arithmetic and the work is to keep HBM busy:
 // no tiles, no TMEM, no cluster set-up on the common path.
 //
-// The kernel covers the case where the reduction runs along the matrix's
-// contiguous dimension: one warp per output, each lane eight 16-byte vectors
-// of the row and of x in flight, a shuffle reduction, the epilogue on lane 0.
-// (With the outputs contiguous instead, a CTA-per-output-block kernel with a
-// cluster reduction over K slices measured slower than the tensor-core
-// kernels at 1 x 4096 x 4096, so that case stays on them.)
+// gemv_rows_kernel covers the case where the reduction runs along the
+// matrix's contiguous dimension: one warp per output, each lane eight 16-byte
+// vectors of the row and of x in flight, a shuffle reduction, the epilogue on
+// lane 0.  gemv_cols_kernel covers the other one, where the outputs are
+// contiguous in the matrix: a CTA per block of outputs and slice of K, the
+// slices of one block in a cluster, added through distributed shared memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -23,7 +23,7 @@ namespace ttc {
 
 namespace {
 constexpr int kThreads = 256;
-constexpr int kRowsUnroll = 8;  // vectors in flight per lane
+constexpr int kRowsUnroll = 16;  // vectors in flight per lane
 
 template <bool BF16>
 __device__ __forceinline__ void epilogue_store(const GemvParams& p, int i, float acc) {
@@ -92,7 +92,126 @@ __global__ void __launch_bounds__(kThreads) gemv_rows_kernel(const GemvParams p)
   }
 }
 
+// ---------------------------------------------------------------- outputs contiguous
+// Line k of the matrix (k < K) holds the terms of consecutive outputs:
+// y[i] = sum_k mat[k * ldm + i] x[k * incx].  A CTA takes kColsBlock outputs
+// and one K slice; each half-warp reads 256 contiguous bytes of a line (8
+// outputs per lane, one 16-byte vector), the CTA's 16 half-warps take lines
+// 16 apart with kColsUnroll lines in flight each.  The half-warps' partial
+// sums meet in shared memory; the cluster's CTAs (gridDim.y, the K slices of
+// one output block) then hand theirs to the first CTA through distributed
+// shared memory, which adds them in slice order and applies the epilogue.
+constexpr int kColsBlock = 128;
+constexpr int kColsUnroll = 16;
+
+template <bool BF16>
+__device__ __forceinline__ void fma8(uint4 w, float xv, float (&acc)[8]) {
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    acc[2 * j] = fmaf(half_bits_to_float<BF16>((uint16_t)(ws[j] & 0xFFFFu)), xv, acc[2 * j]);
+    acc[2 * j + 1] = fmaf(half_bits_to_float<BF16>((uint16_t)(ws[j] >> 16)), xv, acc[2 * j + 1]);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kThreads) gemv_cols_kernel(const GemvParams p) {
+  __shared__ float part[kThreads / 16][kColsBlock];
+  __shared__ float tot[kColsBlock];
+  const int tid = threadIdx.x;
+  const int hw = tid >> 4;  // half-warp
+  const int i0 = blockIdx.x * kColsBlock + (tid & 15) * 8;
+  const int slices = gridDim.y;
+  const int per = ((p.K + slices - 1) / slices + 15) / 16 * 16;
+  const int k_lo = blockIdx.y * per;
+  const int k_hi = min(p.K, k_lo + per);
+  // whole 16-byte vectors: an aligned line pitch and all 8 outputs inside
+  const bool vec = p.vec && i0 + 8 <= p.rows;
+  grid_dependency_wait();  // every load and store after the previous grid on the stream
+  grid_dependents_launch();
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (vec) {
+    // every line's 16 bytes and its x issued before the first use
+    const uint16_t* base = p.mat + i0;
+    for (int k = k_lo + hw; k < k_hi; k += 16 * kColsUnroll) {
+      uint4 w[kColsUnroll];
+      float xv[kColsUnroll];
+#pragma unroll
+      for (int u = 0; u < kColsUnroll; ++u) {
+        const int kk = k + 16 * u;
+        const bool in = kk < k_hi;
+        w[u] = in ? __ldcs(reinterpret_cast<const uint4*>(base + (int64_t)kk * p.ldm)) : make_uint4(0u, 0u, 0u, 0u);
+        xv[u] = in ? half_bits_to_float<BF16>(p.x[(int64_t)kk * p.incx]) : 0.0f;
+      }
+#pragma unroll
+      for (int u = 0; u < kColsUnroll; ++u) fma8<BF16>(w[u], xv[u], acc);
+    }
+  } else if (i0 < p.rows) {
+    for (int k = k_lo + hw; k < k_hi; k += 16) {
+      const uint16_t* line = p.mat + (int64_t)k * p.ldm + i0;
+      const float xv = half_bits_to_float<BF16>(p.x[(int64_t)k * p.incx]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (i0 + j < p.rows) acc[j] = fmaf(half_bits_to_float<BF16>(line[j]), xv, acc[j]);
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) part[hw][(tid & 15) * 8 + j] = acc[j];
+  __syncthreads();
+  if (tid < kColsBlock) {
+    float s = 0.0f;
+#pragma unroll
+    for (int h = 0; h < kThreads / 16; ++h) s += part[h][tid];
+    tot[tid] = s;
+  }
+  if (slices == 1) {
+    const int i = blockIdx.x * kColsBlock + tid;
+    if (tid < kColsBlock && i < p.rows) epilogue_store<BF16>(p, i, tot[tid]);
+    return;
+  }
+  cluster_sync();  // every slice's sums written (release / acquire across the cluster)
+  if (blockIdx.y == 0 && tid < kColsBlock) {
+    float s = 0.0f;
+    for (int r = 0; r < slices; ++r) {
+      const uint32_t a = mapa_shared(smem_u32(&tot[tid]), (uint32_t)r);
+      float v;
+      asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+      s += v;
+    }
+    const int i = blockIdx.x * kColsBlock + tid;
+    if (i < p.rows) epilogue_store<BF16>(p, i, s);
+  }
+  cluster_sync();  // no CTA leaves while the first one may still read its sums
+}
+
 }  // namespace
+
+cudaError_t launch_gemv_cols(const GemvParams& p, int sm_count, cudaStream_t stream) {
+  const int blocks = (p.rows + kColsBlock - 1) / kColsBlock;
+  // K slices per output block (a cluster): up to 8, while the CTAs fit about
+  // two per SM and each slice keeps at least 128 lines
+  int slices = 1;
+  while (slices < 8 && (int64_t)blocks * slices * 2 <= 2 * (int64_t)sm_count && p.K / (slices * 2) >= 128) slices *= 2;
+  if (blocks <= 0) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, (unsigned)slices, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  if (slices > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = (unsigned)slices;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  add_pdl_attribute(cfg, attr);
+  const cudaError_t le = p.bf16 ? cudaLaunchKernelEx(&cfg, gemv_cols_kernel<true>, p)
+                                : cudaLaunchKernelEx(&cfg, gemv_cols_kernel<false>, p);
+  if (le != cudaSuccess) return le;
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gemv_rows(const GemvParams& p, int sm_count, cudaStream_t stream) {
   const int warps = kThreads / 32;

@@ -28,4 +28,11 @@ struct GemvParams {
 
 cudaError_t launch_gemv_rows(const GemvParams& p, int sm_count, cudaStream_t stream);
 
+// The same sums with the outputs contiguous in the matrix: line k (k < K) at
+// mat + k * ldm holds the terms of outputs 0 .. rows - 1,
+//   y[i] = act(alpha * sum_k mat[k * ldm + i] x[k * incx] + beta * c[i * incc] + bias[i * incb]).
+// vec: 16-byte vector loads of the lines are aligned (mat 16-byte aligned,
+// ldm a multiple of 8).
+cudaError_t launch_gemv_cols(const GemvParams& p, int sm_count, cudaStream_t stream);
+
 }  // namespace ttc
