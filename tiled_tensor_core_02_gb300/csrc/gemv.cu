@@ -5,7 +5,7 @@
 // no tiles, no TMEM, no cluster set-up on the common path.
 //
 // gemv_rows_kernel covers the case where the reduction runs along the
-// matrix's contiguous dimension: one warp per output, each lane eight 16-byte
+// matrix's contiguous dimension: one warp per output, each lane sixteen 16-byte
 // vectors of the row and of x in flight, a shuffle reduction, the epilogue on
 // lane 0.  gemv_cols_kernel covers the other one, where the outputs are
 // contiguous in the matrix: a CTA per block of outputs and slice of K, the
