@@ -207,6 +207,38 @@ def test_stalled_pipeline_times_out_and_context_survives(pair):
         ttc.ttc_set_knob("pair", 0)
 
 
+def test_int8_pair_path_stall_times_out_and_context_survives():
+    """The same on the int8 CTA-pair path (widening copy, then the pair kernel
+    with 1024-deep partials): its issuer stalls, every wait gives up within
+    the budget, and the next call on the path is exact."""
+    p = synth.Problem(256, 512, 2048, dtype="i8", seed=36, distA="int8", distB="int8")
+    ttc.ttc_set_knob("i8_wide", 1)
+    ttc.ttc_set_knob("timeout_ns", 200_000_000)
+    ttc.ttc_set_knob("inject_stall", 1)
+    try:
+        A, B = to_dev(p.A), to_dev(p.B)
+        D = torch.zeros(p.M * p.N, dtype=torch.int32, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        need = ttc.ttc_gemm_workspace_size_staged(p.M, p.N, p.K, A.data_ptr(), p.lda, 0, B.data_ptr(), p.ldb, 1,
+                                                  D.data_ptr(), p.N, ttc.DTYPE["i8"])
+        assert need > 0
+        ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+        n0 = ttc.ttc_launch_count()
+        st = ttc.ttc_gemm_ws(p.M, p.N, p.K, A.data_ptr(), p.lda, 0, B.data_ptr(), p.ldb, 1, None, p.N,
+                             D.data_ptr(), p.N, 1.0, 0.0, None, 0, ttc.DTYPE["i8"], ws.data_ptr(), need, s)
+        assert st == 0 and ttc.ttc_launch_count() - n0 == 2
+        assert ttc.ttc_get_device_error(s) == 4
+    finally:
+        ttc.ttc_set_knob("inject_stall", 0)
+        ttc.ttc_set_knob("timeout_ns", 0)
+    try:
+        assert ttc.ttc_get_device_error(None) == 0
+        d = run(p, 1.0, 0.0, workspace=-2)
+        check_full(p, d, 1.0, 0.0)
+    finally:
+        ttc.ttc_set_knob("i8_wide", 0)
+
+
 # ------------------------------------------------------------------ operands TMA cannot describe
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
