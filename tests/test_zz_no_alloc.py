@@ -99,3 +99,24 @@ def test_static_scratch_matches_workspace_entry_twice():
         ok, worst, _ = oracle.check_float(oracle.decode(d_static.ravel(), p.dtype), r.ravel(), sabs.ravel(),
                                           p.dtype)
         assert ok, worst
+
+
+def test_static_scratch_runs_int8_on_the_pair_path():
+    """An int8 problem of 64 pair tiles whose fp16 operand copies (8 MiB) fit
+    the static array: the call widens them there and runs the CTA-pair kernel
+    (two launches), exact against the oracle."""
+    p = synth.Problem(2048, 2048, 1024, dtype="i8", layoutA="row", layoutB="col", seed=44, distA="int8",
+                      distB="int8")
+    A, B = to_dev(p.A), to_dev(p.B)
+    D = torch.full((p.M * p.N,), -1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    before = ttc.ttc_launch_count()
+    st = ttc.ttc_gemm_static_scratch(p.M, p.N, p.K, A.data_ptr(), p.lda, LAY[p.layoutA], B.data_ptr(), p.ldb,
+                                     LAY[p.layoutB], None, p.N, D.data_ptr(), p.N, 1.0, 0.0, None, 0,
+                                     ttc.DTYPE["i8"], s)
+    assert st == 0, ttc.STATUS.get(st, st)
+    assert ttc.ttc_get_device_error(s) == 0
+    assert ttc.ttc_launch_count() - before == 2
+    r, _ = oracle.gemm_full(p, alpha=1.0, beta=0.0)
+    assert np.array_equal(D.cpu().numpy().reshape(p.M, p.N).astype(np.int64), r.astype(np.int64))
