@@ -326,6 +326,10 @@ const char* ttc_status_string(ttc_status status);
  *     holds fp16 copies of A and B (ttc_gemm_workspace_size_staged); 1 does
  *     so from one tile up; 2 never (the single-CTA int8 kernels, which widen
  *     the operands in shared memory, take every int8 problem).
+ *   TTC_KNOB_PAIR_EPI_WARPS: 0 (default) lets the CTA-pair kernel drain
+ *     256-wide tiles whose output rows TMA cannot store with twelve
+ *     epilogue warps (three per TMEM lane quarter) and all others with
+ *     eight; 8 keeps eight everywhere; 12 is the default's choice.
  * Returns TTC_ERR_INVALID_ARG for an unknown knob or value.
  */
 typedef enum {
@@ -343,7 +347,8 @@ typedef enum {
   TTC_KNOB_CONV_HALO = 11,
   TTC_KNOB_PAIR_TAIL = 12,
   TTC_KNOB_PDL = 13,
-  TTC_KNOB_I8_WIDE = 14
+  TTC_KNOB_I8_WIDE = 14,
+  TTC_KNOB_PAIR_EPI_WARPS = 15
 } ttc_knob;
 
 ttc_status ttc_set_knob(ttc_knob knob, int64_t value);

@@ -24,7 +24,7 @@ def _built():
     _build.build()
     ttc.load()
     for k in ("inject_stall", "force_generic_load", "force_generic_store", "tile_n", "pair", "swap_ab",
-              "split_k", "pair_tile_n", "pair_tail", "conv_halo"):
+              "split_k", "pair_tile_n", "pair_tail", "conv_halo", "pair_epi_warps"):
         ttc.ttc_set_knob(k, 0)
     yield
 
@@ -561,20 +561,26 @@ def test_workspace_staged_d_in_place_and_padding(beta):
     assert np.array_equal(rows[:, p.N:], p.C.reshape(-1)[: p.M * 305].reshape(p.M, 305)[:, p.N:])
 
 
-@pytest.mark.parametrize("pair,N", [(1, 300), (2, 77), (1, 320), (2, 96)])
+@pytest.mark.parametrize("pair,N,ew", [(1, 300, 12), (1, 300, 8), (2, 77, 0), (1, 320, 12), (1, 320, 8), (2, 96, 0),
+                                       (1, 600, 12), (1, 600, 0)])
 @pytest.mark.parametrize("c_off,d_off", [(1, 3), (2, 5), (3, 7), (4, 6), (7, 1), (0, 2)])
-def test_unaligned_c_and_d_rows(pair, N, c_off, d_off):
+def test_unaligned_c_and_d_rows(pair, N, ew, c_off, d_off):
     """C and D rows at every 2-byte phase of a 16-byte block (odd pitches and
     element offsets of the base pointers): the epilogue moves each row segment
     as the aligned 16-byte blocks that cover it, and the block two chunks of a
     row share is stored once with the second.  N = 300 and 77 end inside a
     32-column chunk; N = 320 and 96 end at a chunk boundary inside a tile, so
     the tile's last chunks hold no columns.  Nothing outside D's M x N
-    elements is written."""
+    elements is written.  On the CTA-pair kernel, 256-wide tiles of such
+    outputs take twelve epilogue warps (ew = 12, the planner's choice; a
+    third of a tile's chunks each, one or two of a half tile's), eight when
+    forced (ew = 8); ew = 0 leaves the tile width to the planner too."""
     M, K = 300, 128
     ldc, ldd = N + 3, N + 5
     p = synth.Problem(M, N, K, dtype="bf16", seed=50 + c_off, distC="uniform", dist_bias="normal:0.5", ldc=ldc)
     ttc.ttc_set_knob("pair", pair)
+    ttc.ttc_set_knob("pair_epi_warps", ew)
+    ttc.ttc_set_knob("pair_tile_n", 256 if ew else 0)
     try:
         cbig = np.concatenate([np.zeros(c_off, np.uint16), p.C, np.zeros(8, np.uint16)])
         C_dev = to_dev(cbig)[c_off:]
@@ -587,6 +593,8 @@ def test_unaligned_c_and_d_rows(pair, N, c_off, d_off):
         assert np.all(rows[:, N:] == 0xFFFF)
     finally:
         ttc.ttc_set_knob("pair", 0)
+        ttc.ttc_set_knob("pair_epi_warps", 0)
+        ttc.ttc_set_knob("pair_tile_n", 0)
 
 
 def test_workspace_too_small_falls_back():

@@ -29,7 +29,7 @@ STATUS = {0: "TTC_OK", 1: "TTC_ERR_INVALID_ARG", 2: "TTC_ERR_UNSUPPORTED", 3: "T
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024
 KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_generic_store": 3,
         "tile_n": 4, "pair": 5, "swap_ab": 6, "split_k": 7, "pair_tile_n": 8,
-        "group_m": 9, "gemv": 10, "conv_halo": 11, "pair_tail": 12, "pdl": 13, "i8_wide": 14}
+        "group_m": 9, "gemv": 10, "conv_halo": 11, "pair_tail": 12, "pdl": 13, "i8_wide": 14, "pair_epi_warps": 15}
 
 # Every symbol the C header declares (checked by the test suite).
 EXPORTS = ("ttc_gemm", "ttc_gemm_strided_batched", "ttc_gemm_ws", "ttc_gemm_workspace_size",

@@ -45,6 +45,7 @@ std::atomic<int> g_pair_tail{0};
 std::atomic<int> g_gemv_off{0};
 std::atomic<int> g_pdl_off{0};
 std::atomic<int> g_i8_wide{0};
+std::atomic<int> g_pair_epi_warps{0};
 std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
@@ -55,6 +56,7 @@ struct DeviceInfo {
   int pair_clusters[2][4] = {{-1, -1, -1, -1}, {-1, -1, -1, -1}};  // resident CTA pairs [bf16][width 256/224/192/128]
   int halo_clusters[2][2] = {{-1, -1}, {-1, -1}};          // halo convolution pairs [bf16][width 256/128]
   int pair_clusters_i8 = -1;                                // resident CTA pairs of the int8 pair kernel
+  int pair_clusters_ew12[2] = {-1, -1};                     // ... of the twelve-epilogue-warp variant [bf16]
   uint32_t* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -645,6 +647,10 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value) {
       if (value < 0 || value > 1) return TTC_ERR_INVALID_ARG;
       g_gemv_off.store((int)value);
       return TTC_OK;
+    case TTC_KNOB_PAIR_EPI_WARPS:
+      if (value != 0 && value != 8 && value != 12) return TTC_ERR_INVALID_ARG;
+      g_pair_epi_warps.store((int)value);
+      return TTC_OK;
     case TTC_KNOB_I8_WIDE:
       if (value < 0 || value > 2) return TTC_ERR_INVALID_ARG;
       g_i8_wide.store((int)value);
@@ -1071,6 +1077,22 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       }
       prm.a_stream = prm.num_n_blocks == 1;
       prm.b_stream = prm.num_m_blocks == 1;
+      // rows TMA cannot store (written with plain stores, and C read from such
+      // rows too): twelve epilogue warps instead of eight drain a tile sooner
+      const int ew = g_pair_epi_warps.load();
+      if (!store_tma && pbn == 256 && ew != 8) {
+        int& cl12 = dev->pair_clusters_ew12[bf16 ? 1 : 0];
+        if (cl12 < 0) {
+          std::lock_guard<std::mutex> lk(g_mu);
+          if (cl12 < 0) cl12 = pair_max_clusters_ew12(bf16);
+        }
+        if (cl12 >= nclus) {
+          if (launch_pair_ew12(bf16, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+            return TTC_ERR_CUDA;
+          g_launches.fetch_add(1);
+          return TTC_OK;
+        }
+      }
       if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       return TTC_OK;

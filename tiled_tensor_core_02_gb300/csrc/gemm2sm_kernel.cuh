@@ -23,7 +23,9 @@
 //                no memory writes (a release arrive would also wait for the
 //                warp's outstanding C loads and stores).
 // Epilogue: eight warps, two per TMEM lane quarter; the first four drain the
-// left half of a tile's 32-column chunks, the other four the right half.
+// left half of a tile's 32-column chunks, the other four the right half.  For
+// outputs written with plain stores (rows TMA cannot store) a variant has
+// twelve, three per quarter, each draining a third of the chunks.
 // The layout of a CTA's half tiles, the epilogue and the error handling are
 // those of gemm_kernel (one CTA); every wait is bounded.
 //
@@ -45,15 +47,18 @@
 namespace ttc {
 
 constexpr int kPairBM = 256;
-constexpr int kPairEpiWarps = 8;   // two per TMEM lane quarter, each taking half of a tile's columns
-constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // warp 0 producer, warp 1 TMEM + MMA, warps 2..9 epilogue
+constexpr int kPairEpiWarps = 8;   // by default two per TMEM lane quarter, each taking half of a tile's columns
+constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // warp 0 producer, warp 1 TMEM + MMA, then the epilogue
 
 // Pair tile 256 x BN (BN = 256, 224, 192 or 128): each CTA stages 128 A rows and
 // BN / 2 B columns per k-block.  A pipeline stage holds kKPS = 2 k-blocks
 // (128 of K, 8 MMAs per barrier round trip): measured on GB300, one full/empty
 // round trip per 4 MMAs holds the pair to ~85 ns per N = 256 MMA, one per 8
 // MMAs to the tensor pipe's own ~67 ns, with as few as 2 stages.
-template <int BN, bool kI8 = false>
+// kEW: epilogue warps, 8 (two per TMEM lane quarter, each draining half of a
+// tile's columns) or 12 (three per quarter, a third each) for outputs whose
+// rows TMA cannot store, written with plain stores and no staging buffers.
+template <int BN, bool kI8 = false, int kEW = 8>
 struct PairCfg {
   static constexpr int kBHalf = BN / 2;
   static constexpr int kKPS = 2;                        // k-blocks per stage
@@ -64,9 +69,9 @@ struct PairCfg {
   static constexpr int kOutBytes = kI8 ? 4 : 2;
   static constexpr int kEpiBufBytes = 32 * kEpiCols * kOutBytes;
   // staging buffers per epilogue warp: two, or one for int8, whose warps
-  // store their chunks once per tile
-  static constexpr int kEpiBufs = kI8 ? 1 : 2;
-  static constexpr int kEpiBytes = kPairEpiWarps * kEpiBufs * kEpiBufBytes;
+  // store their chunks once per tile, or none with 12 epilogue warps
+  static constexpr int kEpiBufs = kI8 ? 1 : kEW == 8 ? 2 : 0;
+  static constexpr int kEpiBytes = kEW * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemLimit = 227 * 1024;
   static constexpr int kStagesRaw = (kSmemLimit - 1024 - kBarBytes - kEpiBytes) / kStageBytes;
@@ -75,6 +80,7 @@ struct PairCfg {
   static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarBytes;
   static_assert(BN == 256 || BN == 224 || BN == 192 || BN == 128, "pair tile width");
   static_assert(!kI8 || BN == 256, "int8: 256-wide tiles (a warp's running sums cover at most 4 chunks)");
+  static_assert(kEW == 8 || (kEW == 12 && !kI8), "epilogue warps: 8, or 12 for 16-bit plain-store outputs");
   static_assert(kStages >= 2, "pipeline depth");
   static_assert(kSmemBytes <= kSmemLimit, "shared memory budget");
 };
@@ -89,11 +95,11 @@ __device__ __forceinline__ void tma_load_boxes_pair(uint8_t* dst, const CUtensor
   if (bm.boxes > 1) tma_load_3d_pair(dst + bm.smem_step, m, x + bm.box_step, y, z, bar_leader, pol);
 }
 
-template <int BN, bool kBF16, bool kI8 = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+template <int BN, bool kBF16, bool kI8 = false, int kEW = 8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kEW, 1)
     gemm_pair_kernel(const __grid_constant__ GemmParams p) {
   static_assert(!(kI8 && kBF16), "int8 runs on fp16 copies");
-  using PairCfg = ttc::PairCfg<BN, kI8>;
+  using PairCfg = ttc::PairCfg<BN, kI8, kEW>;
   constexpr int kPairBN = BN;
   constexpr int S = PairCfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -128,7 +134,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     }
     if (lane < 2) {
       mbar_init(&tmem_full[lane], 1);
-      mbar_init(&tmem_empty[lane], 2 * kPairEpiWarps);
+      mbar_init(&tmem_empty[lane], 2 * kEW);
     }
     if (lane == 0) {
       mbar_init(stall_bar, 1);
@@ -314,7 +320,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     // ---------------------------------------------------------------- epilogue (both CTAs)
     const int ew = warp - 2;
     const int q = warp & 3;
-    const int part = ew >> 2;  // which half of a tile's columns this warp drains
+    const int part = ew >> 2;  // which half (third) of a tile's columns this warp drains
+    constexpr int kParts = kEW / 4;
     uint8_t* stage_buf = sEpi + ew * PairCfg::kEpiBufs * PairCfg::kEpiBufBytes;
     int buf = 0;
     int it = 0;
@@ -441,8 +448,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const bool row_ok = grow < p.M;
         const EpiPtrs ep = epi_ptrs(p, bz, 2);
         if (part == 0) prefetch_c(u + num_pairs);
-        const int c_lo = part == 0 ? 0 : (chunks + 1) / 2;
-        const int c_hi = part == 0 ? (chunks + 1) / 2 : chunks;
+        const int c_lo = (part * chunks + kParts - 1) / kParts;
+        const int c_hi = ((part + 1) * chunks + kParts - 1) / kParts;
         // the first chunk's C is fetched before waiting for the accumulator
         CChunk16 cc;
         c_fetch16(p, ep, c_path(p, ep, n0 + c_lo * chunk), grow, n0 + c_lo * chunk, lane, cc);

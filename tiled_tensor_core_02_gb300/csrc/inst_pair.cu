@@ -8,7 +8,7 @@
 namespace ttc {
 
 namespace {
-template <int BN, bool kBF16, bool kI8 = false>
+template <int BN, bool kBF16, bool kI8 = false, int kEW = 8>
 cudaError_t set_smem_attr() {
   static std::atomic<bool> done[64];
   int dev = 0;
@@ -16,37 +16,37 @@ cudaError_t set_smem_attr() {
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!done[dev].load()) {
-    e = cudaFuncSetAttribute(gemm_pair_kernel<BN, kBF16, kI8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             PairCfg<BN, kI8>::kSmemBytes);
+    e = cudaFuncSetAttribute(gemm_pair_kernel<BN, kBF16, kI8, kEW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             PairCfg<BN, kI8, kEW>::kSmemBytes);
     if (e != cudaSuccess) return e;
     done[dev].store(true);
   }
   return cudaSuccess;
 }
 
-template <int BN, bool kBF16, bool kI8 = false>
+template <int BN, bool kBF16, bool kI8 = false, int kEW = 8>
 int max_clusters() {
-  if (set_smem_attr<BN, kBF16, kI8>() != cudaSuccess) return 0;
+  if (set_smem_attr<BN, kBF16, kI8, kEW>() != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<BN, kI8>::kSmemBytes;
+  cfg.blockDim = dim3(64 + 32 * kEW, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<BN, kI8, kEW>::kSmemBytes;
   int n = 0;
-  return cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, kBF16, kI8>, &cfg) == cudaSuccess ? n : 0;
+  return cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<BN, kBF16, kI8, kEW>, &cfg) == cudaSuccess ? n : 0;
 }
 
-template <int BN, bool kBF16, bool kI8 = false>
+template <int BN, bool kBF16, bool kI8 = false, int kEW = 8>
 cudaError_t launch(const GemmParams& p, int clusters, cudaStream_t stream) {
-  const cudaError_t e = set_smem_attr<BN, kBF16, kI8>();
+  const cudaError_t e = set_smem_attr<BN, kBF16, kI8, kEW>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters, 1, 1);  // clusters of 2 from the kernel's __cluster_dims__
-  cfg.blockDim = dim3(kPairThreads, 1, 1);
-  cfg.dynamicSmemBytes = PairCfg<BN, kI8>::kSmemBytes;
+  cfg.blockDim = dim3(64 + 32 * kEW, 1, 1);
+  cfg.dynamicSmemBytes = PairCfg<BN, kI8, kEW>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   add_pdl_attribute(cfg, attr);
-  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, kBF16, kI8>, p);
+  const cudaError_t le = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<BN, kBF16, kI8, kEW>, p);
   if (le != cudaSuccess) return le;
   return cudaGetLastError();
 }
@@ -68,6 +68,17 @@ int pair_max_clusters_i8() { return max_clusters<256, false, true>(); }
 
 cudaError_t launch_pair_i8(const GemmParams& p, int clusters, cudaStream_t stream) {
   return launch<256, false, true>(p, clusters, stream);
+}
+
+// 256-wide tiles with twelve epilogue warps and no staging buffers: only for
+// outputs written with plain stores (p.d_tma == 0).
+int pair_max_clusters_ew12(bool bf16) {
+  return bf16 ? max_clusters<256, true, false, 12>() : max_clusters<256, false, false, 12>();
+}
+
+cudaError_t launch_pair_ew12(bool bf16, const GemmParams& p, int clusters, cudaStream_t stream) {
+  if (p.d_tma) return cudaErrorInvalidValue;
+  return bf16 ? launch<256, true, false, 12>(p, clusters, stream) : launch<256, false, false, 12>(p, clusters, stream);
 }
 
 cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream) {
