@@ -597,23 +597,6 @@ def test_unaligned_c_and_d_rows(pair, N, ew, c_off, d_off):
         ttc.ttc_set_knob("pair_tile_n", 0)
 
 
-@pytest.mark.parametrize("beta", [0.0, 0.5])
-def test_pair_twelve_epilogue_warps_tma_store(beta):
-    """Twelve epilogue warps forced on TMA-stored outputs: one staging buffer
-    per warp, each chunk's store read out before the next chunk fills it."""
-    ttc.ttc_set_knob("pair", 1)
-    ttc.ttc_set_knob("pair_tile_n", 256)
-    ttc.ttc_set_knob("pair_epi_warps", 12)
-    try:
-        p = synth.Problem(520, 768, 200, dtype="bf16", seed=51, distC="uniform", dist_bias="normal:0.5")
-        d = run(p, 1.25, beta, "relu")
-        check_full(p, d, 1.25, beta, "relu")
-    finally:
-        ttc.ttc_set_knob("pair", 0)
-        ttc.ttc_set_knob("pair_tile_n", 0)
-        ttc.ttc_set_knob("pair_epi_warps", 0)
-
-
 def test_workspace_too_small_falls_back():
     p = synth.Problem(257, 131, 97, dtype="bf16", seed=32, distC="uniform", lda=98, ldb=99)
     d = run(p, 1.0, 1.0, workspace=64)

@@ -1080,7 +1080,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       // rows TMA cannot store (written with plain stores, and C read from such
       // rows too): twelve epilogue warps instead of eight drain a tile sooner
       const int ew = g_pair_epi_warps.load();
-      if (pbn == 256 && (ew == 12 || (!store_tma && ew != 8))) {
+      if (!store_tma && pbn == 256 && ew != 8) {
         int& cl12 = dev->pair_clusters_ew12[bf16 ? 1 : 0];
         if (cl12 < 0) {
           std::lock_guard<std::mutex> lk(g_mu);

@@ -56,8 +56,8 @@ constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;  // warp 0 producer, warp 
 // round trip per 4 MMAs holds the pair to ~85 ns per N = 256 MMA, one per 8
 // MMAs to the tensor pipe's own ~67 ns, with as few as 2 stages.
 // kEW: epilogue warps, 8 (two per TMEM lane quarter, each draining half of a
-// tile's columns) or 12 (three per quarter, a third each, one staging buffer
-// per warp so that the stages keep their shared memory).
+// tile's columns) or 12 (three per quarter, a third each) for outputs whose
+// rows TMA cannot store, written with plain stores and no staging buffers.
 template <int BN, bool kI8 = false, int kEW = 8>
 struct PairCfg {
   static constexpr int kBHalf = BN / 2;
@@ -69,8 +69,8 @@ struct PairCfg {
   static constexpr int kOutBytes = kI8 ? 4 : 2;
   static constexpr int kEpiBufBytes = 32 * kEpiCols * kOutBytes;
   // staging buffers per epilogue warp: two, or one for int8, whose warps
-  // store their chunks once per tile, and with 12 epilogue warps
-  static constexpr int kEpiBufs = kI8 || kEW == 12 ? 1 : 2;
+  // store their chunks once per tile, or none with 12 epilogue warps
+  static constexpr int kEpiBufs = kI8 ? 1 : kEW == 8 ? 2 : 0;
   static constexpr int kEpiBytes = kEW * kEpiBufs * kEpiBufBytes;
   static constexpr int kBarBytes = 256;
   static constexpr int kSmemLimit = 227 * 1024;
@@ -481,14 +481,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(64 + 32 * kEW, 1)
           uint32_t packed[16];
           epi_f16_values<kBF16>(p, r, row_ok, grow, gcol0, packed, c_path(p, ep, gcol0), cc, ep);
           if (c + 1 < c_hi) c_fetch16(p, ep, c_path(p, ep, gcol0 + chunk), grow, gcol0 + chunk, lane, cc);
-          if constexpr (PairCfg::kEpiBufs == 1) {
-            // one staging buffer: the previous chunk's store must have read it
-            if (p.d_tma && lane == 0) bulk_wait_read<0>();
-            __syncwarp();
-          }
           epi_store_chunk<2>(p, packed, row_ok, grow, gcol0, grow - lane * p.maps.epi_row_step, stage_buf,
-                             PairCfg::kEpiBufs == 2 ? PairCfg::kEpiBufBytes : 0, buf, carry, c == c_hi - 1, lane,
-                             ep);
+                             PairCfg::kEpiBufBytes, buf, carry, c == c_hi - 1, lane, ep);
         }
       }
     }

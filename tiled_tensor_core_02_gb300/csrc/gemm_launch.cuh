@@ -17,7 +17,8 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 // bn: the pair tile's width (256, 224, 192 or 128).
 int pair_max_clusters(bool bf16, int bn);
 cudaError_t launch_pair(bool bf16, int bn, const GemmParams& p, int clusters, cudaStream_t stream);
-// 256-wide tiles with twelve epilogue warps.
+// 256-wide tiles with twelve epilogue warps, for outputs written with plain
+// stores (p.d_tma == 0; cudaErrorInvalidValue otherwise).
 int pair_max_clusters_ew12(bool bf16);
 cudaError_t launch_pair_ew12(bool bf16, const GemmParams& p, int clusters, cudaStream_t stream);
 // Its int8 variant: fp16 copies of int8 operands, exact int32 result, 256-wide tiles.

@@ -70,12 +70,14 @@ cudaError_t launch_pair_i8(const GemmParams& p, int clusters, cudaStream_t strea
   return launch<256, false, true>(p, clusters, stream);
 }
 
-// 256-wide tiles with twelve epilogue warps (one staging buffer each).
+// 256-wide tiles with twelve epilogue warps and no staging buffers: only for
+// outputs written with plain stores (p.d_tma == 0).
 int pair_max_clusters_ew12(bool bf16) {
   return bf16 ? max_clusters<256, true, false, 12>() : max_clusters<256, false, false, 12>();
 }
 
 cudaError_t launch_pair_ew12(bool bf16, const GemmParams& p, int clusters, cudaStream_t stream) {
+  if (p.d_tma) return cudaErrorInvalidValue;
   return bf16 ? launch<256, true, false, 12>(p, clusters, stream) : launch<256, false, false, 12>(p, clusters, stream);
 }
 
