@@ -881,8 +881,9 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       for (int cand = max_bn; cand >= 32; cand /= 2) {
         if (forced_bn != 0 && cand != forced_bn) continue;
         if (bk_mn && cand < 64) continue;
-        // a tile wider than the padded N only wastes work
-        if (forced_bn == 0 && cand > 32 && cand / 2 >= nk) continue;
+        // a tile wider than the padded N only wastes work (but an MN-major B
+        // needs whole 64-column slabs, so 64 stays a candidate for it)
+        if (forced_bn == 0 && cand > (bk_mn ? 64 : 32) && cand / 2 >= nk) continue;
         const int64_t tiles = batch * ((mk + kBM - 1) / kBM) * ((nk + cand - 1) / cand);
         const int sp = forced_bn == 0 ? split_for(tiles, cand) : 1;
         const double rate = cand == 256 ? 1.0 : cand == 128 ? 0.7 : cand == 64 ? 0.45 : 0.3;
