@@ -684,6 +684,21 @@ def test_batched_int8():
     check_batches(probs, outs, 1.0, 0.0)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "i8"])
+def test_batched_aligned_rows_but_odd_batch_strides(dtype):
+    """Rows whose pitch allows vector loads, but a batch stride that moves
+    every other batch off the vector boundary (and a row-major B whose pitch
+    TMA cannot describe, so the plain-load producers run): each batch's
+    start decides the vector loads too."""
+    dist = "int8" if dtype == "i8" else "uniform"
+    probs = batch_problems(5, 256, 129, 128, dtype=dtype, la="row", lb="row", distA=dist, distB=dist, distC=dist,
+                           ldc=130)
+    p0 = probs[0]
+    strides = {"A": p0.A.size + 3, "B": p0.B.size + 1, "C": p0.C.size, "D": 256 * 129}
+    outs = run_batched(probs, strides, 1.0, 1.0)
+    check_batches(probs, outs, 1.0, 1.0)
+
+
 @pytest.mark.parametrize("M,N,K", [(16, 1024, 2048), (1024, 24, 1024)])
 def test_batched_skinny_split_and_transpose(M, N, K):
     probs = batch_problems(3, M, N, K, distC="uniform")

@@ -997,14 +997,19 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   }
 
   // generic producers: 8-element groups load as one vector when every group
-  // start is aligned (16 bytes for 16-bit types, 8 bytes for int8)
+  // start is aligned (16 bytes for 16-bit types, 8 bytes for int8), in every
+  // batch: the batch stride keeps each batch's start aligned too
   const int vec_bytes = 8 * in_esize;
+  auto vec_ok = [&](const void* base, int64_t ld, int64_t bs) {
+    return reinterpret_cast<uintptr_t>(base) % vec_bytes == 0 && (ld * in_esize) % vec_bytes == 0 &&
+           (batch <= 1 || (bs * in_esize) % vec_bytes == 0);
+  };
   prm.A = A;
   prm.B = B;
   prm.lda = lda;
   prm.ldb = ldb;
-  prm.a_vec = reinterpret_cast<uintptr_t>(A) % vec_bytes == 0 && (lda * in_esize) % vec_bytes == 0;
-  prm.b_vec = reinterpret_cast<uintptr_t>(B) % vec_bytes == 0 && (ldb * in_esize) % vec_bytes == 0;
+  prm.a_vec = vec_ok(A, lda, sA);
+  prm.b_vec = vec_ok(B, ldb, sB);
   prm.M = (int)M;
   prm.N = (int)N;
   prm.K = (int)K;
