@@ -19,7 +19,9 @@
  * M x N, row-major, with leading dimensions ldc and ldd.  For TTC_F16 and
  * TTC_BF16, C and D have the input type and the product is accumulated in
  * fp32.  For TTC_I8, A and B are int8 and C and D are int32; the result is
- * exact.  bias is fp32[N] (added per output column) or NULL.
+ * exact.  bias is fp32[N] (added per output column) or NULL.  Only D's M x N
+ * elements are written: the pitch padding of its rows (columns N .. ldd - 1)
+ * and any memory between batches keep their contents.
  *
  * Ownership.  Every pointer is caller-owned device memory.  The library keeps
  * no reference to any of it after the call returns and allocates no device

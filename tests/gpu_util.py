@@ -61,10 +61,12 @@ def run(p, alpha=1.0, beta=0.0, act="none", use_bias=True, ldd=None, D=None, C_d
     return d[: p.M * ldd].reshape(p.M, ldd)[:, : p.N] if p.M else d[:0].reshape(0, p.N)
 
 
-def run_batched(probs, strides, alpha=1.0, beta=0.0, act="none", share_b=False, ldd=None):
+def run_batched(probs, strides, alpha=1.0, beta=0.0, act="none", share_b=False, ldd=None, full=None):
     """Packs a list of same-shaped problems into strided buffers (stride in
     elements per operand: dict with keys A, B, C, D; B's stride 0 when
-    share_b), runs ttc_gemm_strided_batched, and returns one output per batch."""
+    share_b), runs ttc_gemm_strided_batched, and returns one output per batch
+    (and appends the whole D buffer, -1 where nothing was written, to the list
+    `full` when one is given)."""
     p0 = probs[0]
     nb = len(probs)
     out_np = np.int32 if p0.dtype == "i8" else np.int16
@@ -95,6 +97,8 @@ def run_batched(probs, strides, alpha=1.0, beta=0.0, act="none", share_b=False, 
     assert st == 0, ttc.STATUS.get(st, st)
     assert ttc.ttc_get_device_error(s) == 0
     d = D.cpu().numpy()
+    if full is not None:
+        full.append(d.copy())
     if out_np == np.int16:
         d = d.view(np.uint16)
     return [d[i * sD:i * sD + p0.M * ldd].reshape(p0.M, ldd)[:, :p0.N] for i in range(nb)]

@@ -9,8 +9,11 @@ int8 calls.  The planner picks the kernel (CTA pair or single CTA, tile
 width, orientation, split K, matrix-vector kernels) from each shape.  Then
 random strided batches (gaps between batches, a shared B), random
 convolutions (filter sizes, padding, strides, dilations, channel counts on
-and off the 64-channel blocks, an unaligned input, a padded output pitch)
-and random transposes (every element size, tight, odd and 16-byte pitches)."""
+and off the 64-channel blocks, an unaligned input, a padded output pitch),
+random transposes (every element size, tight, odd and 16-byte pitches), and
+GEMMs whose A, B, C and D start at element offsets off every alignment,
+through each entry point including the static-scratch one (nothing outside
+D's elements written)."""
 import numpy as np
 import pytest
 
@@ -185,3 +188,96 @@ def test_random_transpose_matches_oracle(case):
     want = oracle.transpose(src, rows, cols, lds, ldd).reshape(cols, ldd)
     assert np.array_equal(got[:, :rows], want[:, :rows])
     assert (got[:, rows:] == np.iinfo(synth.ELEM_DTYPE[eb]).max).all()  # the pitch padding is not written
+
+
+# ---------------------------------------------------------------- base pointers at any element offset
+def _offset_cases(n=200, seed=20261206):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        dtype = str(rng.choice(["bf16", "bf16", "f16", "i8"]))
+        M, N, K = (int(rng.choice(SIZES_MN)), int(rng.choice(SIZES_MN)), int(rng.choice(SIZES_K)))
+        la, lb = str(rng.choice(["row", "col"])), str(rng.choice(["row", "col"]))
+        pad = [int(rng.choice([0, 0, 1, 8])) for _ in range(4)]
+        offs = [int(rng.choice([0, 0, 1, 3, 8])) for _ in range(4)]  # elements before A, B, C, D
+        if rng.integers(0, 3) == 0:
+            # D's pitch rounded up to 16 bytes (TMA can store its rows) and its
+            # start kept aligned: the rows end inside a 16-byte granule
+            per16 = 4 if dtype == "i8" else 8
+            pad[3] = -N % per16
+            offs[3] = 0
+        entry = str(rng.choice(["plain", "ws_repack", "ws_staged", "static"]))
+        if dtype == "i8":
+            alpha, beta, act, bias = 1.0, float(rng.choice([0.0, 1.0])), "none", False
+        else:
+            alpha, beta = float(rng.choice([1.0, 0.5])), float(rng.choice([0.0, 1.0, 0.25]))
+            act, bias = str(rng.choice(ACTS)), bool(rng.integers(0, 2))
+        out.append((i, dtype, M, N, K, la, lb, pad, offs, entry, alpha, beta, act, bias))
+    return out
+
+
+def _at_offset(host, off):
+    """A device copy of `host` that starts `off` elements into its allocation,
+    and the allocation."""
+    from gpu_util import to_dev
+    buf = to_dev(np.concatenate([np.zeros(off, host.dtype), host, np.zeros(8, host.dtype)]))
+    return buf, buf.data_ptr() + off * host.dtype.itemsize
+
+
+@pytest.mark.parametrize("case", _offset_cases(),
+                         ids=lambda c: f"{c[0]}-{c[1]}-{c[2]}x{c[3]}x{c[4]}-{c[5]}{c[6]}-{c[9]}")
+def test_random_offsets_match_oracle(case):
+    import torch
+    from gpu_util import LAY
+    i, dtype, M, N, K, la, lb, pad, offs, entry, alpha, beta, act, bias = case
+    lda = (K if la == "row" else M) + pad[0]
+    ldb = (N if lb == "row" else K) + pad[1]
+    ldc, ldd = N + pad[2], N + pad[3]
+    dist = "int8" if dtype == "i8" else "uniform"
+    p = synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=11000 + i, distA=dist, distB=dist,
+                      distC=dist if beta != 0.0 else None, dist_bias="normal:0.5" if bias else None,
+                      lda=lda, ldb=ldb, ldc=ldc)
+    A, a_ptr = _at_offset(p.A, offs[0])
+    B, b_ptr = _at_offset(p.B, offs[1])
+    c_ptr = None
+    if p.C is not None:
+        C, c_ptr = _at_offset(p.C, offs[2])
+    out_t = torch.int32 if dtype == "i8" else torch.int16
+    out_size = 4 if dtype == "i8" else 2
+    D = torch.full((offs[3] + M * ldd + 8,), -1, dtype=out_t, device="cuda")
+    d_ptr = D.data_ptr() + offs[3] * out_size
+    bias_dev = torch.from_numpy(p.bias).cuda() if bias else None
+    s = torch.cuda.current_stream().cuda_stream
+    args = (M, N, K, a_ptr, lda, LAY[la], b_ptr, ldb, LAY[lb], c_ptr if beta != 0.0 else None, ldc, d_ptr, ldd,
+            alpha, beta, bias_dev.data_ptr() if bias else None, ttc.ACT[act], ttc.DTYPE[dtype])
+    if entry == "plain":
+        st = ttc.ttc_gemm(*args, s)
+    elif entry == "static":
+        st = ttc.ttc_gemm_static_scratch(*args, s)
+    else:
+        if entry == "ws_staged":
+            need = ttc.ttc_gemm_workspace_size_staged(M, N, K, a_ptr, lda, LAY[la], b_ptr, ldb, LAY[lb], d_ptr,
+                                                      ldd, ttc.DTYPE[dtype])
+        else:
+            need = ttc.ttc_gemm_workspace_size(M, N, K, a_ptr, lda, LAY[la], b_ptr, ldb, LAY[lb], ttc.DTYPE[dtype])
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+        st = ttc.ttc_gemm_ws(*args, ws.data_ptr() if need else None, need, s)
+    if entry == "static" and st == 5:
+        return  # more scratch than the static array holds: refused before any work
+    assert st == 0, ttc.STATUS.get(st, st)
+    assert ttc.ttc_get_device_error(s) == 0
+    full = D.cpu().numpy()
+    if dtype != "i8":
+        full = full.view(np.uint16)
+    none = np.int32(-1) if dtype == "i8" else np.uint16(0xFFFF)
+    assert np.all(full[:offs[3]] == none) and np.all(full[offs[3] + M * ldd:] == none)
+    rows = full[offs[3]:offs[3] + M * ldd].reshape(M, ldd)
+    assert np.all(rows[:, N:] == none)  # the pitch padding is not written
+    d = rows[:, :N]
+    r, sabs = oracle.gemm_full(p, alpha=alpha, beta=beta, act=act, use_bias=bias)
+    if dtype == "i8":
+        assert np.array_equal(d.astype(np.int64), r.astype(np.int64))
+        return
+    ok, worst, w = oracle.check_float(oracle.decode(np.ascontiguousarray(d).ravel(), dtype), r.ravel(),
+                                      sabs.ravel(), dtype)
+    assert ok, f"worst error ratio {worst:.3f} at {divmod(w, N)}"

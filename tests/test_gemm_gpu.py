@@ -597,6 +597,57 @@ def test_unaligned_c_and_d_rows(pair, N, ew, c_off, d_off):
         ttc.ttc_set_knob("pair_tile_n", 0)
 
 
+@pytest.mark.parametrize("dtype,M,N,K,ldd,pair,ws", [
+    ("bf16", 300, 300, 64, 304, 0, None), ("bf16", 300, 297, 64, 304, 0, None),
+    ("bf16", 600, 601, 128, 608, 1, None), ("bf16", 600, 601, 128, 608, 2, None),
+    ("f16", 40, 300, 64, 304, 0, None), ("bf16", 300, 12, 64, 16, 2, None),
+    ("i8", 300, 255, 64, 256, 0, None), ("i8", 300, 254, 64, 256, 0, None), ("i8", 1, 255, 16, 255, 0, None),
+    ("i8", 2048, 2049, 64, 2052, 0, -2)])
+def test_tma_stored_rows_leave_the_pitch_padding(dtype, M, N, K, ldd, pair, ws):
+    """D rows TMA can store (16-byte aligned pitch) whose length is not a
+    whole number of 16-byte granules: a TMA store clips at the row's end only
+    to the granule, so the tensor map stops at the last whole granule and the
+    epilogue writes the rest; nothing in the pitch padding is written.  The
+    last case runs int8 on the CTA-pair path (fp16 copies in the workspace);
+    M = 1 lets the planner pick its own pitch for D's single row."""
+    dist = "int8" if dtype == "i8" else "uniform"
+    p = synth.Problem(M, N, K, dtype=dtype, seed=71, distA=dist, distB=dist, distC=dist)
+    beta = 1.0
+    out_t = torch.int32 if dtype == "i8" else torch.int16
+    D = torch.full((M * ldd + 16,), -1, dtype=out_t, device="cuda")
+    ttc.ttc_set_knob("pair", pair)
+    try:
+        d = run(p, 1.0, beta, D=D, ldd=ldd, workspace=ws)
+    finally:
+        ttc.ttc_set_knob("pair", 0)
+    check_full(p, d, 1.0, beta)
+    full = D.cpu().numpy()
+    rows = full[:M * ldd].reshape(M, ldd)
+    assert np.all(rows[:, N:] == -1) and np.all(full[M * ldd:] == -1)
+
+
+def test_batched_and_conv_tma_rows_leave_the_pitch_padding():
+    probs = batch_problems(3, 300, 300, 64, distC="uniform")
+    p0 = probs[0]
+    sD = 300 * 304 + 8
+    full = []
+    outs = run_batched(probs, {"A": p0.A.size, "B": p0.B.size, "C": p0.C.size, "D": sD}, 1.0, 1.0, ldd=304,
+                       full=full)
+    check_batches(probs, outs, 1.0, 1.0)
+    written = np.zeros(full[0].size, dtype=bool)
+    for b in range(3):
+        rows = np.arange(b * sD, b * sD + 300 * 304).reshape(300, 304)[:, :300]
+        written[rows.ravel()] = True
+    assert np.all(full[0][~written] == -1)  # pitch padding and the gaps between batches
+    from test_conv_gpu import run_conv
+    cp = synth.ConvProblem(2, 10, 10, 16, 70, 3, 3, (1, 1), (1, 1), (1, 1), dtype="bf16", seed=72)
+    out = run_conv(cp, ldd=72).reshape(-1)[:cp.M * 72].reshape(cp.M, 72)
+    r, sabs = oracle.conv_full(cp)
+    ok, worst, w = oracle.check_float(oracle.decode(out[:, :70], "bf16").ravel(), r.ravel(), sabs.ravel(), "bf16")
+    assert ok, worst
+    assert np.all(out[:, 70:] == 0xFFFF)
+
+
 def test_workspace_too_small_falls_back():
     p = synth.Problem(257, 131, 97, dtype="bf16", seed=32, distC="uniform", lda=98, ldb=99)
     d = run(p, 1.0, 1.0, workspace=64)

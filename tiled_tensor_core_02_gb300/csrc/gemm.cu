@@ -178,6 +178,13 @@ bool tma_batch_ok(int64_t batch, int64_t stride, int esize) {
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// Columns of a D row that TMA stores: the whole 16-byte granules.  A tiled
+// TMA store clips at a row's end only to 16-byte granularity (measured: with
+// N = 300 bf16 columns and a pitch of 304 it also wrote columns 300..303), so
+// the tensor map ends at the last whole granule and the epilogue stores the
+// rest of the row (under 16 bytes) itself.
+int64_t tma_store_cols(int64_t N, int esize) { return N & ~(int64_t)(16 / esize - 1); }
+
 // CTA-pair tile width for an M x N problem (times batch): the width whose
 // tiles fill the resident pairs best, weighted by the width's measured
 // relative rate (a narrower tile stages more A per column: 1, 0.95, 0.87,
@@ -402,7 +409,8 @@ ttc_status gemm_i8_wide(DeviceInfo* dev, const I8Wide& w, int64_t M, int64_t N, 
   const CUtensorMapDataType f16 = CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   if (!encode_operand(&prm.tmA, f16, 2, A16, M, K, w.a_ld, prm.maps.a, CU_TENSOR_MAP_SWIZZLE_128B) ||
       !encode_operand(&prm.tmB, f16, 2, B16, N, K, w.b_ld, prm.maps.b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_128B))
+      !encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, tma_store_cols(N, 4), M, ldd, kEpiCols, 32,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
     return TTC_ERR_CUDA;
   prm.A = A16;
   prm.B = B16;
@@ -947,8 +955,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     mode = dtype == TTC_BF16 ? kModeTmaBF16 : kModeTmaF16;
   else
     mode = dtype == TTC_BF16 ? kModeGenBF16 : kModeGenF16;
-  const bool store_tma =
-      !swap && tma_ok(D, ldd, out_esize) && tma_batch_ok(batch, sD, out_esize) && !g_force_generic_store.load();
+  const bool store_tma = !swap && tma_ok(D, ldd, out_esize) && tma_batch_ok(batch, sD, out_esize) &&
+                         tma_store_cols(N, out_esize) > 0 && !g_force_generic_store.load();
   // batch dimensions of the tensor maps: a shared operand (stride 0) keeps one batch
   const BatchDim bdA{batch > 1 && sA != 0 ? (uint64_t)batch : 1u, (uint64_t)sA};
   const BatchDim bdB{batch > 1 && sB != 0 ? (uint64_t)batch : 1u, (uint64_t)sB};
@@ -990,9 +998,10 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   }
   if (store_tma) {
     const bool ok = dtype == TTC_I8
-                        ? encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, N, M, ldd, kEpiCols, 32,
-                                    CU_TENSOR_MAP_SWIZZLE_128B, bdD)
-                        : encode_3d(&prm.tmD, dt, 2, D, N, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B, bdD);
+                        ? encode_3d(&prm.tmD, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, D, tma_store_cols(N, 4), M, ldd,
+                                    kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_128B, bdD)
+                        : encode_3d(&prm.tmD, dt, 2, D, tma_store_cols(N, 2), M, ldd, kEpiCols, 32,
+                                    CU_TENSOR_MAP_SWIZZLE_64B, bdD);
     if (!ok) return TTC_ERR_CUDA;
   }
 
@@ -1198,12 +1207,12 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
   }
   if (bn == 0) return TTC_ERR_UNSUPPORTED;
   const int mode = dtype == TTC_BF16 ? kModeConvBF16 : kModeConvF16;
-  const bool store_tma = tma_ok(D, ldd, 2) && !g_force_generic_store.load();
+  const bool store_tma = tma_ok(D, ldd, 2) && tma_store_cols(K, 2) > 0 && !g_force_generic_store.load();
 
   GemmParams prm;
   std::memset(&prm, 0, sizeof prm);
   const CUtensorMapDataType dt = dtype == TTC_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  if (store_tma && !encode_3d(&prm.tmD, dt, 2, D, K, M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
+  if (store_tma && !encode_3d(&prm.tmD, dt, 2, D, tma_store_cols(K, 2), M, ldd, kEpiCols, 32, CU_TENSOR_MAP_SWIZZLE_64B))
     return TTC_ERR_CUDA;
   // the im2col A and the filters are both K-major operands
   if (!tile_maps({kBM, bn, 1, kBM, 0, 0, 2, 1, 0}, prm.maps)) return TTC_ERR_UNSUPPORTED;

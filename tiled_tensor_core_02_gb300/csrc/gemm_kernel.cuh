@@ -822,6 +822,30 @@ __device__ __forceinline__ void epi_store_chunk(const GemmParams& p, const uint3
       bulk_commit();
     }
     buf ^= 1;
+    // The tensor map ends at the row's last whole 16-byte granule (a TMA
+    // store clips only to granules); the columns after it, fewer than one
+    // granule, are stored here from the thread's own row.
+    constexpr int kGran = 16 / kOutBytes;  // elements per granule
+    const int n_full = p.N & ~(kGran - 1);
+    if (row_ok && n_full < p.N && gcol0 <= n_full && n_full < gcol0 + 32) {
+      const int g = (n_full - gcol0) / kGran;  // the chunk's granule holding the tail
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int q = 0; q < kPacked / 4; ++q)
+        if (q == g) v = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint8_t* dst = static_cast<uint8_t*>(e.D) + ((int64_t)grow * p.ldd + n_full) * kOutBytes;
+      const int cnt = p.N - n_full;
+#pragma unroll
+      for (int t = 0; t < kGran - 1; ++t) {
+        if (t < cnt) {
+          if constexpr (kOutBytes == 4)
+            reinterpret_cast<uint32_t*>(dst)[t] = w[t];
+          else
+            reinterpret_cast<uint16_t*>(dst)[t] = (uint16_t)((w[t >> 1] >> ((t & 1) * 16)) & 0xFFFFu);
+        }
+      }
+    }
   } else if (kOutBytes == 2 && !p.d_trans) {
     // 16-bit rows TMA cannot describe: each thread stores its own row's
     // 64 bytes as the aligned blocks that cover them; the block it shares with
