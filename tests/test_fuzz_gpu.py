@@ -13,7 +13,8 @@ and off the 64-channel blocks, an unaligned input, a padded output pitch),
 random transposes (every element size, tight, odd and 16-byte pitches), and
 GEMMs whose A, B, C and D start at element offsets off every alignment,
 through each entry point including the static-scratch one (nothing outside
-D's elements written)."""
+D's elements written).  The pitch padding of A, B and C, and the elements
+just before and after them, hold NaN (int8: 127), which no kernel may read."""
 import numpy as np
 import pytest
 
@@ -21,6 +22,7 @@ import oracle
 import synth
 import tiled_tensor_core_02_gb300 as ttc
 from gpu_util import run
+from test_gemm_gpu import _poison_padding
 
 pytestmark = pytest.mark.gpu
 
@@ -60,6 +62,7 @@ def test_random_problem_matches_oracle(case):
     p = synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=1000 + i, distA=dist, distB=dist,
                       distC=("int8" if dtype == "i8" else "uniform") if beta != 0.0 else None,
                       dist_bias="normal:0.5" if bias else None, lda=lda, ldb=ldb, ldc=ldc)
+    _poison_padding(p)
     ws = {"plain": None, "ws_repack": -1, "ws_staged": -2}[entry]
     ttc.ttc_set_knob("i8_wide", 1 if wide else 0)
     try:
@@ -216,11 +219,12 @@ def _offset_cases(n=200, seed=20261206):
     return out
 
 
-def _at_offset(host, off):
-    """A device copy of `host` that starts `off` elements into its allocation,
-    and the allocation."""
+def _at_offset(host, off, fill=0):
+    """A device copy of `host` that starts `off` elements into its allocation
+    (with `fill` before it and in 8 elements after it), and its address."""
     from gpu_util import to_dev
-    buf = to_dev(np.concatenate([np.zeros(off, host.dtype), host, np.zeros(8, host.dtype)]))
+    edge = np.full(off, fill, host.dtype), np.full(8, fill, host.dtype)
+    buf = to_dev(np.concatenate([edge[0], host, edge[1]]))
     return buf, buf.data_ptr() + off * host.dtype.itemsize
 
 
@@ -237,11 +241,13 @@ def test_random_offsets_match_oracle(case):
     p = synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=11000 + i, distA=dist, distB=dist,
                       distC=dist if beta != 0.0 else None, dist_bias="normal:0.5" if bias else None,
                       lda=lda, ldb=ldb, ldc=ldc)
-    A, a_ptr = _at_offset(p.A, offs[0])
-    B, b_ptr = _at_offset(p.B, offs[1])
+    _poison_padding(p)
+    nan = {"i8": 127, "bf16": 0x7FC0, "f16": 0x7E00}[dtype]
+    A, a_ptr = _at_offset(p.A, offs[0], nan)
+    B, b_ptr = _at_offset(p.B, offs[1], nan)
     c_ptr = None
     if p.C is not None:
-        C, c_ptr = _at_offset(p.C, offs[2])
+        C, c_ptr = _at_offset(p.C, offs[2], 1 << 30 if dtype == "i8" else nan)
     out_t = torch.int32 if dtype == "i8" else torch.int16
     out_size = 4 if dtype == "i8" else 2
     D = torch.full((offs[3] + M * ldd + 8,), -1, dtype=out_t, device="cuda")

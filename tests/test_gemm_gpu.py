@@ -626,6 +626,39 @@ def test_tma_stored_rows_leave_the_pitch_padding(dtype, M, N, K, ldd, pair, ws):
     assert np.all(rows[:, N:] == -1) and np.all(full[M * ldd:] == -1)
 
 
+def _poison_padding(p):
+    """Fills the pitch padding of A, B and C with NaN (int8: 127, int32 C:
+    2^30), which the oracle never reads: a kernel that read it would show."""
+    val = np.int8(127) if p.dtype == "i8" else np.uint16(0x7FC0 if p.dtype == "bf16" else 0x7E00)
+    for buf, rows, cols, ld, lay in ((p.A, p.M, p.K, p.lda, p.layoutA), (p.B, p.K, p.N, p.ldb, p.layoutB)):
+        if lay == "row":
+            buf.reshape(rows, ld)[:, cols:] = val
+        else:
+            buf.reshape(cols, ld)[:, rows:] = val
+    if p.C is not None:
+        p.C.reshape(p.M, p.ldc)[:, p.N:] = np.int32(1 << 30) if p.dtype == "i8" else val
+
+
+@pytest.mark.parametrize("ws", [None, -2], ids=["plain", "staged"])
+@pytest.mark.parametrize("M,N,K", [(300, 300, 100), (40, 300, 1000), (2048, 2049, 100)])
+@pytest.mark.parametrize("la,lb", synth.MAJORNESS)
+@pytest.mark.parametrize("dtype", ["bf16", "i8"])
+def test_operand_and_c_pitch_padding_is_never_read(dtype, la, lb, M, N, K, ws):
+    """Pitches padded past rows that end inside a 16-byte granule (TMA can
+    still read them), with NaN in every padding element: TMA loads fill past
+    a row's end with zeros element by element, and no other path reads the
+    padding either."""
+    per = 16 if dtype == "i8" else 8
+    ra, rb = (K if la == "row" else M), (N if lb == "row" else K)
+    lda, ldb = -(-ra // per) * per + (per if ra % per == 0 else 0), -(-rb // per) * per + (per if rb % per == 0 else 0)
+    dist = "int8" if dtype == "i8" else "uniform"
+    p = synth.Problem(M, N, K, dtype=dtype, layoutA=la, layoutB=lb, seed=73, distA=dist, distB=dist, distC=dist,
+                      lda=lda, ldb=ldb, ldc=-(-N // 8) * 8 + 8)
+    _poison_padding(p)
+    d = run(p, 1.0, 1.0, workspace=ws)
+    check_full(p, d, 1.0, 1.0)
+
+
 def test_batched_and_conv_tma_rows_leave_the_pitch_padding():
     probs = batch_problems(3, 300, 300, 64, distC="uniform")
     p0 = probs[0]
