@@ -358,6 +358,28 @@ ttc_status ttc_set_knob(ttc_knob knob, int64_t value);
 /* Number of kernel launches ttc_gemm has enqueued in this process. */
 int64_t ttc_launch_count(void);
 
+/*
+ * Planning aid for tests and tuning: runs the planner of ttc_gemm_ws and
+ * ttc_gemm_strided_batched (batch = 1 and workspace NULL describe ttc_gemm)
+ * as if on a GB300-class device with `sm_count` SMs (2 .. 4096), without
+ * touching any GPU: the pointers are only inspected for alignment and
+ * overlap, nothing is read, no tensor map is encoded and nothing is
+ * launched.  Writes the launches the call would make, as "kernel key=value
+ * ..." items separated by "; ", to `out` (NUL-terminated, cut to out_len - 1
+ * bytes; out may be NULL when out_len is 0), and returns the status the call
+ * would return.  Knobs set with ttc_set_knob apply as they do to real calls.
+ * Calls on other threads are unaffected while one thread plans.
+ * TTC_ERR_INVALID_ARG: sm_count out of range, or out NULL with out_len > 0.
+ */
+ttc_status ttc_gemm_plan(int64_t batch, int64_t M, int64_t N, int64_t K,
+                         const void* A, int64_t lda, int64_t strideA, ttc_layout layoutA,
+                         const void* B, int64_t ldb, int64_t strideB, ttc_layout layoutB,
+                         const void* C, int64_t ldc, int64_t strideC,
+                         void* D, int64_t ldd, int64_t strideD,
+                         float alpha, float beta, const float* bias,
+                         ttc_act act, ttc_dtype dtype, void* workspace, size_t workspace_bytes,
+                         int sm_count, char* out, size_t out_len);
+
 #ifdef __cplusplus
 }
 #endif

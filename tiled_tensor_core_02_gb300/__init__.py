@@ -35,7 +35,7 @@ KNOB = {"timeout_ns": 0, "inject_stall": 1, "force_generic_load": 2, "force_gene
 EXPORTS = ("ttc_gemm", "ttc_gemm_strided_batched", "ttc_gemm_ws", "ttc_gemm_workspace_size",
            "ttc_gemm_workspace_size_staged",
            "ttc_gemm_static_scratch", "ttc_transpose", "ttc_conv2d_fprop",
-           "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count")
+           "ttc_get_device_error", "ttc_status_string", "ttc_set_knob", "ttc_launch_count", "ttc_gemm_plan")
 
 _lib = None
 
@@ -86,6 +86,9 @@ def load():
     L.ttc_set_knob.restype = i
     L.ttc_launch_count.argtypes = []
     L.ttc_launch_count.restype = i64
+    L.ttc_gemm_plan.argtypes = [i64, i64, i64, i64, vp, i64, i64, i, vp, i64, i64, i, vp, i64, i64, vp, i64, i64,
+                                f, f, vp, i, i, vp, ctypes.c_size_t, i, ctypes.c_char_p, ctypes.c_size_t]
+    L.ttc_gemm_plan.restype = i
     _lib = L
     return L
 
@@ -128,6 +131,17 @@ def ttc_gemm_static_scratch(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D
     that cannot allocate device memory (see include/ttc.h)."""
     return load().ttc_gemm_static_scratch(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd,
                                           alpha, beta, bias, act, dtype, stream)
+
+
+def ttc_gemm_plan(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, strideB, layoutB, C, ldc, strideC, D, ldd,
+                  strideD, alpha, beta, bias, act, dtype, workspace, workspace_bytes, sm_count):
+    """(status, plan): the launches the call would make on a device with
+    sm_count SMs, planned on the host without a GPU (see include/ttc.h)."""
+    buf = ctypes.create_string_buffer(4096)
+    st = load().ttc_gemm_plan(batch, M, N, K, A, lda, strideA, layoutA, B, ldb, strideB, layoutB, C, ldc, strideC,
+                              D, ldd, strideD, alpha, beta, bias, act, dtype, workspace, workspace_bytes, sm_count,
+                              buf, len(buf))
+    return st, buf.value.decode()
 
 
 def ttc_gemm_workspace_size(M, N, K, A, lda, layoutA, B, ldb, layoutB, dtype) -> int:

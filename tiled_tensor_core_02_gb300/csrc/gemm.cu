@@ -5,12 +5,14 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdarg>
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <string>
 #include <tuple>
 #include <utility>
 
@@ -62,12 +64,36 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
 
+// Planning without a GPU (ttc_gemm_plan): while a thread plans, its calls
+// see a device of t_plan_dev.sm_count SMs, skip tensor-map encoding and
+// record each launch in *t_plan instead of making it.
+thread_local std::string* t_plan = nullptr;
+thread_local DeviceInfo t_plan_dev;
+
+// Appends one launch to the plan ("; " between launches).  Returns true when
+// the thread is planning, i.e. when the caller must not launch.
+bool plan_note(const char* fmt, ...) {
+  if (t_plan == nullptr) return false;
+  char buf[256];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (!t_plan->empty()) *t_plan += "; ";
+  *t_plan += buf;
+  return true;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 EncodeTiledFn g_encode = nullptr;
 
 ttc_status device_info(DeviceInfo** out) {
+  if (t_plan != nullptr) {
+    *out = &t_plan_dev;
+    return TTC_OK;
+  }
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return TTC_ERR_CUDA;
   std::lock_guard<std::mutex> lk(g_mu);
@@ -106,6 +132,7 @@ struct BatchDim {
 bool encode_3d(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
                uint64_t outer, uint64_t pitch_elems, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw,
                BatchDim bd = BatchDim()) {
+  if (t_plan != nullptr) return true;
   const uint64_t pitch = pitch_elems * (uint64_t)esize;
   // one batch: a stride past the matrix (any 16-byte multiple is accepted)
   const uint64_t bstride = bd.count > 1 ? bd.stride * (uint64_t)esize : (pitch * outer + 15) / 16 * 16;
@@ -452,11 +479,31 @@ ttc_status gemm_i8_wide(DeviceInfo* dev, const I8Wide& w, int64_t M, int64_t N, 
   prm.b_stream = prm.num_m_blocks == 1;
   const WidenSpec specs[2] = {{A, lda, w.a_rows, w.a_cols, ws + w.a_off, w.a_ld},
                               {B, ldb, w.b_rows, w.b_cols, ws + w.b_off, w.b_ld}};
-  if (launch_widen_i8(specs, 2, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+  if (!plan_note("widen_i8 a=%lldx%lld b=%lldx%lld", (long long)w.a_rows, (long long)w.a_cols,
+                 (long long)w.b_rows, (long long)w.b_cols) &&
+      launch_widen_i8(specs, 2, dev->sm_count, s) != cudaSuccess)
+    return TTC_ERR_CUDA;
   g_launches.fetch_add(1);
-  if (launch_pair_i8(prm, nclus, s) != cudaSuccess) return TTC_ERR_CUDA;
+  if (!plan_note("pair_i8 bn=256 clusters=%d tiles=%d units=%d", nclus, prm.num_tiles, prm.num_units) &&
+      launch_pair_i8(prm, nclus, s) != cudaSuccess)
+    return TTC_ERR_CUDA;
   g_launches.fetch_add(1);
   return TTC_OK;
+}
+
+const char* mode_name(int mode) {
+  switch (mode) {
+    case kModeTmaF16: return "tma_f16";
+    case kModeTmaBF16: return "tma_bf16";
+    case kModeGenF16: return "plain_f16";
+    case kModeGenBF16: return "plain_bf16";
+    case kModeI8: return "plain_i8";
+    case kModeI8Tma: return "tma_i8";
+    case kModeI8TmemA: return "tma_i8_tmem_a";
+    case kModeConvF16: return "conv_f16";
+    case kModeConvBF16: return "conv_bf16";
+    default: return "?";
+  }
 }
 
 template <int MODE>
@@ -792,10 +839,12 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
     if (gk == kGemvRows) {
       gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0 && gp.incx == 1 &&
                reinterpret_cast<uintptr_t>(gp.x) % 16 == 0;
-      if (launch_gemv_rows(gp, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+      if (!plan_note("gemv_rows vec=%d", gp.vec) && launch_gemv_rows(gp, dev->sm_count, s) != cudaSuccess)
+        return TTC_ERR_CUDA;
     } else {
       gp.vec = reinterpret_cast<uintptr_t>(gp.mat) % 16 == 0 && gp.ldm % 8 == 0;
-      if (launch_gemv_cols(gp, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+      if (!plan_note("gemv_cols vec=%d", gp.vec) && launch_gemv_cols(gp, dev->sm_count, s) != cudaSuccess)
+        return TTC_ERR_CUDA;
     }
     g_launches.fetch_add(1);
     return TTC_OK;
@@ -823,7 +872,8 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       int n = 0;
       if (rp.a) specs[n++] = RepackSpec{A, lda, rp.a_rows, rp.a_cols, ws + rp.a_off, rp.a_ld, in_esize};
       if (rp.b) specs[n++] = RepackSpec{B, ldb, rp.b_rows, rp.b_cols, ws + rp.b_off, rp.b_ld, in_esize};
-      if (launch_repack2(specs, n, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      if (!plan_note("repack a=%d b=%d", rp.a ? 1 : 0, rp.b ? 1 : 0) &&
+          launch_repack2(specs, n, dev->sm_count, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       if (rp.a) {
@@ -841,13 +891,15 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
       uint8_t* dst = static_cast<uint8_t*>(workspace) + ds.off;
       cudaStream_t s = static_cast<cudaStream_t>(stream);
       if (beta != 0.0f) {
-        if (launch_repack(C, ldc, M, N, dst, ds.ld, out_esize, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+        if (!plan_note("stage_c") && launch_repack(C, ldc, M, N, dst, ds.ld, out_esize, dev->sm_count, s) != cudaSuccess)
+          return TTC_ERR_CUDA;
         g_launches.fetch_add(1);
       }
       st = gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, beta != 0.0f ? dst : nullptr, ds.ld, dst, ds.ld,
                      alpha, beta, bias, act, dtype, nullptr, 0, stream);
       if (st != TTC_OK) return st;
-      if (launch_unpack(dst, ds.ld, M, N, D, ldd, out_esize, dev->sm_count, s) != cudaSuccess) return TTC_ERR_CUDA;
+      if (!plan_note("unstage_d") && launch_unpack(dst, ds.ld, M, N, D, ldd, out_esize, dev->sm_count, s) != cudaSuccess)
+        return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       return TTC_OK;
     }
@@ -1102,13 +1154,18 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
           if (cl12 < 0) cl12 = pair_max_clusters_ew12(bf16);
         }
         if (cl12 >= nclus) {
-          if (launch_pair_ew12(bf16, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+          if (!plan_note("pair bn=256 ew=12 clusters=%d tiles=%d units=%d d_tma=0", nclus, prm.num_tiles,
+                         prm.num_units) &&
+              launch_pair_ew12(bf16, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return TTC_ERR_CUDA;
           g_launches.fetch_add(1);
           return TTC_OK;
         }
       }
-      if (launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TTC_ERR_CUDA;
+      if (!plan_note("pair bn=%d ew=8 clusters=%d tiles=%d units=%d d_tma=%d", pbn, nclus, prm.num_tiles,
+                     prm.num_units, prm.d_tma) &&
+          launch_pair(bf16, pbn, prm, nclus, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TTC_ERR_CUDA;
       g_launches.fetch_add(1);
       return TTC_OK;
     }
@@ -1118,7 +1175,10 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   prm.b_stream = prm.num_m_blocks == 1;
   const int max_clusters = dev->sm_count / ksplit > 0 ? dev->sm_count / ksplit : 1;
   const int clusters = prm.num_tiles < max_clusters ? prm.num_tiles : max_clusters;
-  if (launch(mode, bn, prm, clusters * ksplit, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  if (!plan_note("single mode=%s bn=%d ksplit=%d swap=%d grid=%d tiles=%d d_tma=%d a_vec=%d b_vec=%d",
+                 mode_name(mode), bn, ksplit, swap ? 1 : 0, clusters * ksplit, prm.num_tiles, prm.d_tma,
+                 prm.a_vec, prm.b_vec) &&
+      launch(mode, bn, prm, clusters * ksplit, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return TTC_ERR_CUDA;
   g_launches.fetch_add(1);
   return TTC_OK;
@@ -1146,6 +1206,37 @@ ttc_status ttc_gemm_strided_batched(int64_t batch, int64_t M, int64_t N, int64_t
                                     const float* bias, ttc_act act, ttc_dtype dtype, void* stream) {
   return gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act, dtype, nullptr,
                    0, stream, batch, strideA, strideB, strideC, strideD);
+}
+
+ttc_status ttc_gemm_plan(int64_t batch, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,
+                         int64_t strideA, ttc_layout layoutA, const void* B, int64_t ldb, int64_t strideB,
+                         ttc_layout layoutB, const void* C, int64_t ldc, int64_t strideC, void* D, int64_t ldd,
+                         int64_t strideD, float alpha, float beta, const float* bias, ttc_act act, ttc_dtype dtype,
+                         void* workspace, size_t workspace_bytes, int sm_count, char* out, size_t out_len) {
+  if (sm_count < 2 || sm_count > 4096 || (out == nullptr && out_len > 0)) return TTC_ERR_INVALID_ARG;
+  std::string plan;
+  t_plan_dev = DeviceInfo();
+  t_plan_dev.ready = true;
+  t_plan_dev.sm_count = sm_count;
+  // one CTA pair (or one twelve-warp pair, or one halo pair) per two SMs
+  const int pairs = sm_count / 2;
+  for (auto& row : t_plan_dev.pair_clusters)
+    for (int& v : row) v = pairs;
+  for (auto& row : t_plan_dev.halo_clusters)
+    for (int& v : row) v = pairs;
+  t_plan_dev.pair_clusters_i8 = pairs;
+  t_plan_dev.pair_clusters_ew12[0] = t_plan_dev.pair_clusters_ew12[1] = pairs;
+  t_plan = &plan;
+  const ttc_status st = gemm_impl(M, N, K, A, lda, layoutA, B, ldb, layoutB, C, ldc, D, ldd, alpha, beta, bias, act,
+                                  dtype, workspace, workspace_bytes, nullptr, batch, strideA, strideB, strideC,
+                                  strideD);
+  t_plan = nullptr;
+  if (out_len > 0) {
+    const size_t n = plan.size() < out_len - 1 ? plan.size() : out_len - 1;
+    std::memcpy(out, plan.data(), n);
+    out[n] = '\0';
+  }
+  return st;
 }
 
 ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t K, int64_t R, int64_t S,
