@@ -216,3 +216,66 @@ def test_random_problems_are_planned_and_keep_the_kernels_rules():
     # the sweep reaches every kind of launch
     for k in ("pair", "single", "repack", "gemv_rows", "gemv_cols", "stage_c", "unstage_d", "widen_i8", "pair_i8"):
         assert counts.get(k, 0) > 0, (k, counts)
+
+
+# ------------------------------------------------------------------ knobs and workspaces
+
+@pytest.fixture
+def knob():
+    set_ = []
+
+    def f(name, value):
+        ttc.ttc_set_knob(name, value)
+        set_.append(name)
+    yield f
+    for name in set_:
+        ttc.ttc_set_knob(name, 0)
+
+
+def test_knobs_steer_the_plan(knob):
+    knob("pair", 2)
+    assert kernels(plan(8192, 8192, 8192)[1]) == ["single"]
+    knob("pair", 1)
+    assert kernels(plan(300, 300, 64)[1]) == ["pair"]
+    knob("pair", 0)
+    knob("pair_tile_n", 128)
+    assert plan(8192, 8192, 8192)[1][0]["bn"] == "128"
+    knob("pair_tile_n", 0)
+    knob("swap_ab", 1)
+    it = plan(300, 500, 64)[1]
+    assert it[0]["kernel"] == "single" and it[0]["swap"] == "1"
+    knob("swap_ab", 0)
+    knob("split_k", 4)
+    it = plan(256, 256, 4096)[1]
+    assert it[0]["ksplit"] == "4" and it[0]["grid"] == str(4 * int(it[0]["tiles"]))
+    knob("split_k", 0)
+    knob("gemv", 1)
+    assert kernels(plan(1, 4096, 4096)[1]) == ["single"]
+    knob("gemv", 0)
+    knob("force_generic_load", 1)
+    assert plan(1024, 1024, 1024)[1][0]["mode"] == "plain_bf16"
+    knob("force_generic_load", 0)
+    knob("force_generic_store", 1)
+    it = plan(1024, 1024, 1024)[1]
+    assert all(x.get("d_tma", "0") == "0" for x in it)
+    knob("force_generic_store", 0)
+    knob("pair_epi_warps", 8)
+    it = plan(4099, 3001, 1023, beta=1.0, workspace="staged")[1]
+    assert it[-1]["kernel"] == "pair" and it[-1]["ew"] == "8"
+
+
+def test_workspaces_decide_the_copies():
+    # odd pitches: nothing copied without a workspace, both operands with one
+    q = dict(M=2000, N=1500, K=300, lda=301, ldb=303, beta=1.0, ldc=1501, ldd=1503)
+    it = plan(**q)[1]
+    assert kernels(it) == ["single"] and it[0]["mode"] == "plain_bf16"  # the plain-load producer
+    it = plan(**q, workspace="repack")[1]
+    assert kernels(it) == ["repack", "pair"] and it[1]["d_tma"] == "0"  # TMA on the copies; D rows written directly
+    # int8 with an unaligned D: staged through an aligned copy (C copied in, D copied out)
+    q8 = dict(M=300, N=200, K=72, dtype="i8", lda=73, ldb=75, beta=1.0, ldd=203)
+    assert kernels(plan(**q8, workspace="staged")[1]) == ["repack", "stage_c", "single", "unstage_d"]
+    assert kernels(plan(**q8, workspace="repack")[1]) == ["repack", "single"]
+    # a 16-bit D is never staged: its rows are written at any alignment
+    assert "unstage_d" not in kernels(plan(**q, workspace="staged")[1])
+    # matrix-vector problems need no workspace at all
+    assert kernels(plan(1, 4096, 4096, ldb=4097, workspace="staged")[1]) == ["gemv_rows"]
