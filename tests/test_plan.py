@@ -194,7 +194,14 @@ def test_random_problems_are_planned_and_keep_the_kernels_rules():
                     ok_pitch = (ad["ldd"] * oes) % 16 == 0 or q["M"] == 1
                     assert ad["D"] % 16 == 0 and ok_pitch, (q, it)
                     assert q["batch"] == 1 or (q["strides"][3] * oes) % 16 == 0, (q, it)
+            if it["kernel"] in ("pair", "pair_i8"):
+                assert int(it["clusters"]) <= SMS // 2 and int(it["units"]) >= int(it["tiles"]), (q, it)
+            if it.get("d_tma") == "1":
+                # TMA stores whole 16-byte granules only: a row needs at least one
+                assert q["N"] * oes >= 16, (q, it)
             if it["kernel"] == "single":
+                assert int(it["grid"]) <= SMS and it["ksplit"] in ("1", "2", "4", "8"), (q, it)
+                assert it["ksplit"] == "1" or int(it["bn"]) <= 128, (q, it)
                 swap = it["swap"] == "1"
                 assert not (swap and it.get("d_tma") == "1"), (q, it)
                 if it["mode"].startswith("tma") and not repacked:
