@@ -45,7 +45,7 @@
  *     beta != 0; D overlapping C other than exactly in place (D == C and
  *     ldd == ldc); an unknown enum value.
  *   TTC_ERR_UNSUPPORTED: TTC_I8 with bias, act != NONE, alpha != 1 or beta
- *     not in {0, 1}; a size or leading dimension beyond 2^31 - 1 elements.
+ *     not in {0, 1}; a size or leading dimension beyond 2^31 - 2^24 elements.
  *   TTC_ERR_CUDA: a CUDA runtime or driver call failed (launch, device query).
  *   TTC_ERR_TIMEOUT: returned by ttc_get_device_error when a kernel's bounded
  *     wait ran out; the kernel then ended early and D is undefined.

@@ -286,3 +286,18 @@ def test_workspaces_decide_the_copies():
     assert "unstage_d" not in kernels(plan(**q, workspace="staged")[1])
     # matrix-vector problems need no workspace at all
     assert kernels(plan(1, 4096, 4096, ldb=4097, workspace="staged")[1]) == ["gemv_rows"]
+
+
+def test_sizes_near_two_to_the_31_are_refused_before_any_loop_could_wrap():
+    """The kernels count rows, columns and k in 32-bit integers and step past
+    the end by up to a grid's stride before testing a loop bound, so sizes
+    within 2^24 of 2^31 are refused; just below the limit a matrix-vector
+    problem (the kernel whose loops stride furthest) is planned."""
+    lim = (1 << 31) - (1 << 24)
+    for kw in (dict(M=1, N=lim + 1, K=16), dict(M=1, N=4096, K=lim + 1, lb="col"), dict(M=lim + 1, N=1, K=16),
+               dict(M=64, N=64, K=64, lda=lim + 1)):
+        assert plan(**kw)[0] == 2, kw
+    st, it, _ = plan(M=1, N=lim, K=16, lb="row")
+    assert st == 0 and kernels(it) == ["gemv_cols"]
+    st, it, _ = plan(M=1, N=4096, K=lim, lb="col")
+    assert st == 0 and kernels(it) == ["gemv_rows"]

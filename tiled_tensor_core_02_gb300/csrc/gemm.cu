@@ -52,6 +52,11 @@ std::atomic<int64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
 
+// Largest size or leading dimension accepted (elements): the kernels index
+// rows, columns and k in 32-bit integers and step past the end by up to a
+// grid's stride (well under 2^24) before a loop test, which must not wrap.
+constexpr int64_t kSizeLimit = (1ll << 31) - (1ll << 24);
+
 struct DeviceInfo {
   bool ready = false;
   int sm_count = 0;
@@ -778,7 +783,7 @@ static ttc_status gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, int6
   if (dtype == TTC_I8 &&
       (bias != nullptr || act != TTC_ACT_NONE || alpha != 1.0f || (beta != 0.0f && beta != 1.0f)))
     return TTC_ERR_UNSUPPORTED;
-  const int64_t lim = 0x7FFFFFFFll;
+  const int64_t lim = kSizeLimit;
   if (M > lim || N > lim || K > lim || lda > lim || ldb > lim || ldc > lim || ldd > lim || batch > 65535)
     return TTC_ERR_UNSUPPORTED;
   const int in_esize = dtype == TTC_I8 ? 1 : 2;
@@ -1260,7 +1265,7 @@ ttc_status ttc_conv2d_fprop(int64_t N, int64_t H, int64_t W, int64_t C, int64_t 
   if (span_h < 0 || span_w < 0) return TTC_ERR_INVALID_ARG;  // the filter does not fit the padded input
   const int64_t P = span_h / stride_h + 1, Q = span_w / stride_w + 1;
   if (N == 0 || K == 0) return TTC_OK;
-  const int64_t lim = 0x7FFFFFFFll;
+  const int64_t lim = kSizeLimit;
   if (N > lim / (P * Q) || N > lim / (H * W) || C > lim / (R * S) || K > lim || ldd > lim || ldc > lim)
     return TTC_ERR_UNSUPPORTED;
   const int64_t M = N * P * Q, Kg = R * S * C;
