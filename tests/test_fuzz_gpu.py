@@ -10,7 +10,9 @@ width, orientation, split K, matrix-vector kernels) from each shape.  Then
 random strided batches (gaps between batches, a shared B), random
 convolutions (filter sizes, padding, strides, dilations, channel counts on
 and off the 64-channel blocks, an unaligned input, a padded output pitch),
-random transposes (every element size, tight, odd and 16-byte pitches), and
+larger random convolutions on the CTA-pair paths (halo tiles for unit
+strides, im2col loads otherwise), random transposes (every element size,
+tight, odd and 16-byte pitches), and
 GEMMs whose A, B, C and D start at element offsets off every alignment,
 through each entry point including the static-scratch one (nothing outside
 D's elements written).  The pitch padding of A, B and C, and the elements
@@ -287,3 +289,42 @@ def test_random_offsets_match_oracle(case):
     ok, worst, w = oracle.check_float(oracle.decode(np.ascontiguousarray(d).ravel(), dtype), r.ravel(),
                                       sabs.ravel(), dtype)
     assert ok, f"worst error ratio {worst:.3f} at {divmod(w, N)}"
+
+
+# ---------------------------------------------------------------- larger convolutions (the CTA-pair paths)
+def _large_conv_cases(n=30, seed=77):
+    """Whole 64-channel blocks and at least 128 filters on outputs of a few
+    hundred pixels: unit strides take the halo kernel, other strides the
+    im2col loads on the CTA-pair kernel."""
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        N = int(rng.integers(1, 5))
+        H, W = int(rng.integers(8, 41)), int(rng.integers(8, 41))
+        C = int(rng.choice([64, 128, 192]))
+        K = int(rng.choice([128, 160, 256, 320]))
+        R, S = int(rng.choice([1, 3, 5])), int(rng.choice([1, 3, 5]))
+        pad = (int(rng.integers(0, 3)), int(rng.integers(0, 3)))
+        stride = (int(rng.choice([1, 1, 2, 3])), int(rng.choice([1, 1, 2, 3])))
+        dil = (int(rng.choice([1, 1, 2])), int(rng.choice([1, 1, 2])))
+        if H + 2 * pad[0] - dil[0] * (R - 1) - 1 < 0 or W + 2 * pad[1] - dil[1] * (S - 1) - 1 < 0:
+            continue
+        dtype = str(rng.choice(["bf16", "f16"]))
+        beta = float(rng.choice([0.0, 1.0]))
+        act = str(rng.choice(["none", "relu", "gelu_tanh"]))
+        out.append((len(out), N, H, W, C, K, R, S, pad, stride, dil, dtype, beta, act))
+    return out
+
+
+@pytest.mark.parametrize("case", _large_conv_cases(),
+                         ids=lambda c: f"{c[0]}-{c[11]}-n{c[1]}h{c[2]}w{c[3]}c{c[4]}k{c[5]}r{c[6]}s{c[7]}")
+def test_random_larger_convolution_matches_oracle(case):
+    from test_conv_gpu import run_conv
+    i, N, H, W, C, K, R, S, pad, stride, dil, dtype, beta, act = case
+    cp = synth.ConvProblem(N, H, W, C, K, R, S, pad, stride, dil, dtype=dtype, seed=500 + i, with_c=beta != 0.0,
+                           dist_bias="uniform")
+    out = run_conv(cp, alpha=1.0, beta=beta, act=act)
+    r, sabs = oracle.conv_full(cp, alpha=1.0, beta=beta, act=act)
+    d = oracle.decode(out.reshape(-1)[:cp.M * K].reshape(cp.M, K), dtype)
+    ok, worst, w = oracle.check_float(d.ravel(), r.ravel(), sabs.ravel(), dtype)
+    assert ok, f"worst error ratio {worst:.3f} at {divmod(w, K)}"
