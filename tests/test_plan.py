@@ -220,6 +220,13 @@ def test_random_problems_are_planned_and_keep_the_kernels_rules():
                                             lines=_lines(q, op)), (q, it)
         if q["workspace"] is None:
             assert not repacked and not staged, (q, items)
+        if staged:
+            assert q["dtype"] == "i8" and q["workspace"] == "staged", (q, items)  # only int32 D is staged
+        if names[0].startswith("gemv"):
+            assert q["dtype"] != "i8" and q["batch"] == 1 and (q["M"] == 1 or q["N"] == 1), (q, items)
+            assert len(items) == 1, (q, items)  # no workspace copies for matrix-vector problems
+        if "pair" in names or "pair_i8" in names:
+            assert q["M"] >= 256 and q["N"] >= 256, (q, items)
     # the sweep reaches every kind of launch
     for k in ("pair", "single", "repack", "gemv_rows", "gemv_cols", "stage_c", "unstage_d", "widen_i8", "pair_i8"):
         assert counts.get(k, 0) > 0, (k, counts)
