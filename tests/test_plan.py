@@ -12,10 +12,17 @@ import numpy as np
 import pytest
 
 import tiled_tensor_core_02_gb300 as ttc
+from tiled_tensor_core_02_gb300 import _build
 
 R, COL = ttc.ROW_MAJOR, ttc.COL_MAJOR
 BASE = 1 << 36  # fake, widely spaced device addresses: only their alignment matters
 SMS = 152
+
+
+@pytest.fixture(autouse=True, scope="module")
+def built():
+    _build.build()  # nvcc cross-compiles here; nothing below touches a GPU
+    ttc.load()
 
 
 def plan(M, N, K, dtype="bf16", la="row", lb="col", lda=None, ldb=None, ldc=None, ldd=None, beta=0.0,
