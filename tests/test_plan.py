@@ -315,3 +315,43 @@ def test_sizes_near_two_to_the_31_are_refused_before_any_loop_could_wrap():
     assert st == 0 and kernels(it) == ["gemv_cols"]
     st, it, _ = plan(M=1, N=4096, K=lim, lb="col")
     assert st == 0 and kernels(it) == ["gemv_rows"]
+
+
+def test_reported_workspace_sizes_are_enough_and_needed():
+    """For random problems whose operands TMA cannot read: with exactly the
+    size ttc_gemm_workspace_size reports the plan repacks them, with one byte
+    less it does not (the plain-load producer reads them in place); the
+    staged size adds D's aligned copy for int32 outputs alike."""
+    rng = np.random.default_rng(20261208)
+    checked = staged_checked = 0
+    lay = {"row": R, "col": COL}
+    for _ in range(400):
+        dtype = str(rng.choice(["bf16", "i8"]))
+        M, N, K = (int(rng.integers(2, 3000)) for _ in range(3))
+        la, lb = str(rng.choice(["row", "col"])), str(rng.choice(["row", "col"]))
+        lda = (K if la == "row" else M) + int(rng.choice([1, 3]))
+        ldb = (N if lb == "row" else K) + int(rng.choice([0, 1]))
+        ldd = N + int(rng.choice([0, 1, 3]))
+        es, oes = (1, 4) if dtype == "i8" else (2, 2)
+        A, B, D = BASE, 2 * BASE, 4 * BASE
+        dt = ttc.DTYPE[dtype]
+        need = ttc.ttc_gemm_workspace_size(M, N, K, A, lda, lay[la], B, ldb, lay[lb], dt)
+        need_st = ttc.ttc_gemm_workspace_size_staged(M, N, K, A, lda, lay[la], B, ldb, lay[lb], D, ldd, dt)
+        assert need_st >= need
+
+        def names(ws):
+            st, text = ttc.ttc_gemm_plan(1, M, N, K, A, lda, 0, lay[la], B, ldb, 0, lay[lb], None, N, 0, D, ldd, 0,
+                                         1.0, 0.0, None, 0, dt, 5 * BASE if ws else None, ws, SMS)
+            assert st == 0
+            return [it.split()[0] for it in text.split("; ") if it]
+        if need == 0:
+            continue  # a matrix-vector problem, or nothing to repack
+        checked += 1
+        with_ws = names(need)
+        if "widen_i8" not in with_ws:
+            assert with_ws[0] == "repack", (dtype, M, N, K, la, lb, lda, ldb, with_ws)
+        assert "repack" not in names(need - 1)
+        if need_st > need and "widen_i8" not in names(need_st):
+            staged_checked += 1
+            assert "unstage_d" in names(need_st) and "unstage_d" not in names(need_st - 1)
+    assert checked > 300 and staged_checked > 50, (checked, staged_checked)
